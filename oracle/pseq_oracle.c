@@ -223,7 +223,8 @@ int oracle_thd_padding_mask(int64_t total_tokens, const int64_t* valid_seq_lens,
  *   other slot of the [num_bins, width] output holds pad_value and is marked
  *   1 in padding_mask.  A bin whose padded total exceeds capacity or width
  *   is ORC_CAPACITY; an empty bin, a member index outside [0,N), or a real
- *   length outside [0,W] is ORC_VALUE.
+ *   length outside [0,W] is ORC_VALUE.  Malformed input is reported before
+ *   any capacity problem, wherever in the bin list each one sits.
  * Per-bin cu arrays are stored one after the other: bin b starts at
  *   bin_offsets[b] + b and has (members of b) + 1 entries.
  * *max_total receives the largest padded total over bins before stretching.
@@ -239,11 +240,22 @@ int oracle_pack_squeeze(const void* src, int64_t N, int64_t W, int elem_bytes,
   unsigned char* o = (unsigned char*)out;
   unsigned char pad_bytes[8];
   memcpy(pad_bytes, &pad_value, 8); /* low-order bytes, little-endian */
-  int64_t widest = 0;
+  /* Pass 1: the input must be well formed. */
   for (int64_t b = 0; b < num_bins; ++b) {
     int64_t first = bin_offsets[b];
     int64_t count = (int64_t)bin_offsets[b + 1] - first;
     if (count <= 0) return ORC_VALUE;
+    for (int64_t k = 0; k < count; ++k) {
+      int64_t i = bin_members[first + k];
+      if (i < 0 || i >= N) return ORC_VALUE;
+      if (real_lens[i] < 0 || real_lens[i] > W) return ORC_VALUE;
+    }
+  }
+  /* Pass 2: lay each bin out. */
+  int64_t widest = 0;
+  for (int64_t b = 0; b < num_bins; ++b) {
+    int64_t first = bin_offsets[b];
+    int64_t count = (int64_t)bin_offsets[b + 1] - first;
     int32_t* bcu = cu + first + b;
     int32_t* bcup = cu_padded + first + b;
     /* fill the whole output row with padding first */
@@ -257,9 +269,7 @@ int oracle_pack_squeeze(const void* src, int64_t N, int64_t W, int elem_bytes,
     bcup[0] = 0;
     for (int64_t k = 0; k < count; ++k) {
       int64_t i = bin_members[first + k];
-      if (i < 0 || i >= N) return ORC_VALUE;
       int64_t real = real_lens[i];
-      if (real < 0 || real > W) return ORC_VALUE;
       int64_t padded = ((real + multiple - 1) / multiple) * multiple;
       if (run_padded + padded > capacity) return ORC_CAPACITY;
       if (run_padded + padded > width) return ORC_CAPACITY;

@@ -319,6 +319,13 @@ def pin_squeeze_errors(lib):
         raise AssertionError("width overflow not reported")
     except oracle.OracleCapacityError:
         pass
+    # malformed input is reported ahead of a capacity problem in an earlier bin
+    offs, mem = oracle.bins_to_csr([[0], [1, 5]])
+    try:
+        oracle.pack_squeeze(np.zeros((3, 8), np.int64), np.array([8, 1, 1]), offs, mem, 4, 4, False, 16, lib=lib)
+        raise AssertionError("malformed bin not reported")
+    except oracle.OracleValueError:
+        pass
     for lens, bins in ((np.array([9, 1]), [[0, 1]]), (np.array([-1, 1]), [[0, 1]]),
                        (np.array([1, 1]), [[0], []]), (np.array([1, 1]), [[0, 2]])):
         offs, mem = oracle.bins_to_csr(bins)

@@ -1,0 +1,438 @@
+"""CUDA path against the CPU oracle, element by element (tolerance 0: all of
+this work is integer, index or bit-copy work).
+
+Every call goes through the C ABI of libpseq.so (ctypes binding).  Sizes
+span several tiles with ragged tails; the five workloads run at full size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from varlen_attention_metadata_gb300 import build
+
+    build.build()
+    import varlen_attention_metadata_gb300 as v
+
+    v.load_library()
+    yield
+
+
+def V():
+    import varlen_attention_metadata_gb300 as v
+
+    return v
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def info_of(block):
+    return tuple(block[:16].view(torch.int32).tolist())
+
+
+CANARY = 0x5A
+
+
+# --------------------------------------------------------------------------
+# pseq_from_doc_ids
+# --------------------------------------------------------------------------
+def run_doc_ids(d: np.ndarray, offset_elems: int = 0):
+    """Run the scan; optionally place doc_ids at an element offset so the
+    pointer is not 16-byte aligned.  Returns (cu, info, canary_ok)."""
+    v = V()
+    B, S = d.shape
+    flat = torch.zeros(B * S + offset_elems, dtype=torch.int32 if d.dtype == np.int32 else torch.int64, device=DEV)
+    src = flat[offset_elems:]
+    src.copy_(torch.from_numpy(d.reshape(-1)))
+    src = src.view(B, S)
+    guard = 16
+    cu_full = torch.full((B * S + 1 + 2 * guard,), CANARY, dtype=torch.int32, device=DEV)
+    cu = cu_full[guard:guard + B * S + 1]
+    _, info = v.pseq_from_doc_ids(src, cu_seqlens=cu)
+    st, count, mx, total = info_of(info)
+    host = cu_full.cpu().numpy()
+    canary_ok = (np.all(host[:guard] == CANARY) and np.all(host[guard + count + 1:] == CANARY))
+    return host[guard:guard + count + 1], (st, count, mx, total), canary_ok
+
+
+def check_doc_ids(d, offset_elems=0):
+    cu, (st, count, mx, total), canary_ok = run_doc_ids(d, offset_elems)
+    ref_cu, ref_mx = oracle.from_doc_ids(d)
+    assert st == 0
+    assert canary_ok, "write outside cu_seqlens[0 .. num_segments]"
+    assert count == len(ref_cu) - 1
+    np.testing.assert_array_equal(cu, ref_cu)
+    assert mx == ref_mx
+    assert total == d.size
+
+
+def test_doc_ids_page_example():
+    check_doc_ids(np.array([[1, 1, 2, 2, 2, 0]], np.int32))
+
+
+@pytest.mark.parametrize("kind", ["runs", "iid", "zeros", "const", "alternating", "long"])
+@pytest.mark.parametrize("dtype", [np.int32, np.int64])
+def test_doc_ids_random(kind, dtype):
+    rng = np.random.default_rng(7)
+    shapes = [(1, 1), (1, 7), (3, 1), (2, 5), (5, 4096), (3, 4097), (7, 1500), (1, 3 * 4096 + 123),
+              (13, 2049), (40, 1)]
+    for B, S in shapes:
+        d = synth.random_doc_ids(rng, B, S, kind, dtype)
+        check_doc_ids(d)
+        check_doc_ids(d, offset_elems=1)  # unaligned pointer: scalar load path
+
+
+def test_doc_ids_many_tiles_chain():
+    """Hundreds of tiles, so the look-back crosses many 32-tile windows."""
+    rng = np.random.default_rng(11)
+    d = synth.random_doc_ids(rng, 9, 200_003, "runs", np.int32)
+    check_doc_ids(d)
+    d = synth.random_doc_ids(rng, 2, 700_001, "long", np.int32)  # tiles with no boundary at all
+    check_doc_ids(d)
+
+
+def test_doc_ids_empty():
+    v = V()
+    for shape in ((0, 5), (4, 0)):
+        d = torch.zeros(shape, dtype=torch.int32, device=DEV)
+        p = v.packed_seq_params_from_doc_ids(d)
+        assert p.cu_seqlens.tolist() == [0] and p.max_seqlen == 0
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_doc_ids_small_map_workload(seed):
+    check_doc_ids(synth.doc_map_small(seed)["doc_ids"])
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_doc_ids_stress_map_workload(seed):
+    check_doc_ids(synth.doc_map_stress(seed))
+
+
+def test_doc_ids_workspace_is_left_clean():
+    """Back-to-back calls of different sizes on one cached workspace."""
+    rng = np.random.default_rng(3)
+    for S in (50_000, 4096 * 5, 999, 120_000, 7):
+        check_doc_ids(synth.random_doc_ids(rng, 3, S, "runs", np.int32))
+
+
+def test_packed_seq_params_api():
+    v = V()
+    d = torch.tensor([[1, 1, 2, 2, 2, 0]], dtype=torch.int32, device=DEV)
+    p = v.packed_seq_params_from_doc_ids(d)
+    assert p.cu_seqlens.dtype == torch.int32 and p.cu_seqlens.tolist() == [0, 2, 5, 6]
+    assert p.max_seqlen == 3 and p.doc_ids is d
+    kw = v.to_flash_attention_kwargs(p)
+    assert kw["cu_seq_lens_q"] is kw["cu_seq_lens_k"] is p.cu_seqlens
+    assert kw["max_length_q"] == kw["max_length_k"] == 3
+
+
+# --------------------------------------------------------------------------
+# process_input_for_thd / thd_from_batch
+# --------------------------------------------------------------------------
+def check_thd(batch_np: dict, absorb=True, with_padded=True, hidden=None):
+    """Run thd_from_batch on every field of the batch and compare all outputs."""
+    v = V()
+    real = batch_np["seq_lens"]
+    padded = batch_np["seq_lens_padded"] if with_padded else None
+    ids = batch_np["input_ids"]
+    B, S = ids.shape[:2]
+    fields_np = [(ids, 1)]
+    if "labels" in batch_np:
+        fields_np.append((batch_np["labels"], 1))
+    if "position_ids" in batch_np:
+        pos = batch_np["position_ids"]
+        fields_np.append((pos, pos.shape[0] if pos.ndim == 3 else 1))
+    fields_t = [(dev(a), p) for a, p in fields_np]
+    if hidden is not None:
+        fields_t.append((hidden, 1))
+    r = v.thd_from_batch(dev(real), None if padded is None else dev(padded), S, fields_t, -1000, absorb)
+    st, n, mx, T = info_of(r["info"])
+    try:
+        meta = oracle.thd_meta(real, padded, S, -1000, absorb)
+    except oracle.OracleValueError:
+        assert st == 3, f"device status {st}, oracle raised VALUE"
+        return None
+    assert st == 0
+    assert n == meta["num_sequences"] and T == meta["total_tokens"] and mx == meta["max_seqlen"]
+    np.testing.assert_array_equal(r["cu_seqlens"][: n + 1].cpu().numpy(), meta["cu_seqlens"])
+    if padded is not None:
+        np.testing.assert_array_equal(r["cu_seqlens_padded"][: n + 1].cpu().numpy(), meta["cu_seqlens_padded"])
+    assert bool(r["info"][16].item()) == meta["pad_between_seqs"]
+    for (a, planes), (dst, _, _) in zip(fields_np, r["dst"]):
+        want = oracle.thd_gather(a, meta, B, S, planes=planes)
+        got = dst[: want.size].cpu().numpy().reshape(want.shape)
+        np.testing.assert_array_equal(got, want)
+    if hidden is not None:
+        h = hidden.cpu().view(torch.int16).numpy()
+        want = oracle.thd_gather(h, meta, B, S)
+        got = r["dst"][-1][0][: want.size].cpu().view(torch.int16).numpy().reshape(want.shape)
+        np.testing.assert_array_equal(got, want)
+    mask_ref = oracle.thd_padding_mask(T, meta["seq_real"], meta["seq_padded"] if padded is not None else None)
+    np.testing.assert_array_equal(r["padding_mask"][:T].cpu().numpy(), mask_ref)
+    return r
+
+
+def test_thd_page_example():
+    import json
+    import os
+
+    with open(os.path.join(os.path.dirname(__file__), "golden", "thd_utils_process_input_example.json")) as f:
+        g = json.load(f)
+    batch = {k: np.asarray(v, np.int64) for k, v in g["batch"].items()}
+    check_thd(batch)
+    v = V()
+    out = v.process_input_for_thd({k: dev(a) for k, a in batch.items()} | {"qkv_format": "thd"})
+    e = g["expected"]
+    for k in ("input_ids", "labels", "position_ids", "cu_seqlens", "cu_seqlens_padded"):
+        assert out[k].tolist() == e[k], k
+    assert int(out["max_seqlen"]) == e["max_seqlen"] and out["max_seqlen"].dtype == torch.int32
+    assert out["padding_mask"].tolist() == e["padding_mask"]
+    assert out["pad_between_seqs"] == e["pad_between_seqs"]
+    assert out["qkv_format"] == "thd"
+    assert out["cu_seqlens"].dtype == torch.int32
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_thd_random(seed):
+    rng = np.random.default_rng(500 + seed)
+    for trial in range(6):
+        B = int(rng.integers(1, 6))
+        S = int(rng.integers(1, 3000))
+        P = int(rng.integers(1, 40))
+        real, padded = synth.random_thd(rng, B, S, P, multiple=int(rng.choice([1, 4, 64])),
+                                        interleave_filler=bool(trial % 2), fill_rows=bool(trial % 3 == 0),
+                                        with_zero_lengths=True)
+        batch = {
+            "input_ids": rng.integers(0, 32000, size=(B, S)).astype(np.int64),
+            "labels": rng.integers(0, 32000, size=(B, S)).astype(np.int64),
+            "position_ids": rng.integers(0, 1 << 40, size=(3, B, S)).astype(np.int64),
+            "seq_lens": real,
+            "seq_lens_padded": padded,
+        }
+        H = int(rng.choice([1, 5, 8, 64]))
+        hidden = torch.randn(B, S, H, device=DEV).to(torch.bfloat16)
+        check_thd(batch, absorb=bool(trial % 2 == 0), with_padded=trial != 5, hidden=hidden)
+
+
+def test_thd_field_widths():
+    """1-, 2-, 4- and 8-byte elements with odd row widths (unaligned rows)."""
+    rng = np.random.default_rng(42)
+    B, S, P = 3, 777, 9
+    real, padded = synth.random_thd(rng, B, S, P, multiple=3)
+    v = V()
+    arrays = [rng.integers(-100, 100, size=(B, S, 3)).astype(np.int8),
+              rng.integers(-3000, 3000, size=(B, S, 7)).astype(np.int16),
+              rng.integers(-10 ** 9, 10 ** 9, size=(2, B, S, 5)).astype(np.int32),
+              rng.integers(-10 ** 12, 10 ** 12, size=(B, S, 3)).astype(np.int64)]
+    planes = [1, 1, 2, 1]
+    r = v.thd_from_batch(dev(real), dev(padded), S, [(dev(a), p) for a, p in zip(arrays, planes)])
+    st, n, mx, T = info_of(r["info"])
+    assert st == 0
+    meta = oracle.thd_meta(real, padded, S)
+    for a, p, (dst, _, _) in zip(arrays, planes, r["dst"]):
+        want = oracle.thd_gather(a, meta, B, S, planes=p)
+        np.testing.assert_array_equal(dst[: want.size].cpu().numpy().reshape(want.shape), want)
+
+
+def test_thd_errors():
+    cases = [
+        (np.array([[3, -1000]]), np.array([[3, 4]])),
+        (np.array([[3, 2]]), np.array([[2, 2]])),
+        (np.array([[-2, 2]]), np.array([[-2, 2]])),
+        (np.array([[5, 3]]), np.array([[5, 4]])),
+    ]
+    for real, padded in cases:
+        batch = {"input_ids": np.arange(8, dtype=np.int64).reshape(1, 8), "seq_lens": real, "seq_lens_padded": padded}
+        assert check_thd(batch) is None
+    v = V()
+    with pytest.raises(ValueError):
+        v.process_input_for_thd({"input_ids": dev(np.zeros((1, 8), np.int64)), "seq_lens": dev(cases[1][0]),
+                                 "seq_lens_padded": dev(cases[1][1])})
+
+
+def test_thd_filler_only_and_empty():
+    batch = {"input_ids": np.zeros((2, 6), np.int64), "seq_lens": np.full((2, 3), -1000, np.int64),
+             "seq_lens_padded": np.full((2, 3), -1000, np.int64)}
+    r = check_thd(batch)
+    assert info_of(r["info"])[1] == 0
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_thd_small_map_workload(seed):
+    c = synth.doc_map_small(seed)
+    check_thd({k: c[k] for k in ("input_ids", "labels", "position_ids", "seq_lens", "seq_lens_padded")})
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_thd_ids_workload(seed):
+    check_thd(synth.thd_ids(seed))
+
+
+def test_thd_embeddings_workload():
+    c = synth.thd_embeddings(0)
+    hidden = c["hidden"].to(DEV)
+    v = V()
+    B, S, H = hidden.shape
+    r = v.thd_from_batch(dev(c["seq_lens"]), dev(c["seq_lens_padded"]), S, [(hidden, 1)])
+    st, n, mx, T = info_of(r["info"])
+    meta = oracle.thd_meta(c["seq_lens"], c["seq_lens_padded"], S)
+    assert st == 0 and n == meta["num_sequences"] and T == meta["total_tokens"] and mx == meta["max_seqlen"]
+    np.testing.assert_array_equal(r["cu_seqlens"][: n + 1].cpu().numpy(), meta["cu_seqlens"])
+    np.testing.assert_array_equal(r["cu_seqlens_padded"][: n + 1].cpu().numpy(), meta["cu_seqlens_padded"])
+    want = oracle.thd_gather(c["hidden"].view(torch.int16).numpy(), meta, B, S)
+    got = r["dst"][0][0][: T * H].view(torch.int16).cpu().numpy().reshape(T, H)
+    np.testing.assert_array_equal(got, want)
+    mask_ref = oracle.thd_padding_mask(T, meta["seq_real"], meta["seq_padded"])
+    np.testing.assert_array_equal(r["padding_mask"][:T].cpu().numpy(), mask_ref)
+
+
+def test_thd_split_calls_match_whole():
+    v = V()
+    c = synth.thd_ids(3)
+    S = c["input_ids"].shape[1]
+    m = v.thd_meta(dev(c["seq_lens"]), dev(c["seq_lens_padded"]), S)
+    g = v.thd_gather(m, [(dev(c["input_ids"]), 1)])
+    st, n, mx, T = info_of(m["info"])
+    meta = oracle.thd_meta(c["seq_lens"], c["seq_lens_padded"], S)
+    np.testing.assert_array_equal(g["dst"][0][0][:T].cpu().numpy(), oracle.thd_gather(c["input_ids"], meta, 8, S))
+
+
+# --------------------------------------------------------------------------
+# _thd_padding_mask
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", range(4))
+def test_padding_mask_random(seed):
+    v = V()
+    rng = np.random.default_rng(900 + seed)
+    for _ in range(10):
+        n = int(rng.integers(0, 60))
+        real = rng.integers(0, 300, size=n).astype(np.int64)
+        padded = real + rng.integers(0, 70, size=n).astype(np.int64)
+        use_padded = bool(rng.integers(0, 2))
+        layout = int((padded if use_padded else real).sum())
+        total = layout + int(rng.integers(0, 500))
+        mask, info = v.thd_padding_mask(total, dev(real), dev(padded) if use_padded else None)
+        st, cnt, mx, tot = info_of(info)
+        ref = oracle.thd_padding_mask(total, real, padded if use_padded else None)
+        assert st == 0 and cnt == n and tot == total
+        np.testing.assert_array_equal(mask.cpu().numpy(), ref)
+
+
+def test_padding_mask_errors():
+    v = V()
+    for real, padded, total in ((np.array([3, 2]), np.array([4, 2]), 5), (np.array([3]), np.array([2]), 9),
+                                (np.array([-1]), None, 9)):
+        mask, info = v.thd_padding_mask(total, dev(real), None if padded is None else dev(padded))
+        assert info_of(info)[0] == 3
+        with pytest.raises(oracle.OracleValueError):
+            oracle.thd_padding_mask(total, real, padded)
+
+
+# --------------------------------------------------------------------------
+# squeeze
+# --------------------------------------------------------------------------
+def check_squeeze(prob, multiple, capacity, stretch, width, pad_value=0):
+    v = V()
+    src = prob["src"]
+    N, W = src.shape
+    r = v.pack_squeeze(dev(src), dev(prob["real_lens"]), (dev(prob["bin_offsets"]), dev(prob["bin_members"])),
+                       multiple, capacity, stretch, width, pad_value)
+    st, count, mx, total = info_of(r["info"])
+    try:
+        ref = oracle.pack_squeeze(src, prob["real_lens"], prob["bin_offsets"], prob["bin_members"], multiple,
+                                  capacity, stretch, width, pad_value)
+    except oracle.OracleCapacityError:
+        assert st == 4
+        return None
+    except oracle.OracleValueError:
+        assert st == 3
+        return None
+    assert st == 0
+    M = int(prob["bin_offsets"][-1])
+    nb = len(prob["bin_offsets"]) - 1
+    assert count == M and total == ref["max_total"]
+    assert mx == (int(prob["real_lens"][prob["bin_members"]].max()) if M else 0)
+    np.testing.assert_array_equal(r["packed"].cpu().numpy(), ref["packed"])
+    np.testing.assert_array_equal(r["padding_mask"].cpu().numpy(), ref["padding_mask"])
+    np.testing.assert_array_equal(r["cu_seqlens"][: M + nb].cpu().numpy(), ref["cu_flat"])
+    np.testing.assert_array_equal(r["cu_seqlens_padded"][: M + nb].cpu().numpy(), ref["cu_padded_flat"])
+    return r
+
+
+def test_squeeze_page_example():
+    import json
+    import os
+
+    with open(os.path.join(os.path.dirname(__file__), "golden", "who_packs_squeeze_example.json")) as f:
+        g = json.load(f)
+    offs, mem = oracle.bins_to_csr(g["bins"])
+    prob = {"src": np.asarray(g["rows"], np.int64), "real_lens": np.asarray(g["input_lengths"], np.int64),
+            "bin_offsets": offs, "bin_members": mem}
+    check_squeeze(prob, g["multiple"], g["capacity"], False, g["trainer"]["width"])
+    check_squeeze(prob, g["multiple"], g["capacity"], True, g["loader"]["width"])
+    v = V()
+    t = v.squeeze_bins(dev(prob["src"]), dev(prob["real_lens"]), g["bins"], g["multiple"], g["capacity"])
+    assert t["packed_input_ids"].tolist() == g["trainer"]["packed"]
+    assert t["cu_seqlens"][0].tolist() == g["trainer"]["cu_seqlens"]
+    assert t["cu_seqlens_padded"][0].tolist() == g["trainer"]["cu_seqlens_padded"]
+    lo = v.squeeze_bins(dev(prob["src"]), dev(prob["real_lens"]), g["bins"], g["multiple"], g["capacity"],
+                        stretch_to_capacity=True)
+    assert tuple(lo["packed_input_ids"].shape) == (1, g["loader"]["width"])
+    assert lo["cu_seqlens_padded"][0].tolist() == g["loader"]["cu_seqlens_padded"]
+
+
+@pytest.mark.parametrize("dtype", [np.int8, np.int16, np.int32, np.int64])
+def test_squeeze_random(dtype):
+    rng = np.random.default_rng(77)
+    for trial in range(12):
+        N = int(rng.integers(1, 40))
+        W = int(rng.integers(1, 300))
+        prob = synth.random_squeeze(rng, N, W, int(rng.integers(1, 8)), elem_dtype=dtype)
+        m = int(rng.choice([1, 3, 8, 64]))
+        need = max(sum(-(-int(prob["real_lens"][i]) // m) * m for i in b) for b in prob["bins"])
+        stretch = bool(trial % 2)
+        cap = need + int(rng.integers(0, 40))
+        width = cap if stretch else need + int(rng.integers(0, 5))
+        check_squeeze(prob, m, cap, stretch, width, pad_value=int(rng.integers(-5, 5)))
+
+
+def test_squeeze_workload():
+    c = synth.squeeze(0)
+    check_squeeze(c, c["multiple"], c["capacity"], c["stretch"], c["width"], c["pad_value"])
+
+
+def test_squeeze_errors():
+    rng = np.random.default_rng(5)
+    prob = synth.random_squeeze(rng, 6, 20, 2)
+    # capacity too small
+    assert check_squeeze(prob, 4, 3, False, 64) is None
+    # a member index out of range
+    bad = dict(prob)
+    bad["bin_members"] = prob["bin_members"].copy()
+    bad["bin_members"][0] = 99
+    assert check_squeeze(bad, 4, 1000, False, 1000) is None
+
+
+def test_squeeze_metadata_only_sizes_trainer_row():
+    v = V()
+    c = synth.squeeze(1)
+    r = v.pack_squeeze(dev(c["src"]), dev(c["real_lens"]), (dev(c["bin_offsets"]), dev(c["bin_members"])),
+                       c["multiple"], c["capacity"], False, None, 0, with_output=False)
+    st, count, mx, total = info_of(r["info"])
+    ref = oracle.pack_squeeze(c["src"], c["real_lens"], c["bin_offsets"], c["bin_members"], c["multiple"],
+                              c["capacity"], False, c["capacity"])
+    assert st == 0 and total == ref["max_total"]

@@ -1,0 +1,75 @@
+// Host-side state of libpseq: error text, launch counter, device properties,
+// bounded-wait settings.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace pseq {
+
+namespace {
+thread_local char g_last_error[512] = "";
+std::atomic<int64_t> g_launches{0};
+constexpr int64_t kDefaultWaitNs = 1000000000;  // 1 s
+std::atomic<int64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int64_t> g_withhold{-1};
+std::mutex g_dev_mu;
+int g_sm_count[64] = {0};
+}  // namespace
+
+pseq_status fail(pseq_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+void clear_error() { g_last_error[0] = '\0'; }
+
+pseq_status check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return PSEQ_OK;
+}
+
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (dev >= 64) {
+    int n = 1;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+  }
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+int64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+int64_t withhold_tile() { return g_withhold.load(std::memory_order_relaxed); }
+
+}  // namespace pseq
+
+extern "C" {
+
+int pseq_version(void) { return 100; }
+
+const char* pseq_last_error(void) { return pseq::g_last_error; }
+
+int64_t pseq_launch_count(void) { return pseq::g_launches.load(std::memory_order_relaxed); }
+
+void pseq_debug_set_wait(int64_t spin_limit_ns, int64_t withhold_tile) {
+  pseq::g_wait_ns.store(spin_limit_ns >= 0 ? spin_limit_ns : pseq::kDefaultWaitNs);
+  pseq::g_withhold.store(withhold_tile >= 0 ? withhold_tile : -1);
+}
+
+}  // extern "C"

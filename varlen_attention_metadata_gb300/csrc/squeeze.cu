@@ -1,0 +1,322 @@
+// pack_squeeze: the trainer-side squeeze of a padded rectangle into bins.
+//
+// Follows "Who packs the sequences: the loader, or the trainer?" (NeMo-RL
+// #4105 explainer): "Trainer packs" (sources padded to a multiple and laid
+// end to end; cu_seqlens from real lengths, cu_seqlens_padded from padded
+// lengths) and "Loader packs" (the last padded boundary stretched to the pack
+// capacity).
+//
+// squeeze_meta_kernel gives each bin one warp: a chunked warp scan over the
+// bin's members computes both cumulative sums, the slot where each member
+// starts, and the bin's checks.  squeeze_copy_kernel (programmatic dependent
+// launch) tiles every output row into equal chunks; a CTA finds the member
+// owning its first slot with a 32-way warp search and walks the members of
+// its chunk: real tokens are one contiguous block copy from the source row,
+// padding slots one block fill, and the padding mask is written alongside.
+// Every output slot is written exactly once.
+#include "common.cuh"
+
+namespace pseq {
+namespace {
+
+constexpr int kMetaThreads = 256;
+constexpr int kMetaWarps = kMetaThreads / 32;
+constexpr int kCopyThreads = 512;
+
+struct Workspace {
+  int4* bin_stat;    // [num_bins] {status, padded total, largest real, members}
+  int32_t* mem_dst;  // [M] slot where the member starts in its bin
+  int32_t* mem_real; // [M]
+  int32_t* mem_src;  // [M] source row
+};
+
+size_t workspace_bytes(int64_t M, int64_t num_bins) {
+  return round_up(16 * (size_t)num_bins, 16) + 3 * round_up(4 * (size_t)M, 16);
+}
+
+template <typename P>
+Workspace carve(P base_, int64_t M, int64_t num_bins) {
+  unsigned char* p = (unsigned char*)(base_);
+  Workspace w;
+  w.bin_stat = reinterpret_cast<int4*>(p);
+  p += round_up(16 * (size_t)num_bins, 16);
+  w.mem_dst = reinterpret_cast<int32_t*>(p);
+  p += round_up(4 * (size_t)M, 16);
+  w.mem_real = reinterpret_cast<int32_t*>(p);
+  p += round_up(4 * (size_t)M, 16);
+  w.mem_src = reinterpret_cast<int32_t*>(p);
+  return w;
+}
+
+struct MetaArgs {
+  const int64_t* real;
+  const int32_t* off;
+  const int32_t* mem;
+  int num_bins, M;
+  int64_t N, W, multiple, capacity, width;
+  int stretch, check_width;
+  int32_t* cu;
+  int32_t* cup;
+};
+
+__global__ void __launch_bounds__(kMetaThreads) squeeze_meta_kernel(MetaArgs a, Workspace ws) {
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.x * kMetaWarps + warp;
+  if (b >= a.num_bins) return;
+  const int lo = __ldg(a.off + b), hi = __ldg(a.off + b + 1);
+  const bool bad_offsets = (b == 0 && lo != 0) || (b == a.num_bins - 1 && hi != a.M) || lo < 0 || hi > a.M ||
+                           hi <= lo;
+  if (bad_offsets) {
+    if (lane == 0) ws.bin_stat[b] = make_int4(PSEQ_ERR_VALUE, 0, 0, 0);
+    return;
+  }
+  long long run_real = 0, run_padded = 0;
+  int longest = 0;
+  bool bad = false;
+  for (int base = lo; base < hi; base += 32) {
+    const int e = base + lane;
+    long long real = 0, padded = 0;
+    int src = 0;
+    if (e < hi) {
+      src = __ldg(a.mem + e);
+      if (src < 0 || src >= a.N) {
+        bad = true;
+      } else {
+        real = __ldg(a.real + src);
+        if (real < 0 || real > a.W) {
+          bad = true;
+          real = 0;
+        }
+      }
+      padded = (real + a.multiple - 1) / a.multiple * a.multiple;
+      longest = max(longest, (int)real);
+    }
+    long long ir = real, ip = padded;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const long long r = __shfl_up_sync(~0u, ir, d), q = __shfl_up_sync(~0u, ip, d);
+      if (lane >= d) {
+        ir += r;
+        ip += q;
+      }
+    }
+    if (e < hi) {
+      const long long R = run_real + ir - real, Pd = run_padded + ip - padded;
+      a.cu[e + b] = (int32_t)R;
+      a.cup[e + b] = (int32_t)Pd;
+      ws.mem_dst[e] = (int32_t)Pd;
+      ws.mem_real[e] = (int32_t)real;
+      ws.mem_src[e] = src;
+    }
+    run_real += __shfl_sync(~0u, ir, 31);
+    run_padded += __shfl_sync(~0u, ip, 31);
+  }
+  bad = __any_sync(~0u, bad);
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) longest = max(longest, __shfl_xor_sync(~0u, longest, d));
+  if (lane == 0) {
+    int status = PSEQ_OK;
+    if (bad) status = PSEQ_ERR_VALUE;
+    else if (run_padded > a.capacity || (a.check_width && run_padded > a.width)) status = PSEQ_ERR_CAPACITY;
+    a.cu[hi + b] = (int32_t)run_real;
+    a.cup[hi + b] = a.stretch ? (int32_t)a.capacity : (int32_t)run_padded;
+    ws.bin_stat[b] = make_int4(status, (int)min(run_padded, (long long)INT32_MAX), longest, hi - lo);
+  }
+}
+
+struct CopyArgs {
+  const unsigned char* src;
+  int64_t W;
+  int elem_bytes;
+  const int32_t* off;
+  int num_bins, M;
+  int64_t width, chunk, pad_value;
+  unsigned char* out;   // may be NULL (metadata only)
+  uint8_t* mask;        // may be NULL
+  pseq_info* info;
+};
+
+// Largest k in [lo, hi) with dst[k] <= x, given dst[lo] <= x.
+__device__ __forceinline__ int warp_find(const int32_t* dst, int lo, int hi, int64_t x) {
+  const int lane = threadIdx.x & 31;
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) / 32;
+    const int probe = lo + lane * step;
+    const bool ok = probe < hi && (int64_t)__ldcg(dst + probe) <= x;
+    const unsigned m = __ballot_sync(~0u, ok);
+    lo = lo + (31 - __clz(m)) * step;
+    hi = min(lo + step, hi);
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kCopyThreads) squeeze_copy_kernel(CopyArgs c, Workspace ws) {
+  __shared__ int s_value, s_capacity, s_longest, s_widest, s_first;
+  pdl_wait();
+  const int tid = threadIdx.x;
+  const int b = blockIdx.y;
+  if (blockIdx.x == 0 && b == 0) {
+    if (tid == 0) s_value = s_capacity = s_longest = s_widest = 0;
+    __syncthreads();
+    for (int i = tid; i < c.num_bins; i += kCopyThreads) {
+      const int4 st = __ldcg(ws.bin_stat + i);
+      if (st.x == PSEQ_ERR_VALUE) s_value = 1;
+      if (st.x == PSEQ_ERR_CAPACITY) s_capacity = 1;
+      atomicMax(&s_longest, st.z);
+      atomicMax(&s_widest, st.y);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const int status = s_value ? PSEQ_ERR_VALUE : (s_capacity ? PSEQ_ERR_CAPACITY : PSEQ_OK);
+      *c.info = status == PSEQ_OK ? pseq_info{PSEQ_OK, c.M, s_longest, s_widest} : pseq_info{status, 0, 0, 0};
+    }
+  }
+  if (!c.out || b >= c.num_bins) return;
+  const int4 st = __ldcg(ws.bin_stat + b);
+  if (st.x != PSEQ_OK) return;
+  const int64_t c0 = (int64_t)blockIdx.x * c.chunk;
+  const int64_t c1 = min(c0 + c.chunk, c.width);
+  if (c0 >= c1) return;
+  const int eb = c.elem_bytes;
+  const int64_t total = st.y;
+  unsigned char* row = c.out + (int64_t)b * c.width * eb;
+  uint8_t* mrow = c.mask ? c.mask + (int64_t)b * c.width : nullptr;
+  if (c0 < total) {
+    const int lo = __ldg(c.off + b), hi = __ldg(c.off + b + 1);
+    if (tid < 32) {
+      const int k = warp_find(ws.mem_dst, lo, hi, c0);
+      if (tid == 0) s_first = k;
+    }
+    __syncthreads();
+    for (int k = s_first; k < hi; ++k) {
+      const int64_t s = __ldcg(ws.mem_dst + k);
+      if (s >= c1) break;
+      const int64_t real_end = s + __ldcg(ws.mem_real + k);
+      const int64_t e = (k + 1 < hi) ? (int64_t)__ldcg(ws.mem_dst + k + 1) : total;
+      const int64_t a0 = max(s, c0), a1 = min(real_end, c1);
+      if (a0 < a1) {
+        const int64_t i = __ldcg(ws.mem_src + k);
+        block_copy(row + a0 * eb, c.src + (i * c.W + (a0 - s)) * eb, (a1 - a0) * eb);
+        if (mrow) block_fill_bytes(mrow + a0, a1 - a0, 0);
+      }
+      const int64_t p0 = max(real_end, c0), p1 = min(e, c1);
+      if (p0 < p1) {
+        block_fill(row + p0 * eb, p1 - p0, eb, c.pad_value);
+        if (mrow) block_fill_bytes(mrow + p0, p1 - p0, 1);
+      }
+    }
+  }
+  const int64_t t0 = max(total, c0);
+  if (t0 < c1) {
+    block_fill(row + t0 * eb, c1 - t0, eb, c.pad_value);
+    if (mrow) block_fill_bytes(mrow + t0, c1 - t0, 1);
+  }
+}
+
+__global__ void empty_squeeze_kernel(pseq_info* info) { *info = {PSEQ_OK, 0, 0, 0}; }
+
+}  // namespace
+}  // namespace pseq
+
+using namespace pseq;
+
+extern "C" size_t pack_squeeze_workspace_size(int64_t num_members, int64_t num_bins) {
+  if (num_members < 0 || num_bins < 0) return 0;
+  return workspace_bytes(num_members, num_bins);
+}
+
+extern "C" pseq_status pack_squeeze(const void* src, int64_t N, int64_t W, int32_t elem_bytes,
+                                    const int64_t* real_lens, const int32_t* bin_offsets,
+                                    const int32_t* bin_members, int64_t num_bins, int64_t num_members,
+                                    int64_t multiple, int64_t capacity, int32_t stretch_to_capacity,
+                                    int64_t width, int64_t pad_value, void* out, int32_t* cu_seqlens,
+                                    int32_t* cu_seqlens_padded, uint8_t* padding_mask, pseq_info* info,
+                                    void* workspace, size_t workspace_bytes_, pseq_stream stream) {
+  clear_error();
+  const char* fn = "pack_squeeze";
+  if (N < 0 || W < 0 || num_bins < 0 || num_members < 0 || width < 0 || capacity < 0)
+    return fail(PSEQ_ERR_ARG, "%s: negative size", fn);
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
+    return fail(PSEQ_ERR_ARG, "%s: elem_bytes must be 1, 2, 4 or 8", fn);
+  if (multiple < 1 || multiple > INT32_MAX) return fail(PSEQ_ERR_ARG, "%s: multiple must be in [1, INT32_MAX]", fn);
+  if (N > INT32_MAX || W > INT32_MAX || capacity > INT32_MAX || width > INT32_MAX || num_bins > INT32_MAX / 2 ||
+      num_members > INT32_MAX / 2)
+    return fail(PSEQ_ERR_OVERFLOW, "%s: a size exceeds the int32 range", fn);
+  if (num_bins > 65535) return fail(PSEQ_ERR_ARG, "%s: at most 65535 bins per call", fn);
+  if ((out == nullptr) != (padding_mask == nullptr) && out == nullptr)
+    return fail(PSEQ_ERR_ARG, "%s: padding_mask needs out", fn);
+  if (stretch_to_capacity && out && width < capacity)
+    return fail(PSEQ_ERR_ARG, "%s: stretching to capacity needs width >= capacity", fn);
+  if (!info || !cu_seqlens || !cu_seqlens_padded) return fail(PSEQ_ERR_ARG, "%s: NULL output", fn);
+  if (num_bins > 0 && (!bin_offsets || (num_members > 0 && (!bin_members || !real_lens))))
+    return fail(PSEQ_ERR_ARG, "%s: NULL bin arrays", fn);
+  if (out && num_members > 0 && N * W > 0 && !src) return fail(PSEQ_ERR_ARG, "%s: NULL src", fn);
+  if (!aligned(real_lens, 8) || !aligned(bin_offsets, 4) || !aligned(bin_members, 4) || !aligned(cu_seqlens, 4) ||
+      !aligned(cu_seqlens_padded, 4) || !aligned(info, 4) || !aligned(src, (uintptr_t)elem_bytes) ||
+      !aligned(out, (uintptr_t)elem_bytes))
+    return fail(PSEQ_ERR_ARG, "%s: misaligned pointer", fn);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (num_bins == 0) {
+    if (num_members != 0) return fail(PSEQ_ERR_ARG, "%s: members without bins", fn);
+    empty_squeeze_kernel<<<1, 1, 0, st>>>(info);
+    count_launches(1);
+    return check_launch(fn);
+  }
+  const size_t need = workspace_bytes(num_members, num_bins);
+  if (!workspace || workspace_bytes_ < need || !aligned(workspace, 16))
+    return fail(PSEQ_ERR_ARG, "%s: workspace needs %zu bytes, 16-byte aligned (got %zu)", fn, need, workspace_bytes_);
+  Workspace ws = carve(workspace, num_members, num_bins);
+
+  MetaArgs m = {};
+  m.real = real_lens;
+  m.off = bin_offsets;
+  m.mem = bin_members;
+  m.num_bins = (int)num_bins;
+  m.M = (int)num_members;
+  m.N = N;
+  m.W = W;
+  m.multiple = multiple;
+  m.capacity = capacity;
+  m.width = width;
+  m.stretch = stretch_to_capacity ? 1 : 0;
+  m.check_width = out ? 1 : 0;
+  m.cu = cu_seqlens;
+  m.cup = cu_seqlens_padded;
+  squeeze_meta_kernel<<<(unsigned)((num_bins + kMetaWarps - 1) / kMetaWarps), kMetaThreads, 0, st>>>(m, ws);
+  count_launches(1);
+  pseq_status s = check_launch(fn);
+  if (s != PSEQ_OK) return s;
+
+  CopyArgs c = {};
+  c.src = static_cast<const unsigned char*>(src);
+  c.W = W;
+  c.elem_bytes = elem_bytes;
+  c.off = bin_offsets;
+  c.num_bins = (int)num_bins;
+  c.M = (int)num_members;
+  c.width = width;
+  c.pad_value = pad_value;
+  c.out = static_cast<unsigned char*>(out);
+  c.mask = padding_mask;
+  c.info = info;
+  dim3 grid(1, 1);
+  if (out && width > 0) {
+    // chunks of whole 16-byte groups, about four CTAs per SM over the output
+    const int64_t slots = num_bins * width;
+    const int64_t target = (int64_t)sm_count() * 4;
+    int64_t chunk = (slots + target - 1) / target;
+    const int64_t per16 = 16 / elem_bytes;
+    const int64_t min_chunk = 4096 / elem_bytes;
+    if (chunk < min_chunk) chunk = min_chunk;
+    chunk = (chunk + per16 - 1) / per16 * per16;
+    c.chunk = chunk;
+    grid = dim3((unsigned)((width + chunk - 1) / chunk), (unsigned)num_bins);
+  } else {
+    c.chunk = 1;
+  }
+  cudaError_t e = launch_pdl(squeeze_copy_kernel, grid, dim3(kCopyThreads), 0, st, c, ws);
+  count_launches(1);
+  if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  return check_launch(fn);
+}
