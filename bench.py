@@ -1,0 +1,741 @@
+#!/usr/bin/env python
+"""Throughput of the packed-sequence preprocessing hot path on GB300.
+
+One step is one pass of the whole hot path over one batch of each of the
+five synthetic workloads (all inputs resident in HBM when timing starts):
+
+  map_small   pseq_from_doc_ids on doc_ids int32 [4, 2048]
+  thd_small   thd_from_batch of the matching int64 ids / labels / positions
+  thd_ids     thd_from_batch, B=8 S=8192, 64 pack slots, int64 ids, labels,
+              mRoPE positions [3, 8, 8192]
+  thd_emb     thd_meta + thd_gather of bf16 hidden [4, 8192, 4096]
+  squeeze     pack_squeeze of int64 [256, 4096] into FFD bins of 32768
+  map_stress  pseq_from_doc_ids on doc_ids int32 [64, 32768] (~250k segments)
+
+Metric: packed tokens per second (tokens of every produced stream: B*S per
+map, T per THD stream, bins*width per squeeze) and achieved HBM GB/s of the
+dominant kernel (the embedding gather) against the measured copy bandwidth.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+For N > 1 launch under torchrun; every rank runs its own batches (weak
+scaling, no data-path collective) and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "packed tokens/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+WORKLOAD = ("packed-sequence preprocessing step: doc_ids map [4,2048] + its THD batch (int64 ids/labels/positions); "
+            "THD B=8 S=8192 64 packs (ids, labels, mRoPE [3,8,8192]); THD bf16 hidden [4,8192,4096]; "
+            "squeeze int64 [256,4096] -> FFD bins x 32768; doc_ids map [64,32768] (~250k segments)")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (timing only; the path itself exchanges nothing)
+# ----------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend: str):
+        if self.world > 1:
+            import torch.distributed as dist
+
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float, device=None) -> float:
+        if self.pg is None:
+            return x
+        import torch
+
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float, device=None) -> float:
+        if self.pg is None:
+            return x
+        import torch
+
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# inputs
+# ----------------------------------------------------------------------------
+def make_inputs(seed: int) -> dict:
+    """Host inputs of every part of one step (numpy; hidden as torch bf16)."""
+    small = synth.doc_map_small(seed)
+    return {
+        "map_small": small["doc_ids"],
+        "thd_small": {k: small[k] for k in ("input_ids", "labels", "position_ids", "seq_lens", "seq_lens_padded")},
+        "thd_ids": synth.thd_ids(seed),
+        "thd_emb": synth.thd_embeddings(seed),
+        "squeeze": synth.squeeze(seed),
+        "map_stress": synth.doc_map_stress(seed),
+    }
+
+
+# ----------------------------------------------------------------------------
+# native arm
+# ----------------------------------------------------------------------------
+class NativeStep:
+    """Device buffers and the C ABI calls of one step (no allocation inside)."""
+
+    def __init__(self, host: dict, device):
+        import torch
+
+        import varlen_attention_metadata_gb300 as v
+
+        self.torch = torch
+        self.v = v
+        self.lib = v.load_library()
+        self.dev = device
+        self.host = host
+        self.inputs = []   # (device tensor, host tensor) pairs copied in by the e2e leg
+        self.outputs = []  # (device tensor, nbytes) pairs copied out by the e2e leg
+        self.tokens = {}
+        self.alg_bytes = {}
+        self.calls = []
+        self._build()
+
+    def _in(self, a):
+        torch = self.torch
+        t = a if isinstance(a, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(a))
+        d = t.to(self.dev)
+        self.inputs.append((d, t.pin_memory()))
+        return d
+
+    def _zeros(self, n, dtype):
+        return self.torch.zeros(n, dtype=dtype, device=self.dev)
+
+    @staticmethod
+    def _p(t, off=0):
+        return ctypes.c_void_p(t.data_ptr() + off)
+
+    def _stream(self):
+        return ctypes.c_void_p(self.torch.cuda.current_stream(self.dev).cuda_stream)
+
+    def _map(self, name, doc_ids):
+        torch, lib = self.torch, self.lib
+        B, S = doc_ids.shape
+        d = self._in(doc_ids)
+        cu = self._zeros(B * S + 1, torch.int32)
+        info = self._zeros(8, torch.int32)
+        ws = self._zeros(lib.pseq_from_doc_ids_workspace_size(B, S), torch.uint8)
+
+        def call():
+            lib.pseq_from_doc_ids(self._p(d), 4, B, S, self._p(cu), self._p(info), self._p(ws), ws.numel(),
+                                  self._stream())
+
+        self.calls.append((name, call))
+        self.tokens[name] = B * S
+        self._finish[name] = lambda: (info, cu, d)
+
+    def _thd(self, name, batch, fields_np, hidden=None, split=False):
+        torch, lib, v = self.torch, self.lib, self.v
+        real, padded = batch["seq_lens"], batch["seq_lens_padded"]
+        B, P = real.shape
+        S = (fields_np[0][0] if fields_np else hidden).shape[1]
+        dreal, dpad = self._in(real), self._in(padded)
+        fields = (v._lib.PseqField * 8)()
+        dsts = []
+        srcs = []
+        k = 0
+        for a, planes in fields_np:
+            src = self._in(a)
+            row = int(np.prod(a.shape[3 if planes > 1 else 2:])) if a.ndim > (3 if planes > 1 else 2) else 1
+            dst = self._zeros(planes * B * S * row, src.dtype)
+            fields[k].src, fields[k].dst = src.data_ptr(), dst.data_ptr()
+            fields[k].elem_bytes, fields[k].planes, fields[k].row_elems = src.element_size(), planes, row
+            dsts.append((dst, planes, row, src.element_size()))
+            srcs.append(src)
+            k += 1
+        if hidden is not None:
+            src = self._in(hidden)
+            H = hidden.shape[2]
+            dst = self._zeros(B * S * H, src.dtype)
+            fields[k].src, fields[k].dst = src.data_ptr(), dst.data_ptr()
+            fields[k].elem_bytes, fields[k].planes, fields[k].row_elems = 2, 1, H
+            dsts.append((dst, 1, H, 2))
+            k += 1
+        nf = k
+        cu = self._zeros(B * P + 1, torch.int32)
+        cup = self._zeros(B * P + 1, torch.int32)
+        mask = self._zeros(B * S, torch.uint8)
+        info = self._zeros(8, torch.int32)
+        ws = self._zeros(lib.thd_workspace_size(B, P), torch.uint8)
+        self._keep.append((fields, srcs))
+
+        if split:
+            def call(events=None):
+                lib.thd_meta(self._p(dreal), self._p(dpad), B, S, P, -1000, 1, self._p(cu), self._p(cup),
+                             self._p(info, 16), self._p(info), self._p(ws), ws.numel(), self._stream())
+                if events is not None:
+                    events[0].record()
+                lib.thd_gather(fields, nf, B, S, P, self._p(mask), self._p(ws), ws.numel(), self._stream())
+                if events is not None:
+                    events[1].record()
+        else:
+            def call():
+                lib.thd_from_batch(self._p(dreal), self._p(dpad), B, S, P, -1000, 1, fields, nf, self._p(cu),
+                                   self._p(cup), self._p(mask), self._p(info, 16), self._p(info), self._p(ws),
+                                   ws.numel(), self._stream())
+
+        self.calls.append((name, call))
+        self._finish[name] = lambda: (info, cu, cup, mask, dsts)
+
+    def _squeeze(self, name, c):
+        torch, lib = self.torch, self.lib
+        src = self._in(c["src"])
+        real = self._in(c["real_lens"])
+        offs = self._in(c["bin_offsets"])
+        mem = self._in(c["bin_members"])
+        N, W = c["src"].shape
+        nb, M = len(c["bin_offsets"]) - 1, int(c["bin_offsets"][-1])
+        width = c["width"]
+        out = self._zeros(nb * width, torch.int64)
+        mask = self._zeros(nb * width, torch.uint8)
+        cu = self._zeros(M + nb + 1, torch.int32)
+        cup = self._zeros(M + nb + 1, torch.int32)
+        info = self._zeros(8, torch.int32)
+        ws = self._zeros(lib.pack_squeeze_workspace_size(M, nb), torch.uint8)
+
+        def call():
+            lib.pack_squeeze(self._p(src), N, W, 8, self._p(real), self._p(offs), self._p(mem), nb, M,
+                             c["multiple"], c["capacity"], 1 if c["stretch"] else 0, width, c["pad_value"],
+                             self._p(out), self._p(cu), self._p(cup), self._p(mask), self._p(info), self._p(ws),
+                             ws.numel(), self._stream())
+
+        self.calls.append((name, call))
+        self.tokens[name] = nb * width
+        self._finish[name] = lambda: (info, cu, cup, mask, out, M + nb)
+
+    def _build(self):
+        h = self.host
+        self._finish = {}
+        self._keep = []
+        self._map("map_small", h["map_small"])
+        t0 = h["thd_small"]
+        self._thd("thd_small", t0, [(t0["input_ids"], 1), (t0["labels"], 1), (t0["position_ids"], 1)])
+        t1 = h["thd_ids"]
+        self._thd("thd_ids", t1, [(t1["input_ids"], 1), (t1["labels"], 1), (t1["position_ids"], 3)])
+        self._thd("thd_emb", h["thd_emb"], [], hidden=h["thd_emb"]["hidden"], split=True)
+        self._squeeze("squeeze", h["squeeze"])
+        self._map("map_stress", h["map_stress"])
+
+    def run(self, gather_events=None):
+        for name, call in self.calls:
+            if name == "thd_emb":
+                call(gather_events)
+            else:
+                call()
+
+    def resolve(self):
+        """After one untimed step: exact token counts, output sizes, checks."""
+        torch = self.torch
+        torch.cuda.synchronize(self.dev)
+        self.outputs = []
+        for name, get in self._finish.items():
+            res = get()
+            info = res[0][:4].tolist()
+            if info[0] != 0:
+                raise RuntimeError(f"{name}: device status {info[0]}")
+            if name.startswith("map"):
+                _, cu, d = res
+                self.outputs.append((cu, 4 * (info[1] + 1)))
+                self.alg_bytes[name] = d.numel() * 4 + 4 * (info[1] + 1)
+            elif name.startswith("thd"):
+                _, cu, cup, mask, dsts = res
+                n, T = info[1], info[3]
+                self.tokens[name] = T
+                self.outputs += [(cu, 4 * (n + 1)), (cup, 4 * (n + 1)), (mask, T)]
+                moved = 0
+                for dst, planes, row, eb in dsts:
+                    self.outputs.append((dst, planes * T * row * eb))
+                    moved += 2 * planes * T * row * eb
+                self.alg_bytes[name] = moved + T + 8 * (n + 1) + 2 * 8 * self.host[name]["seq_lens"].size
+                if name == "thd_emb":
+                    self.gather_bytes = moved + T  # what thd_gather alone must move
+            else:
+                _, cu, cup, mask, out, ncu = res
+                self.outputs += [(cu, 4 * ncu), (cup, 4 * ncu), (mask, mask.numel()), (out, out.numel() * 8)]
+                c = self.host["squeeze"]
+                real_bytes = 8 * int(c["real_lens"].sum())
+                self.alg_bytes[name] = real_bytes + out.numel() * 8 + mask.numel() + 8 * ncu
+        self.h2d_bytes = sum(h.numel() * h.element_size() for _, h in self.inputs)
+        self.d2h_bytes = sum(n for _, n in self.outputs)
+        self.host_out = [torch.empty(n, dtype=torch.uint8, pin_memory=True) for _, n in self.outputs]
+
+    def copy_in(self):
+        for d, h in self.inputs:
+            d.copy_(h, non_blocking=True)
+
+    def copy_out(self):
+        for (d, n), h in zip(self.outputs, self.host_out):
+            h.copy_(d.view(self.torch.uint8)[:n], non_blocking=True)
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "varlen_attention_metadata_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    with open(os.path.join(ROOT, "include", "pseq.h"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the gather from the committed ncu summary,
+    or None when the kernels changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "thd_gather_embeddings.md")
+    try:
+        with open(path) as f:
+            text = f.read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, _, val = line.strip()[2:].partition(":")
+            vals[k.strip()] = val.strip().strip("`")
+    if vals.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    try:
+        return int(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.window = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id:
+            cmd.insert(1, f"--id={self.gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        if self.window:
+            inside = [r for r in rows if self.window[0] <= r[0] <= self.window[1] + 0.25]
+            if inside:
+                rows = inside
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for _, p in rows if num(p[1]) is not None]
+        mx = [num(p[2]) for _, p in rows if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in rows for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def run_native(args, dist: Dist):
+    import torch
+
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    dist.init("nccl")
+    from varlen_attention_metadata_gb300 import build
+
+    if dist.local_rank == 0:
+        build.build()
+    dist.barrier()
+
+    host = make_inputs(args.seed + dist.rank)
+    step = NativeStep(host, dev)
+    step.run()
+    step.resolve()
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def flush_l2():
+        # write a buffer larger than L2, then read another one so that the
+        # dirty lines of the write are evicted here and not inside the next step
+        flush_w.zero_()
+        flush_r.sum()
+
+    lib = step.lib
+    tokens = sum(step.tokens.values())
+
+    for _ in range(max(args.warmup, 3)):
+        flush_l2()
+        step.run()
+    torch.cuda.synchronize(dev)
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    time.sleep(0.5)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = lib.pseq_launch_count()
+    t_wall0 = time.time()
+    for i in range(K):
+        flush_l2()
+        ev[i][0].record()
+        step.run(gev[i])
+        ev[i][1].record()
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    dist.barrier()
+    launches = lib.pseq_launch_count() - launches0
+    clocks.mark(t_wall0, t_wall1)
+    time.sleep(0.3)
+    clocks.stop()
+
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    gather_ms = [a.elapsed_time(b) for a, b in gev]
+    total_ms = dist.max(sum(step_ms), dev)
+    ms_per_step = total_ms / K
+    all_tokens = dist.sum(float(tokens), dev)
+    value = all_tokens / (ms_per_step / 1e3)
+
+    # end to end: pinned host inputs in, results out, every step
+    Ke = min(K, 100)
+    e2e_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    for _ in range(3):
+        step.copy_in()
+        step.run()
+        step.copy_out()
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    e2e_ev[0].record()
+    for _ in range(Ke):
+        step.copy_in()
+        step.run()
+        step.copy_out()
+    e2e_ev[1].record()
+    torch.cuda.synchronize(dev)
+    e2e_ms = dist.max(e2e_ev[0].elapsed_time(e2e_ev[1]), dev) / Ke
+    e2e_value = all_tokens / (e2e_ms / 1e3)
+
+    peak, peak_kind = measured_peak()
+    g_avg_ms = statistics.mean(gather_ms)
+    achieved = step.gather_bytes / (g_avg_ms / 1e3) / 1e9
+    traffic = profiled_traffic()
+    cpu = None
+    if dist.rank == 0:
+        cpu = cpu_baseline(host, budget_s=10.0)
+    dist.barrier()
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 1),
+            "unit": UNIT,
+            "n_gpus": dist.world,
+            "steps": K,
+            "warmup": max(args.warmup, 3),
+            "ms_per_step": round(ms_per_step, 6),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "int64",
+            "data": "synthetic (seeded generators; shapes and length mixes of packed SFT batches)",
+            "config": {
+                "workload": WORKLOAD,
+                "tokens_per_step_per_gpu": tokens,
+                "parts_tokens": step.tokens,
+                "l2": "flushed between steps outside the timed events (256 MiB write, then 256 MiB read of another buffer)",
+                "parallelism": f"replicas x{dist.world} (independent batches per GPU)",
+                "algorithmic_bytes_per_step": sum(step.alg_bytes.values()),
+            },
+            "roofline": {
+                "kernel": "thd_gather_kernel (bf16 hidden [4,8192,4096] -> [T,4096] + padding mask)",
+                "bound": "hbm",
+                "achieved": round(achieved, 1),
+                "peak": peak,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": traffic,
+                "algorithmic_bytes_per_launch": step.gather_bytes,
+                "avg_launch_us": round(g_avg_ms * 1e3, 3),
+            },
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": step.h2d_bytes,
+                    "d2h_bytes_per_step": step.d2h_bytes, "steps": Ke, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": int(launches),
+            "clocks": clocks.summary(),
+            "wall_s_timed_region": round(t_wall1 - t_wall0, 3),
+        }
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+# ----------------------------------------------------------------------------
+# oracle arms: cpu_baseline (inside the native run) and --impl reference
+# ----------------------------------------------------------------------------
+class OracleUnits:
+    """The composite workload cut into small independent units for the oracle.
+
+    Units: one row of a doc_ids map (rows are independent: every row start is
+    a boundary), one row of a THD batch, one sequence of the embedding batch,
+    one bin of the squeeze.  Each unit runs the oracle function on its own
+    sub-problem; rates are kept per part.
+    """
+
+    def __init__(self, host: dict):
+        import oracle
+        import torch
+
+        self.oracle = oracle
+        self.parts = {}
+        ms = host["map_small"]
+        self.parts["map_small"] = ([ms[b:b + 1] for b in range(ms.shape[0])], ms.size)
+        mst = host["map_stress"]
+        self.parts["map_stress"] = ([mst[b:b + 1] for b in range(mst.shape[0])], mst.size)
+        for name in ("thd_small", "thd_ids"):
+            bt = host[name]
+            B = bt["input_ids"].shape[0]
+            units = []
+            for b in range(B):
+                sub = {"input_ids": bt["input_ids"][b:b + 1], "labels": bt["labels"][b:b + 1],
+                       "seq_lens": bt["seq_lens"][b:b + 1], "seq_lens_padded": bt["seq_lens_padded"][b:b + 1]}
+                pos = bt["position_ids"]
+                sub["position_ids"] = pos[:, b:b + 1] if pos.ndim == 3 else pos[b:b + 1]
+                units.append(sub)
+            meta = oracle.thd_meta(bt["seq_lens"], bt["seq_lens_padded"], bt["input_ids"].shape[1])
+            self.parts[name] = (units, meta["total_tokens"])
+        emb = host["thd_emb"]
+        h = emb["hidden"].view(torch.int16).numpy()
+        meta = oracle.thd_meta(emb["seq_lens"], emb["seq_lens_padded"], h.shape[1])
+        units = []
+        for i in range(meta["num_sequences"]):
+            b, o, r, p = (int(meta[k][i]) for k in ("seq_row", "seq_off", "seq_real", "seq_padded"))
+            units.append({"hidden": h[b:b + 1, o:o + p], "seq_lens": np.array([[r]], np.int64),
+                          "seq_lens_padded": np.array([[p]], np.int64)})
+        self.parts["thd_emb"] = (units, meta["total_tokens"])
+        sq = host["squeeze"]
+        units = []
+        for members in sq["bins"]:
+            offs, mem = oracle.bins_to_csr([members])
+            units.append((sq["src"], sq["real_lens"], offs, mem))
+        self.parts["squeeze"] = (units, len(sq["bins"]) * sq["width"])
+        self.sq = sq
+        self.next = {k: 0 for k in self.parts}
+        self.done_tokens = {k: 0 for k in self.parts}
+        self.done_s = {k: 0.0 for k in self.parts}
+
+    def _run(self, name, u):
+        o = self.oracle
+        if name.startswith("map"):
+            o.from_doc_ids(u)
+            return u.size
+        if name == "thd_emb":
+            meta = o.thd_meta(u["seq_lens"], u["seq_lens_padded"], u["hidden"].shape[1])
+            o.thd_gather(u["hidden"], meta, 1, u["hidden"].shape[1])
+            o.thd_padding_mask(meta["total_tokens"], meta["seq_real"], meta["seq_padded"])
+            return meta["total_tokens"]
+        if name.startswith("thd"):
+            return o.process_input_for_thd(u)["total_tokens"]
+        src, real, offs, mem = u
+        sq = self.sq
+        o.pack_squeeze(src, real, offs, mem, sq["multiple"], sq["capacity"], sq["stretch"], sq["width"],
+                       sq["pad_value"])
+        return sq["width"]
+
+    def step(self):
+        """One unit of every part; returns the seconds spent."""
+        spent = 0.0
+        for name, (units, _) in self.parts.items():
+            u = units[self.next[name] % len(units)]
+            self.next[name] += 1
+            t0 = time.perf_counter()
+            tok = self._run(name, u)
+            dt = time.perf_counter() - t0
+            self.done_tokens[name] += tok
+            self.done_s[name] += dt
+            spent += dt
+        return spent
+
+    def composite(self):
+        """Seconds the oracle needs for one whole step, from per-part rates."""
+        total_s, tokens = 0.0, 0
+        for name, (_, part_tokens) in self.parts.items():
+            rate = self.done_tokens[name] / max(self.done_s[name], 1e-12)
+            total_s += part_tokens / rate
+            tokens += part_tokens
+        return total_s, tokens
+
+    def units_done(self):
+        return sum(self.next.values())
+
+
+def cpu_baseline(host: dict, budget_s: float = 10.0) -> dict:
+    u = OracleUnits(host)
+    t0 = time.perf_counter()
+    steps = 0
+    while time.perf_counter() - t0 < budget_s or steps < 2:
+        u.step()
+        steps += 1
+    step_s, tokens = u.composite()
+    return {"value": round(tokens / step_s, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{u.units_done()} oracle units ({steps} rounds of one map row, one THD row per batch, one "
+                      f"embedding sequence and one squeeze bin), {time.perf_counter() - t0:.1f} s single-threaded; "
+                      f"per-part rates combined over one whole step ({tokens} tokens)",
+            "oracle_ms_per_step": round(step_s * 1e3, 3)}
+
+
+def run_reference(args, dist: Dist):
+    if dist.world > 1:
+        dist.init("gloo")
+        if dist.rank != 0:
+            dist.close()
+            return
+    host = make_inputs(args.seed)
+    u = OracleUnits(host)
+    for _ in range(max(args.warmup, 3)):
+        u.step()
+    u.done_tokens = {k: 0 for k in u.parts}
+    u.done_s = {k: 0.0 for k in u.parts}
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        u.step()
+    wall = time.perf_counter() - t0
+    step_s, tokens = u.composite()
+    value = tokens / step_s
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": UNIT,
+        "n_gpus": dist.world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(step_s * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int64",
+        "data": "synthetic (seeded generators; shapes and length mixes of packed SFT batches)",
+        "config": {"workload": WORKLOAD, "tokens_per_step_per_gpu": tokens},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step one unit of every part (a map row, a THD row, one embedding "
+                                   f"sequence, one squeeze bin); {args.steps} steps in {wall:.1f} s; per-part "
+                                   f"rates combined over one whole step"},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if dist.pg is not None:
+        dist.close()
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    if args.gpus > 1 and dist.world == 1:
+        sys.exit("bench.py --gpus N > 1 must be launched with torchrun (one process per GPU)")
+    if args.impl == "reference":
+        run_reference(args, dist)
+    else:
+        run_native(args, dist)
+
+
+if __name__ == "__main__":
+    main()
