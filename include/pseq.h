@@ -99,6 +99,35 @@ pseq_status pseq_from_doc_ids(const void* doc_ids, int32_t id_bytes, int64_t B,
                               pseq_stream stream);
 
 /* ------------------------------------------------------------------------
+ * pseq_from_doc_ids_static -- pseq_from_doc_ids without a workspace
+ * The paper has no counterpart to this entry point; it is an integration
+ * variant of the call above.
+ * Some callers cannot allocate device memory when they call in: code running
+ * under a memory-pool policy that forbids new allocations, a plugin or
+ * callback that is handed only input and output pointers, or a process that
+ * has reserved all of HBM up front.  This entry point takes the same inputs
+ * and outputs as pseq_from_doc_ids and no workspace.  Its scratch is a
+ * static device array of about 144 KiB inside libpseq.so, which every GPU
+ * that loads the library holds until the process exits.
+ *  - B*S must not exceed PSEQ_STATIC_MAX_TOKENS; larger maps get
+ *    PSEQ_ERR_ARG before anything is enqueued (use pseq_from_doc_ids).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call clears the part of the array that must start at zero
+ *    (cudaMemsetAsync on the caller's stream) and then runs the scan.  All
+ *    calls share the one array, so calls that may overlap on the GPU (other
+ *    streams, other host threads) race and must be serialised by the caller.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * Outputs and errors are those of pseq_from_doc_ids.
+ * ---------------------------------------------------------------------- */
+#define PSEQ_STATIC_MAX_TOKENS (1LL << 24)
+pseq_status pseq_from_doc_ids_static(const void* doc_ids, int32_t id_bytes,
+                                     int64_t B, int64_t S,
+                                     int32_t* cu_seqlens, pseq_info* info,
+                                     pseq_stream stream);
+
+/* ------------------------------------------------------------------------
  * BSHD -> THD conversion
  * [thd_utils] "process_input_for_thd" (description, Example, Parameters,
  * Returns) and "_thd_padding_mask".

@@ -30,6 +30,7 @@ STATUS_NAMES = {
     PSEQ_ERR_CUDA: "PSEQ_ERR_CUDA",
 }
 PSEQ_MAX_FIELDS = 8
+PSEQ_STATIC_MAX_TOKENS = 1 << 24
 
 
 class PseqInfo(ctypes.Structure):
@@ -63,6 +64,7 @@ SIGNATURES = {
     "pseq_debug_set_wait": (None, [_I64, _I64]),
     "pseq_from_doc_ids_workspace_size": (_SZ, [_I64, _I64]),
     "pseq_from_doc_ids": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _P, _SZ, _P]),
+    "pseq_from_doc_ids_static": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _P]),
     "thd_workspace_size": (_SZ, [_I64, _I64]),
     "thd_from_batch": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _I64, _I32, _P, _I32,
                                       _P, _P, _P, _P, _P, _P, _SZ, _P]),

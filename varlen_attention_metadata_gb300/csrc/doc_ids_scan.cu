@@ -18,6 +18,8 @@
 // are compacted through shared memory and written with coalesced stores.
 // The last CTA to finish writes cu_seqlens[num_segments] and the info block
 // and clears the tile flags, so the workspace is zero again for the next call.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace pseq {
@@ -329,4 +331,87 @@ extern "C" pseq_status pseq_from_doc_ids(const void* doc_ids, int32_t id_bytes, 
     launch_scan<int64_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st);
   count_launches(1);
   return check_launch("pseq_from_doc_ids");
+}
+
+// ----------------------------------------------------------------------------
+// pseq_from_doc_ids_static: the same scan with its scratch in a static array.
+//
+// For callers that cannot allocate device memory at call time -- code running
+// under a memory-pool policy that forbids new allocations, inside a plugin or
+// callback that has no allocator handle, or in a process that has reserved the
+// whole HBM for itself -- this entry point takes only inputs and outputs.  Its
+// scratch is a file-scope device array, loaded with the library and held by
+// every GPU that loads it until the process exits.
+// ----------------------------------------------------------------------------
+namespace pseq {
+namespace {
+
+constexpr int64_t kStaticMaxTokens = PSEQ_STATIC_MAX_TOKENS;  // B*S limit of the static scratch
+constexpr int64_t kStaticMaxTiles = kStaticMaxTokens / kTile;
+constexpr size_t kStaticBytes = sizeof(Header) + ((4 * kStaticMaxTiles + 15) / 16) * 16 + 32 * kStaticMaxTiles;
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
+
+std::mutex g_static_mu;
+void* g_static_ptr[64] = {nullptr};
+
+// Device address of g_static_scratch on the current device, looked up once
+// per device.  In host code the array's name is only a stand-in symbol.
+pseq_status static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "pseq_from_doc_ids_static: cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(PSEQ_ERR_ARG, "pseq_from_doc_ids_static: device %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(PSEQ_ERR_CUDA, "pseq_from_doc_ids_static: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return PSEQ_OK;
+}
+
+}  // namespace
+}  // namespace pseq
+
+extern "C" pseq_status pseq_from_doc_ids_static(const void* doc_ids, int32_t id_bytes, int64_t B, int64_t S,
+                                                int32_t* cu_seqlens, pseq_info* info, pseq_stream stream) {
+  clear_error();
+  const char* fn = "pseq_from_doc_ids_static";
+  if (B < 0 || S < 0) return fail(PSEQ_ERR_ARG, "%s: negative shape [%lld, %lld]", fn, (long long)B, (long long)S);
+  if (id_bytes != 4 && id_bytes != 8) return fail(PSEQ_ERR_ARG, "%s: id_bytes must be 4 or 8, got %d", fn, id_bytes);
+  if (!cu_seqlens || !info) return fail(PSEQ_ERR_ARG, "%s: cu_seqlens and info are required", fn);
+  if (B > 0 && S > kStaticMaxTokens / B)
+    return fail(PSEQ_ERR_ARG, "%s: B*S = %lld*%lld exceeds the static scratch limit of %lld tokens", fn, (long long)B,
+                (long long)S, (long long)kStaticMaxTokens);
+  const int64_t N = B * S;
+  if (N > 0 && !doc_ids) return fail(PSEQ_ERR_ARG, "%s: doc_ids is NULL", fn);
+  if (!aligned(doc_ids, (uintptr_t)id_bytes) || !aligned(cu_seqlens, 4) || !aligned(info, 4))
+    return fail(PSEQ_ERR_ARG, "%s: misaligned pointer", fn);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    empty_map_kernel<<<1, 1, 0, st>>>(cu_seqlens, info);
+    count_launches(1);
+    return check_launch(fn);
+  }
+  void* scratch = nullptr;
+  pseq_status s = static_scratch(&scratch);
+  if (s != PSEQ_OK) return s;
+  const int64_t tiles = (N + kTile - 1) / kTile;
+  // The counters and tile flags must start at zero.  A completed call leaves
+  // them zero, but clear them anyway so an interrupted earlier call cannot leak
+  // into this one.
+  const size_t clear = sizeof(Header) + round_up(4 * (size_t)tiles, 16);
+  cudaError_t e = cudaMemsetAsync(scratch, 0, clear, st);
+  if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: cudaMemsetAsync: %s", fn, cudaGetErrorString(e));
+  Workspace ws = carve(scratch, tiles);
+  if (id_bytes == 4)
+    launch_scan<int32_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st);
+  else
+    launch_scan<int64_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st);
+  count_launches(1);
+  return check_launch(fn);
 }
