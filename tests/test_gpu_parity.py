@@ -87,8 +87,8 @@ def test_doc_ids_page_example():
 @pytest.mark.parametrize("dtype", [np.int32, np.int64])
 def test_doc_ids_random(kind, dtype):
     rng = np.random.default_rng(7)
-    shapes = [(1, 1), (1, 7), (3, 1), (2, 5), (5, 4096), (3, 4097), (7, 1500), (1, 3 * 4096 + 123),
-              (13, 2049), (40, 1)]
+    shapes = [(1, 1), (1, 7), (3, 1), (2, 5), (5, 4096), (3, 4097), (7, 1500), (1, 3 * 16384 + 123),
+              (13, 2049), (40, 1), (2, 16385)]
     for B, S in shapes:
         d = synth.random_doc_ids(rng, B, S, kind, dtype)
         check_doc_ids(d)
@@ -96,12 +96,18 @@ def test_doc_ids_random(kind, dtype):
 
 
 def test_doc_ids_many_tiles_chain():
-    """Hundreds of tiles, so the look-back crosses many 32-tile windows."""
+    """Over a hundred tiles, so the look-back crosses several 32-tile windows."""
     rng = np.random.default_rng(11)
     d = synth.random_doc_ids(rng, 9, 200_003, "runs", np.int32)
     check_doc_ids(d)
     d = synth.random_doc_ids(rng, 2, 700_001, "long", np.int32)  # tiles with no boundary at all
     check_doc_ids(d)
+
+
+def test_doc_ids_long_lookback():
+    """Over 500 tiles: long look-back chains."""
+    rng = np.random.default_rng(12)
+    check_doc_ids(synth.random_doc_ids(rng, 4, 2_200_001, "runs", np.int32))
 
 
 def test_doc_ids_empty():
@@ -228,6 +234,30 @@ def test_thd_random(seed):
         check_thd(batch, absorb=bool(trial % 2 == 0), with_padded=trial != 5, hidden=hidden)
 
 
+def test_thd_large_tables_two_kernel_path():
+    """B * num_packs above the one-launch limit: metadata kernel + gather."""
+    rng = np.random.default_rng(321)
+    B, S, P = 48, 700, 60  # 2880 table entries
+    real, padded = synth.random_thd(rng, B, S, P, multiple=4, interleave_filler=True)
+    batch = {"input_ids": rng.integers(0, 32000, size=(B, S)).astype(np.int64),
+             "position_ids": rng.integers(0, 99, size=(3, B, S)).astype(np.int64),
+             "seq_lens": real, "seq_lens_padded": padded}
+    hidden = torch.randn(B, S, 24, device=DEV).to(torch.bfloat16)
+    check_thd(batch, hidden=hidden)
+    check_thd(batch, absorb=False, with_padded=False)
+
+
+def test_thd_many_planes_use_block_copies():
+    """More (field, plane) pairs than the row-by-row path takes."""
+    rng = np.random.default_rng(99)
+    B, S, P = 2, 300, 5
+    real, padded = synth.random_thd(rng, B, S, P, multiple=2)
+    batch = {"input_ids": rng.integers(0, 32000, size=(B, S)).astype(np.int64),
+             "position_ids": rng.integers(0, 99, size=(20, B, S)).astype(np.int64),
+             "seq_lens": real, "seq_lens_padded": padded}
+    check_thd(batch)
+
+
 def test_thd_field_widths():
     """1-, 2-, 4- and 8-byte elements with odd row widths (unaligned rows)."""
     rng = np.random.default_rng(42)
@@ -332,6 +362,18 @@ def test_padding_mask_random(seed):
         np.testing.assert_array_equal(mask.cpu().numpy(), ref)
 
 
+def test_padding_mask_long_table():
+    v = V()
+    rng = np.random.default_rng(4)
+    n = 3000  # above the one-launch limit
+    real = rng.integers(0, 20, size=n).astype(np.int64)
+    padded = real + rng.integers(0, 5, size=n).astype(np.int64)
+    total = int(padded.sum()) + 77
+    mask, info = v.thd_padding_mask(total, dev(real), dev(padded))
+    assert info_of(info)[0] == 0
+    np.testing.assert_array_equal(mask.cpu().numpy(), oracle.thd_padding_mask(total, real, padded))
+
+
 def test_padding_mask_errors():
     v = V()
     for real, padded, total in ((np.array([3, 2]), np.array([4, 2]), 5), (np.array([3]), np.array([2]), 9),
@@ -408,6 +450,15 @@ def test_squeeze_random(dtype):
         cap = need + int(rng.integers(0, 40))
         width = cap if stretch else need + int(rng.integers(0, 5))
         check_squeeze(prob, m, cap, stretch, width, pad_value=int(rng.integers(-5, 5)))
+
+
+def test_squeeze_many_members_two_kernel_path():
+    rng = np.random.default_rng(8)
+    prob = synth.random_squeeze(rng, 1500, 40, 30)
+    m = 8
+    need = max(sum(-(-int(prob["real_lens"][i]) // m) * m for i in b) for b in prob["bins"])
+    check_squeeze(prob, m, need + 16, True, need + 16, pad_value=3)
+    check_squeeze(prob, m, need, False, need)
 
 
 def test_squeeze_workload():

@@ -50,6 +50,15 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Acquire side of a release/acquire pair whose flag was read with ld_relaxed.
+__device__ __forceinline__ void fence_acquire() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -67,6 +76,17 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 // Let the dependent grid be scheduled now (its pdl_wait still waits for us).
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// First statement of every kernel of this library.  Every launch carries the
+// programmatic-dependent-launch attribute, so a kernel may become resident
+// while the previous kernel on the stream is still running: wait until that
+// kernel has finished and its writes are visible before touching memory,
+// then let the next kernel on the stream be scheduled.  This hides the launch
+// latency between back-to-back calls without reordering any memory access.
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_launch_dependents();
 }
 
 __device__ __forceinline__ int4 ld_stream(const int4* p) {
@@ -177,6 +197,93 @@ __device__ __forceinline__ void block_fill(void* dst_, int64_t count, int elem_b
 // Fill `count` bytes with `b` using every thread of the block.
 __device__ __forceinline__ void block_fill_bytes(uint8_t* dst, int64_t count, uint8_t b) {
   block_fill(dst, count, 1, b);
+}
+
+// ----------------------------------------------------------------------------
+// block-wide scans of small tables
+// ----------------------------------------------------------------------------
+struct Triple {
+  int count;
+  long long real, padded;
+};
+
+__device__ __forceinline__ Triple add(const Triple& a, const Triple& b) {
+  return {a.count + b.count, a.real + b.real, a.padded + b.padded};
+}
+
+__device__ __forceinline__ Triple shfl_up(const Triple& v, int d) {
+  return {__shfl_up_sync(~0u, v.count, d), __shfl_up_sync(~0u, v.real, d), __shfl_up_sync(~0u, v.padded, d)};
+}
+
+// Exclusive scan of one Triple per thread over a block of WARPS warps;
+// `total` receives the block sum.  `scratch` holds WARPS entries.
+template <int WARPS>
+__device__ __forceinline__ Triple block_exclusive(Triple x, Triple* scratch, Triple& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  Triple inc = x;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const Triple o = shfl_up(inc, d);
+    if (lane >= d) inc = add(o, inc);
+  }
+  if (lane == 31) scratch[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    Triple w = lane < WARPS ? scratch[lane] : Triple{0, 0, 0};
+#pragma unroll
+    for (int d = 1; d < WARPS; d <<= 1) {
+      const Triple o = shfl_up(w, d);
+      if (lane >= d) w = add(o, w);
+    }
+    if (lane < WARPS) scratch[lane] = w;
+  }
+  __syncthreads();
+  Triple ex = shfl_up(inc, 1);
+  if (lane == 0) ex = {0, 0, 0};
+  if (warp > 0) ex = add(scratch[warp - 1], ex);
+  total = scratch[WARPS - 1];
+  return ex;
+}
+
+// ----------------------------------------------------------------------------
+// row-sized loads and stores, table lookups
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ int4 load_row(const unsigned char* p, int rb) {
+  int4 v = make_int4(0, 0, 0, 0);
+  switch (rb) {
+    case 16: v = __ldg(reinterpret_cast<const int4*>(p)); break;
+    case 8: {
+      const uint2 t = __ldg(reinterpret_cast<const uint2*>(p));
+      v.x = (int)t.x;
+      v.y = (int)t.y;
+    } break;
+    case 4: v.x = __ldg(reinterpret_cast<const int*>(p)); break;
+    case 2: v.x = __ldg(reinterpret_cast<const unsigned short*>(p)); break;
+    default: v.x = __ldg(p); break;
+  }
+  return v;
+}
+
+__device__ __forceinline__ void store_row(unsigned char* p, const int4& v, int rb) {
+  switch (rb) {
+    case 16: *reinterpret_cast<int4*>(p) = v; break;
+    case 8: *reinterpret_cast<uint2*>(p) = make_uint2((unsigned)v.x, (unsigned)v.y); break;
+    case 4: *reinterpret_cast<int*>(p) = v.x; break;
+    case 2: *reinterpret_cast<unsigned short*>(p) = (unsigned short)v.x; break;
+    default: *p = (unsigned char)v.x; break;
+  }
+}
+
+// Largest j in [0, cnt) with cup[j] <= r, given cup[0] <= r < cup[cnt].
+// It is never a zero-length sequence: cup[j + 1] > r.
+__device__ __forceinline__ int seq_of(const int32_t* cup, int cnt, int64_t r) {
+  int lo = 0, hi = cnt;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((int64_t)cup[mid] <= r) lo = mid;
+    else hi = mid;
+  }
+  return lo;
 }
 
 }  // namespace pseq

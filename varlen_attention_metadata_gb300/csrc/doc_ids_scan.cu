@@ -6,18 +6,23 @@
 // padding runs are segments, cu_seqlens ends at B*S, max_seqlen is the
 // longest segment.
 //
-// One pass over doc_ids.  Each CTA takes the next 4096-token tile (dynamic
-// tile index, so every tile it waits on is already running), flags the
-// boundaries in it, and summarises them as (count, first, last, largest
-// inner gap).  The summaries form an associative "followed by" operation,
-// so a decoupled look-back over the preceding tiles gives each tile its
+// One pass over doc_ids.  CTA t takes tile t (16384 tokens), flags the
+// boundaries in it and summarises them as (count, first, last, largest inner
+// gap) -- an associative "followed by" operation -- with a block scan.  A
+// decoupled look-back over the preceding tiles then gives the tile its
 // exclusive prefix: the output index of its first boundary and the position
-// of the boundary before it, which closes the segment that crosses into the
-// tile.  The largest gap over all tiles is max_seqlen, so the segment-length
-// maximum rides along with the scan and needs no second pass.  Boundaries
-// are compacted through shared memory and written with coalesced stores.
-// The last CTA to finish writes cu_seqlens[num_segments] and the info block
-// and clears the tile flags, so the workspace is zero again for the next call.
+// of the boundary before it, which closes the segment crossing into the tile.
+// The gap term makes max_seqlen a by-product of the scan.
+//
+// Every published summary is two 64-bit words, each carrying a valid bit, so
+// a single poll returns the summary itself: no flag-then-value round trip and
+// no release fence on the publishing side.  A look-back round polls 128
+// predecessors at once.  A map that fits one tile skips all of this.  Waits are bounded by a time limit
+// and report PSEQ_ERR_TIMEOUT.  Boundaries are compacted through shared
+// memory (tile-relative 16-bit positions) and stored coalesced.  The CTA that
+// finishes its look-back last writes cu_seqlens[num_segments] and the info
+// block and clears the summary words, so the workspace is zero again for the
+// next call.
 #include <mutex>
 
 #include "common.cuh"
@@ -25,11 +30,18 @@
 namespace pseq {
 namespace {
 
-constexpr int kThreads = 256;
+#ifndef PSEQ_SCAN_THREADS
+#define PSEQ_SCAN_THREADS 1024
+#endif
+#ifndef PSEQ_SCAN_ITEMS
+#define PSEQ_SCAN_ITEMS 16
+#endif
+constexpr int kThreads = PSEQ_SCAN_THREADS;
 constexpr int kWarps = kThreads / 32;
-constexpr int kItems = 16;
+constexpr int kItems = PSEQ_SCAN_ITEMS;
+constexpr int kPerLane = 4;  // look-back windows of 32 tiles polled together
 constexpr int kTile = kThreads * kItems;  // tokens per tile
-constexpr uint32_t kEmpty = 0, kAggregate = 1, kInclusive = 2;
+static_assert(kTile <= 65536, "tile-relative positions are 16-bit");
 
 // Boundaries inside a span of tokens: how many, the first and last boundary
 // position, and the largest distance between consecutive boundaries.
@@ -60,39 +72,60 @@ __device__ __forceinline__ Bounds shfl(const Bounds& v, int src) {
           __shfl_sync(~0u, v.gap, src)};
 }
 
-__device__ __forceinline__ int4 pack(const Bounds& b) { return make_int4(b.count, b.first, b.last, b.gap); }
-__device__ __forceinline__ Bounds unpack(const int4& v) { return {v.x, v.y, v.z, v.w}; }
+// A summary as two self-validating words: {valid, count, last} and
+// {valid, gap, first}.  count and gap are below 2^31, positions fit 32 bits
+// (-1 for "no boundary" round-trips through the unsigned field).
+constexpr unsigned long long kValid = 1ull << 63;
+
+__device__ __forceinline__ unsigned long long word_a(const Bounds& b) {
+  return kValid | ((unsigned long long)(unsigned)b.count << 32) | (unsigned)b.last;
+}
+__device__ __forceinline__ unsigned long long word_b(const Bounds& b) {
+  return kValid | ((unsigned long long)(unsigned)b.gap << 32) | (unsigned)b.first;
+}
+__device__ __forceinline__ Bounds from_words(unsigned long long a, unsigned long long b) {
+  return {(int)((a >> 32) & 0x7fffffffu), (int)(unsigned)b, (int)(unsigned)a, (int)((b >> 32) & 0x7fffffffu)};
+}
+
+__device__ __forceinline__ unsigned long long ld_word(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_word(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+// Increment that wraps back to 0 after `limit`, with acquire-release order.
+__device__ __forceinline__ unsigned inc_acq_rel(unsigned* p, unsigned limit) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(limit) : "memory");
+  return old;
+}
 
 struct Header {
-  unsigned int next_tile;  // dynamic tile index; wraps back to 0 after each call
-  unsigned int finished;   // tiles done; wraps back to 0 after each call
-  unsigned int gave_up;    // nonzero when some wait hit its time limit
-  unsigned int pad[29];
+  unsigned int finished;  // tiles done with their look-back; wraps back to 0 after each call
+  unsigned int gave_up;   // nonzero when some wait hit its time limit
+  unsigned int pad[30];
 };
 static_assert(sizeof(Header) == 128, "header is 128 bytes");
 
+// Per tile: its own summary and the inclusive one (everything up to it).
+struct Slot {
+  unsigned long long agg_a, agg_b, inc_a, inc_b;
+};
+static_assert(sizeof(Slot) == 32, "slot is 32 bytes");
+
 struct Workspace {
   Header* hdr;
-  uint32_t* status;  // [tiles]: kEmpty / kAggregate / kInclusive
-  int4* aggregate;   // [tiles]: the tile's own Bounds
-  int4* inclusive;   // [tiles]: Bounds of tiles 0..t
+  Slot* slots;  // [tiles]
 };
 
-size_t workspace_bytes(int64_t tiles) {
-  return sizeof(Header) + round_up(4 * (size_t)tiles, 16) + 32 * (size_t)tiles;
-}
+size_t workspace_bytes(int64_t tiles) { return sizeof(Header) + sizeof(Slot) * (size_t)tiles; }
 
 Workspace carve(void* base, int64_t tiles) {
   unsigned char* p = static_cast<unsigned char*>(base);
-  Workspace w;
-  w.hdr = reinterpret_cast<Header*>(p);
-  p += sizeof(Header);
-  w.status = reinterpret_cast<uint32_t*>(p);
-  p += round_up(4 * (size_t)tiles, 16);
-  w.aggregate = reinterpret_cast<int4*>(p);
-  p += 16 * (size_t)tiles;
-  w.inclusive = reinterpret_cast<int4*>(p);
-  return w;
+  (void)tiles;
+  return {reinterpret_cast<Header*>(p), reinterpret_cast<Slot*>(p + sizeof(Header))};
 }
 
 template <typename Id>
@@ -102,28 +135,20 @@ union Items {
 };
 
 template <typename Id, bool kVector>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
     doc_ids_scan_kernel(const Id* __restrict__ doc, int N, int S, int32_t* __restrict__ cu,
                         pseq_info* __restrict__ info, Workspace ws, int tiles, int64_t wait_ns,
                         int withhold) {
-  __shared__ int s_tile;
-  __shared__ int s_last_cta;
   __shared__ Bounds s_warp[kWarps];
   __shared__ Bounds s_prefix;
-  __shared__ int s_pos[kTile];
+  __shared__ int s_last_cta;
+  __shared__ unsigned short s_pos[kTile];
 
+  pdl_enter();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    unsigned t = atomicInc(&ws.hdr->next_tile, (unsigned)(tiles - 1));
-    if (t >= (unsigned)tiles) {  // the workspace was not zero-filled
-      atomicOr(&ws.hdr->gave_up, 2u);
-      t %= (unsigned)tiles;
-    }
-    s_tile = (int)t;
-  }
-  __syncthreads();
-  const int tile = s_tile;
-  const int64_t t0 = (int64_t)tile * kTile + (int64_t)tid * kItems;
+  const int tile = blockIdx.x;
+  const int64_t tile_base = (int64_t)tile * kTile;
+  const int64_t t0 = tile_base + (int64_t)tid * kItems;
 
   // ---- this thread's 16 tokens and the token to their left
   Items<Id> it;
@@ -138,7 +163,7 @@ __global__ void __launch_bounds__(kThreads)
   const Id left = (t0 > 0 && t0 < N) ? __ldg(doc + t0 - 1) : Id(0);
 
   // ---- boundary flags: row start, or a different index than the left token
-  unsigned flags = 0;
+  unsigned long long flags = 0;
   Bounds mine = none();
   int r = (int)(t0 % S);
 #pragma unroll
@@ -152,7 +177,7 @@ __global__ void __launch_bounds__(kThreads)
       else mine.first = ti;
       mine.last = ti;
       mine.count += 1;
-      flags |= 1u << k;
+      flags |= 1ull << k;
     }
     if (++r == S) r = 0;
   }
@@ -181,85 +206,140 @@ __global__ void __launch_bounds__(kThreads)
   if (warp > 0) before_me = join(s_warp[warp - 1], before_me);
   const Bounds tile_sum = s_warp[kWarps - 1];
 
+  // ---- one tile: no neighbours, no workspace
+  if (tiles == 1) {
+    int li = before_me.count;
+#pragma unroll
+    for (int k = 0; k < kItems; ++k)
+      if (flags & (1ull << k)) s_pos[li++] = (unsigned short)(t0 + k - tile_base);
+    __syncthreads();
+    for (int i = tid; i < tile_sum.count; i += kThreads) cu[i] = (int32_t)s_pos[i];
+    if (tid == 0) {
+      cu[tile_sum.count] = N;
+      *info = {PSEQ_OK, tile_sum.count, max(tile_sum.gap, N - tile_sum.last), N};
+    }
+    return;
+  }
+
   // ---- publish the tile summary, then look back for the exclusive prefix
   if (warp == 0) {
+    Slot* mine_slot = ws.slots + tile;
     Bounds prefix = none();
-    if (tile == 0) {
-      if (lane == 0 && withhold != 0) {
-        __stcg(&ws.inclusive[0], pack(tile_sum));
-        st_release(&ws.status[0], kInclusive);
-      }
-    } else {
+    if (tile > 0) {
       if (lane == 0 && withhold != tile) {
-        __stcg(&ws.aggregate[tile], pack(tile_sum));
-        st_release(&ws.status[tile], kAggregate);
+        st_word(&mine_slot->agg_a, word_a(tile_sum));
+        st_word(&mine_slot->agg_b, word_b(tile_sum));
       }
-      Bounds run = none();  // summary of the tiles between the window and this one
+      // Each round polls kPerLane windows of 32 predecessors at once (lane L
+      // of window w looks at tile j - 32w - L), waits until every one has
+      // published, and joins the tiles after the nearest inclusive summary.
+      Bounds run = none();  // summary of the tiles between the polled span and this one
       int j = tile - 1;
       bool gave_up = false;
       while (true) {
-        const int idx = j - lane;  // lane 0 looks at the nearest predecessor
-        uint32_t st = kInclusive;  // lanes before tile 0 stand for an empty prefix
-        Bounds b = none();
-        if (idx >= 0) {
-          st = ld_acquire(&ws.status[idx]);
-          if (st == kEmpty) {
-            const uint64_t start = global_ns();
-            do {
-              __nanosleep(32);
-              st = ld_acquire(&ws.status[idx]);
-            } while (st == kEmpty && (int64_t)(global_ns() - start) < wait_ns);
+        Bounds b[kPerLane];
+        bool incl[kPerLane], done[kPerLane];
+#pragma unroll
+        for (int w = 0; w < kPerLane; ++w) {
+          b[w] = none();
+          incl[w] = true;  // before tile 0: an empty inclusive prefix
+          done[w] = j - 32 * w - lane < 0;
+        }
+        int polls = 0;
+        uint64_t start = 0;
+        while (true) {
+          bool all_done = true;
+#pragma unroll
+          for (int w = 0; w < kPerLane; ++w) {
+            if (done[w]) continue;
+            const Slot* sl = ws.slots + (j - 32 * w - lane);
+            const unsigned long long ia = ld_word(&sl->inc_a), ib = ld_word(&sl->inc_b);
+            const unsigned long long aa = ld_word(&sl->agg_a), ab = ld_word(&sl->agg_b);
+            if (ia & ib & kValid) {
+              b[w] = from_words(ia, ib);
+              done[w] = true;
+            } else if (aa & ab & kValid) {
+              b[w] = from_words(aa, ab);
+              incl[w] = false;
+              done[w] = true;
+            } else {
+              all_done = false;
+            }
           }
-          if (st == kEmpty) {
-            gave_up = true;  // treat as an empty inclusive prefix and finish
-            st = kInclusive;
-          } else {
-            b = unpack(st == kInclusive ? __ldcg(&ws.inclusive[idx]) : __ldcg(&ws.aggregate[idx]));
+          if (all_done) break;
+          if (polls == 0) {
+            start = global_ns();
+          } else if ((int64_t)(global_ns() - start) >= wait_ns) {
+            gave_up = true;  // treat what is missing as an empty inclusive prefix and finish
+#pragma unroll
+            for (int w = 0; w < kPerLane; ++w)
+              if (!done[w]) {
+                b[w] = none();
+                incl[w] = true;
+                done[w] = true;
+              }
+            break;
+          }
+          if (++polls > 64) __nanosleep(64);
+        }
+        // nearest inclusive summary: lowest window, then lowest lane
+        int stop_w = kPerLane, stop_l = 32;
+#pragma unroll
+        for (int w = kPerLane - 1; w >= 0; --w) {
+          const unsigned m = __ballot_sync(~0u, incl[w]);
+          if (m) {
+            stop_w = w;
+            stop_l = __ffs(m) - 1;
           }
         }
-        const unsigned stop_mask = __ballot_sync(~0u, st == kInclusive);
-        const int stop = stop_mask ? __ffs(stop_mask) - 1 : 32;
-        Bounds win = none();
-        for (int L = (stop < 32 ? stop : 31); L >= 0; --L) win = join(win, shfl(b, L));
-        run = join(win, run);
-        if (stop < 32) break;
-        j -= 32;
+        // join from the farthest counted tile to the nearest one
+        Bounds span = none();
+        for (int w = (stop_w < kPerLane ? stop_w : kPerLane - 1); w >= 0; --w) {
+          const int top = w == stop_w ? stop_l : 31;
+          for (int L = top; L >= 0; --L) span = join(span, shfl(b[w], L));
+        }
+        run = join(span, run);
+        if (stop_w < kPerLane) break;
+        j -= 32 * kPerLane;
       }
       if (__any_sync(~0u, gave_up) && lane == 0) atomicOr(&ws.hdr->gave_up, 1u);
       prefix = run;
-      if (lane == 0 && withhold != tile) {
-        __stcg(&ws.inclusive[tile], pack(join(prefix, tile_sum)));
-        st_release(&ws.status[tile], kInclusive);
-      }
     }
-    if (lane == 0) s_prefix = prefix;
+    if (lane == 0) {
+      if (withhold != tile) {
+        const Bounds all = join(prefix, tile_sum);
+        st_word(&mine_slot->inc_a, word_a(all));
+        st_word(&mine_slot->inc_b, word_b(all));
+      }
+      s_prefix = prefix;
+      // this CTA reads no more summary words: count it finished (release
+      // orders the words above; the last one to arrive acquires them all)
+      s_last_cta = inc_acq_rel(&ws.hdr->finished, (unsigned)(tiles - 1)) == (unsigned)(tiles - 1);
+    }
   }
 
   // ---- compact this tile's boundary positions and store them
   int li = before_me.count;
 #pragma unroll
   for (int k = 0; k < kItems; ++k)
-    if (flags & (1u << k)) s_pos[li++] = (int)(t0 + k);
+    if (flags & (1ull << k)) s_pos[li++] = (unsigned short)(t0 + k - tile_base);
   __syncthreads();
   const int base = s_prefix.count;
   if (base >= 0 && base <= N - tile_sum.count) {
-    for (int i = tid; i < tile_sum.count; i += kThreads) cu[base + i] = s_pos[i];
+    for (int i = tid; i < tile_sum.count; i += kThreads) cu[base + i] = (int32_t)(tile_base + s_pos[i]);
   } else if (tid == 0) {
-    atomicOr(&ws.hdr->gave_up, 2u);  // only reachable from a corrupt workspace
+    atomicOr(&ws.hdr->gave_up, 2u);  // only reachable from a workspace that was not zero-filled
   }
-
-  // ---- the last CTA to finish closes the array and resets the workspace
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last_cta = atomicInc(&ws.hdr->finished, (unsigned)(tiles - 1)) == (unsigned)(tiles - 1);
-  __syncthreads();
   if (!s_last_cta) return;
-  __threadfence();
+
+  // ---- last CTA: close the array, report, and clear the summary words
   if (tid == 0) {
-    const Bounds all = unpack(__ldcg(&ws.inclusive[tiles - 1]));
+    const Slot* sl = ws.slots + (tiles - 1);
+    const unsigned long long ia = ld_word(&sl->inc_a), ib = ld_word(&sl->inc_b);
     const unsigned failed = atomicExch(&ws.hdr->gave_up, 0u);
+    const Bounds all = from_words(ia, ib);
     pseq_info out;
-    if (failed || all.count < 1 || all.count > N) {
+    if (failed || !(ia & ib & kValid) || all.count < 1 || all.count > N) {
       out = {(failed & 2u) ? PSEQ_ERR_ARG : PSEQ_ERR_TIMEOUT, 0, 0, N};
     } else {
       cu[all.count] = N;
@@ -267,25 +347,31 @@ __global__ void __launch_bounds__(kThreads)
     }
     *info = out;
   }
-  for (int i = tid; i < tiles; i += kThreads) ws.status[i] = kEmpty;
+  unsigned long long* words = reinterpret_cast<unsigned long long*>(ws.slots);
+  for (int i = tid; i < 4 * tiles; i += kThreads) words[i] = 0ull;
 }
 
 __global__ void empty_map_kernel(int32_t* cu, pseq_info* info) {
+  pdl_enter();
   cu[0] = 0;
   *info = {PSEQ_OK, 0, 0, 0};
 }
 
 template <typename Id>
-cudaError_t launch_scan(const void* doc, int N, int S, int32_t* cu, pseq_info* info, Workspace ws,
-                        int tiles, cudaStream_t st) {
+cudaError_t launch_scan(const void* doc, int N, int S, int32_t* cu, pseq_info* info, Workspace ws, int tiles,
+                        cudaStream_t st) {
   const Id* d = static_cast<const Id*>(doc);
   const int64_t wait = wait_limit_ns();
   const int withhold = (int)(withhold_tile() < 0 ? -1 : (withhold_tile() > INT32_MAX ? -1 : withhold_tile()));
   if (aligned(doc, 16))
-    doc_ids_scan_kernel<Id, true><<<tiles, kThreads, 0, st>>>(d, N, S, cu, info, ws, tiles, wait, withhold);
-  else
-    doc_ids_scan_kernel<Id, false><<<tiles, kThreads, 0, st>>>(d, N, S, cu, info, ws, tiles, wait, withhold);
-  return cudaSuccess;
+    return launch_pdl(doc_ids_scan_kernel<Id, true>, dim3(tiles), dim3(kThreads), 0, st, d, N, S, cu, info, ws,
+                      tiles, wait, withhold);
+  return launch_pdl(doc_ids_scan_kernel<Id, false>, dim3(tiles), dim3(kThreads), 0, st, d, N, S, cu, info, ws, tiles,
+                    wait, withhold);
+}
+
+cudaError_t launch_empty_map(int32_t* cu, pseq_info* info, cudaStream_t st) {
+  return launch_pdl(empty_map_kernel, dim3(1), dim3(1), 0, st, cu, info);
 }
 
 }  // namespace
@@ -316,8 +402,9 @@ extern "C" pseq_status pseq_from_doc_ids(const void* doc_ids, int32_t id_bytes, 
     return fail(PSEQ_ERR_ARG, "pseq_from_doc_ids: misaligned pointer");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (N == 0) {
-    empty_map_kernel<<<1, 1, 0, st>>>(cu_seqlens, info);
+    const cudaError_t e = launch_empty_map(cu_seqlens, info, st);
     count_launches(1);
+    if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "pseq_from_doc_ids: %s", cudaGetErrorString(e));
     return check_launch("pseq_from_doc_ids");
   }
   const int64_t tiles = (N + kTile - 1) / kTile;
@@ -325,11 +412,11 @@ extern "C" pseq_status pseq_from_doc_ids(const void* doc_ids, int32_t id_bytes, 
   if (!workspace || ws_bytes < need || !aligned(workspace, 16))
     return fail(PSEQ_ERR_ARG, "pseq_from_doc_ids: workspace needs %zu bytes, 16-byte aligned (got %zu)", need, ws_bytes);
   Workspace ws = carve(workspace, tiles);
-  if (id_bytes == 4)
-    launch_scan<int32_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st);
-  else
-    launch_scan<int64_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st);
+  const cudaError_t e = id_bytes == 4
+                            ? launch_scan<int32_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st)
+                            : launch_scan<int64_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st);
   count_launches(1);
+  if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "pseq_from_doc_ids: %s", cudaGetErrorString(e));
   return check_launch("pseq_from_doc_ids");
 }
 
@@ -348,7 +435,7 @@ namespace {
 
 constexpr int64_t kStaticMaxTokens = PSEQ_STATIC_MAX_TOKENS;  // B*S limit of the static scratch
 constexpr int64_t kStaticMaxTiles = kStaticMaxTokens / kTile;
-constexpr size_t kStaticBytes = sizeof(Header) + ((4 * kStaticMaxTiles + 15) / 16) * 16 + 32 * kStaticMaxTiles;
+constexpr size_t kStaticBytes = sizeof(Header) + sizeof(Slot) * kStaticMaxTiles;
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
 
@@ -393,25 +480,25 @@ extern "C" pseq_status pseq_from_doc_ids_static(const void* doc_ids, int32_t id_
     return fail(PSEQ_ERR_ARG, "%s: misaligned pointer", fn);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (N == 0) {
-    empty_map_kernel<<<1, 1, 0, st>>>(cu_seqlens, info);
+    const cudaError_t e = launch_empty_map(cu_seqlens, info, st);
     count_launches(1);
+    if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
     return check_launch(fn);
   }
   void* scratch = nullptr;
   pseq_status s = static_scratch(&scratch);
   if (s != PSEQ_OK) return s;
   const int64_t tiles = (N + kTile - 1) / kTile;
-  // The counters and tile flags must start at zero.  A completed call leaves
-  // them zero, but clear them anyway so an interrupted earlier call cannot leak
-  // into this one.
-  const size_t clear = sizeof(Header) + round_up(4 * (size_t)tiles, 16);
+  // The counters and summary words must start at zero.  A completed call
+  // leaves them zero, but clear them anyway so an interrupted earlier call
+  // cannot leak into this one.
+  const size_t clear = workspace_bytes(tiles);
   cudaError_t e = cudaMemsetAsync(scratch, 0, clear, st);
   if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: cudaMemsetAsync: %s", fn, cudaGetErrorString(e));
   Workspace ws = carve(scratch, tiles);
-  if (id_bytes == 4)
-    launch_scan<int32_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st);
-  else
-    launch_scan<int64_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st);
+  e = id_bytes == 4 ? launch_scan<int32_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st)
+                    : launch_scan<int64_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st);
   count_launches(1);
+  if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
   return check_launch(fn);
 }

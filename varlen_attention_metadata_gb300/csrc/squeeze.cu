@@ -6,14 +6,20 @@
 // lengths) and "Loader packs" (the last padded boundary stretched to the pack
 // capacity).
 //
-// squeeze_meta_kernel gives each bin one warp: a chunked warp scan over the
-// bin's members computes both cumulative sums, the slot where each member
-// starts, and the bin's checks.  squeeze_copy_kernel (programmatic dependent
-// launch) tiles every output row into equal chunks; a CTA finds the member
-// owning its first slot with a 32-way warp search and walks the members of
-// its chunk: real tokens are one contiguous block copy from the source row,
-// padding slots one block fill, and the padding mask is written alongside.
-// Every output slot is written exactly once.
+// Fused path (up to kFusedMaxMembers members, one launch): a grid of
+// (row chunk, bin) CTAs.  Every CTA scans its own bin's members into shared
+// memory -- padded lengths, both cumulative sums, the slot where each member
+// starts -- and then writes each slot of its chunk once: one thread per slot
+// looks its member up in the table and either loads the source token or
+// writes pad_value, with the padding mask alongside.  The first chunk of a bin
+// writes the bin's cu arrays; CTA (0, 0) also makes one pass over all members
+// to fold every bin's checks into the info block.
+//
+// Two-kernel path (larger inputs): squeeze_meta_kernel gives each bin one
+// warp (chunked warp scan); squeeze_copy_kernel (programmatic dependent
+// launch) walks the members of its chunk: real tokens are one contiguous
+// block copy from the source row, padding slots one block fill.  Every
+// output slot is written exactly once.
 #include "common.cuh"
 
 namespace pseq {
@@ -22,6 +28,9 @@ namespace {
 constexpr int kMetaThreads = 256;
 constexpr int kMetaWarps = kMetaThreads / 32;
 constexpr int kCopyThreads = 512;
+constexpr int kFusedThreads = 512;
+constexpr int kFusedMaxMembers = 1024;
+constexpr int kSlotsPerThread = 4;
 
 struct Workspace {
   int4* bin_stat;    // [num_bins] {status, padded total, largest real, members}
@@ -60,7 +69,7 @@ struct MetaArgs {
 };
 
 __global__ void __launch_bounds__(kMetaThreads) squeeze_meta_kernel(MetaArgs a, Workspace ws) {
-  pdl_launch_dependents();
+  pdl_enter();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.x * kMetaWarps + warp;
   if (b >= a.num_bins) return;
@@ -153,7 +162,7 @@ __device__ __forceinline__ int warp_find(const int32_t* dst, int lo, int hi, int
 
 __global__ void __launch_bounds__(kCopyThreads) squeeze_copy_kernel(CopyArgs c, Workspace ws) {
   __shared__ int s_value, s_capacity, s_longest, s_widest, s_first;
-  pdl_wait();
+  pdl_enter();
   const int tid = threadIdx.x;
   const int b = blockIdx.y;
   if (blockIdx.x == 0 && b == 0) {
@@ -214,7 +223,167 @@ __global__ void __launch_bounds__(kCopyThreads) squeeze_copy_kernel(CopyArgs c, 
   }
 }
 
-__global__ void empty_squeeze_kernel(pseq_info* info) { *info = {PSEQ_OK, 0, 0, 0}; }
+struct FusedArgs {
+  const unsigned char* src;
+  const int64_t* real;
+  const int32_t* off;
+  const int32_t* mem;
+  int num_bins, M;
+  int64_t N, W, multiple, capacity, width, pad_value;
+  int stretch, elem_bytes;
+  unsigned char* out;  // may be NULL (metadata only)
+  uint8_t* mask;       // may be NULL
+  int32_t* cu;
+  int32_t* cup;
+  pseq_info* info;
+};
+
+__device__ __forceinline__ bool offsets_bad(const FusedArgs& a, int b, int lo, int hi) {
+  return (b == 0 && lo != 0) || (b == a.num_bins - 1 && hi != a.M) || lo < 0 || hi > a.M || hi <= lo;
+}
+
+// CTA (0, 0): one pass over every member to fold all bins' checks into info.
+__device__ void squeeze_info_pass(const FusedArgs& a, int32_t* s_off, unsigned long long* s_tot) {
+  __shared__ int s_value, s_capacity, s_longest, s_widest;
+  const int tid = threadIdx.x;
+  if (tid == 0) s_value = s_capacity = s_longest = s_widest = 0;
+  for (int i = tid; i <= a.num_bins; i += kFusedThreads) s_off[i] = __ldg(a.off + i);
+  for (int i = tid; i < a.num_bins; i += kFusedThreads) s_tot[i] = 0ull;
+  __syncthreads();
+  for (int b = tid; b < a.num_bins; b += kFusedThreads)
+    if (offsets_bad(a, b, s_off[b], s_off[b + 1])) s_value = 1;
+  for (int e = tid; e < a.M; e += kFusedThreads) {
+    const int b = seq_of(s_off, a.num_bins, e);
+    const int i = __ldg(a.mem + e);
+    if (i < 0 || i >= a.N) {
+      s_value = 1;
+      continue;
+    }
+    const long long real = __ldg(a.real + i);
+    if (real < 0 || real > a.W) {
+      s_value = 1;
+      continue;
+    }
+    atomicAdd(&s_tot[b], (unsigned long long)((real + a.multiple - 1) / a.multiple * a.multiple));
+    atomicMax(&s_longest, (int)real);
+  }
+  __syncthreads();
+  for (int b = tid; b < a.num_bins; b += kFusedThreads) {
+    const unsigned long long t = s_tot[b];
+    if (t > (unsigned long long)a.capacity || (a.out && t > (unsigned long long)a.width)) s_capacity = 1;
+    atomicMax(&s_widest, (int)min(t, (unsigned long long)INT32_MAX));
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int status = s_value ? PSEQ_ERR_VALUE : (s_capacity ? PSEQ_ERR_CAPACITY : PSEQ_OK);
+    *a.info = status == PSEQ_OK ? pseq_info{PSEQ_OK, a.M, s_longest, s_widest} : pseq_info{status, 0, 0, 0};
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kFusedThreads) squeeze_fused_kernel(const __grid_constant__ FusedArgs a) {
+  __shared__ int32_t s_dst[kFusedMaxMembers + 1];
+  __shared__ int32_t s_real[kFusedMaxMembers];
+  __shared__ int32_t s_src[kFusedMaxMembers];
+  __shared__ int32_t s_off[kFusedMaxMembers + 1];
+  __shared__ unsigned long long s_tot[kFusedMaxMembers];
+  __shared__ Triple scratch[kFusedThreads / 32];
+  __shared__ int s_bad;
+  pdl_enter();
+  const int tid = threadIdx.x;
+  const int b = blockIdx.y;
+  if (blockIdx.x == 0 && b == 0) squeeze_info_pass(a, s_off, s_tot);
+  const int lo = __ldg(a.off + b), hi = __ldg(a.off + b + 1);
+  if (offsets_bad(a, b, lo, hi) || hi - lo > kFusedMaxMembers) return;
+  const int n = hi - lo;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  // scan the bin's members: slot where each starts, both cumulative sums
+  Triple carry = {0, 0, 0};
+  for (int base = 0; base < n; base += kFusedThreads) {
+    const int j = base + tid;
+    long long real = 0, padded = 0;
+    int src = 0;
+    if (j < n) {
+      src = __ldg(a.mem + lo + j);
+      if (src < 0 || src >= a.N) {
+        s_bad = 1;
+      } else {
+        real = __ldg(a.real + src);
+        if (real < 0 || real > a.W) {
+          s_bad = 1;
+          real = 0;
+        }
+      }
+      padded = (real + a.multiple - 1) / a.multiple * a.multiple;
+    }
+    Triple total;
+    const Triple ex = block_exclusive<kFusedThreads / 32>({0, real, padded}, scratch, total);
+    if (j < n) {
+      const long long R = carry.real + ex.real, Pd = carry.padded + ex.padded;
+      s_dst[j] = (int32_t)Pd;
+      s_real[j] = (int32_t)real;
+      s_src[j] = src;
+      if (blockIdx.x == 0) {
+        a.cu[lo + b + j] = (int32_t)R;
+        a.cup[lo + b + j] = (int32_t)Pd;
+      }
+    }
+    carry = add(carry, total);
+  }
+  const long long total_pad = carry.padded;
+  if (tid == 0) {
+    s_dst[n] = (int32_t)min(total_pad, (long long)INT32_MAX);
+    if (blockIdx.x == 0) {
+      a.cu[hi + b] = (int32_t)carry.real;
+      a.cup[hi + b] = a.stretch ? (int32_t)a.capacity : (int32_t)total_pad;
+    }
+  }
+  __syncthreads();
+  if (s_bad || total_pad > a.capacity || !a.out || total_pad > a.width) return;
+  // every slot of this chunk, once
+  const int eb = a.elem_bytes;
+  const int64_t chunk = (int64_t)kFusedThreads * kSlotsPerThread;
+  const int64_t c0 = (int64_t)blockIdx.x * chunk;
+  const int64_t c1 = min(c0 + chunk, a.width);
+  unsigned char* row = a.out + (int64_t)b * a.width * eb;
+  uint8_t* mrow = a.mask ? a.mask + (int64_t)b * a.width : nullptr;
+  int4 v[kSlotsPerThread];
+  bool pad[kSlotsPerThread];
+  int4 pv = make_int4(0, 0, 0, 0);
+  {
+    const uint64_t p = (uint64_t)a.pad_value;
+    pv.x = (int)(uint32_t)p;
+    pv.y = (int)(uint32_t)(p >> 32);
+  }
+#pragma unroll
+  for (int q = 0; q < kSlotsPerThread; ++q) {
+    const int64_t t = c0 + tid + (int64_t)q * kFusedThreads;
+    pad[q] = true;
+    v[q] = pv;
+    if (t < c1 && t < total_pad) {
+      const int j = seq_of(s_dst, n, t);
+      const int64_t off = t - s_dst[j];
+      if (off < s_real[j]) {
+        pad[q] = false;
+        v[q] = load_row(a.src + ((int64_t)s_src[j] * a.W + off) * eb, eb);
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < kSlotsPerThread; ++q) {
+    const int64_t t = c0 + tid + (int64_t)q * kFusedThreads;
+    if (t < c1) {
+      store_row(row + t * eb, v[q], eb);
+      if (mrow) mrow[t] = pad[q] ? 1 : 0;
+    }
+  }
+}
+
+__global__ void empty_squeeze_kernel(pseq_info* info) {
+  pdl_enter();
+  *info = {PSEQ_OK, 0, 0, 0};
+}
 
 }  // namespace
 }  // namespace pseq
@@ -259,13 +428,42 @@ extern "C" pseq_status pack_squeeze(const void* src, int64_t N, int64_t W, int32
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (num_bins == 0) {
     if (num_members != 0) return fail(PSEQ_ERR_ARG, "%s: members without bins", fn);
-    empty_squeeze_kernel<<<1, 1, 0, st>>>(info);
+    const cudaError_t e = launch_pdl(empty_squeeze_kernel, dim3(1), dim3(1), 0, st, info);
     count_launches(1);
+    if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
     return check_launch(fn);
   }
   const size_t need = workspace_bytes(num_members, num_bins);
   if (!workspace || workspace_bytes_ < need || !aligned(workspace, 16))
     return fail(PSEQ_ERR_ARG, "%s: workspace needs %zu bytes, 16-byte aligned (got %zu)", fn, need, workspace_bytes_);
+  if (num_members <= kFusedMaxMembers && num_bins <= kFusedMaxMembers) {
+    FusedArgs a = {};
+    a.src = static_cast<const unsigned char*>(src);
+    a.real = real_lens;
+    a.off = bin_offsets;
+    a.mem = bin_members;
+    a.num_bins = (int)num_bins;
+    a.M = (int)num_members;
+    a.N = N;
+    a.W = W;
+    a.multiple = multiple;
+    a.capacity = capacity;
+    a.width = width;
+    a.pad_value = pad_value;
+    a.stretch = stretch_to_capacity ? 1 : 0;
+    a.elem_bytes = elem_bytes;
+    a.out = static_cast<unsigned char*>(out);
+    a.mask = padding_mask;
+    a.cu = cu_seqlens;
+    a.cup = cu_seqlens_padded;
+    a.info = info;
+    const int64_t chunk = (int64_t)kFusedThreads * kSlotsPerThread;
+    const unsigned gx = out && width > 0 ? (unsigned)((width + chunk - 1) / chunk) : 1u;
+    const cudaError_t e = launch_pdl(squeeze_fused_kernel, dim3(gx, (unsigned)num_bins), dim3(kFusedThreads), 0, st, a);
+    count_launches(1);
+    if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    return check_launch(fn);
+  }
   Workspace ws = carve(workspace, num_members, num_bins);
 
   MetaArgs m = {};
@@ -283,8 +481,10 @@ extern "C" pseq_status pack_squeeze(const void* src, int64_t N, int64_t W, int32
   m.check_width = out ? 1 : 0;
   m.cu = cu_seqlens;
   m.cup = cu_seqlens_padded;
-  squeeze_meta_kernel<<<(unsigned)((num_bins + kMetaWarps - 1) / kMetaWarps), kMetaThreads, 0, st>>>(m, ws);
+  cudaError_t e = launch_pdl(squeeze_meta_kernel, dim3((unsigned)((num_bins + kMetaWarps - 1) / kMetaWarps)),
+                             dim3(kMetaThreads), 0, st, m, ws);
   count_launches(1);
+  if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
   pseq_status s = check_launch(fn);
   if (s != PSEQ_OK) return s;
 
@@ -315,7 +515,7 @@ extern "C" pseq_status pack_squeeze(const void* src, int64_t N, int64_t W, int32
   } else {
     c.chunk = 1;
   }
-  cudaError_t e = launch_pdl(squeeze_copy_kernel, grid, dim3(kCopyThreads), 0, st, c, ws);
+  e = launch_pdl(squeeze_copy_kernel, grid, dim3(kCopyThreads), 0, st, c, ws);
   count_launches(1);
   if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
   return check_launch(fn);

@@ -1,33 +1,46 @@
-// BSHD -> THD conversion: thd_meta, thd_gather, thd_from_batch,
+// BSHD -> THD conversion: thd_from_batch, thd_meta, thd_gather,
 // thd_padding_mask.
 //
 // Follows NeMo AutoModel v0.5 "nemo_automodel.components.distributed.thd_utils":
 // process_input_for_thd (description, Example, Parameters, Returns) and
 // _thd_padding_mask.
 //
-// thd_meta runs in one CTA: the length tables are small (B * num_packs
-// entries), so a chunked block scan over them in row-major order drops the
-// filler entries, computes both cumulative sums (int64 running totals), the
-// in-row source offset of every kept sequence, the absorption gate,
-// pad_between_seqs and max_seqlen, and leaves the per-sequence layout
-// (source token, stream start, real length) in the workspace.
+// The length tables are small (B * num_packs entries) and the streams large,
+// so the metadata is one block-wide scan and the data movement is a grid-wide
+// copy.  Two shapes:
 //
-// thd_gather is a persistent grid launched with programmatic dependent
-// launch, so its CTAs are resident before thd_meta ends.  Each CTA owns an
-// equal slice of stream rows, finds the sequence owning its first row with a
-// 32-way warp search, and walks the sequences of its slice.  A sequence's
-// rows are contiguous in the source and in the stream, so every piece is one
-// contiguous block copy per field and plane (16-byte streaming loads and
-// stores when source and destination share their 16-byte alignment).  The
-// same CTA writes the padding mask of its slice.
+//  * fused (tables of up to kFusedMaxEntries entries, the usual case): one
+//    launch.  Every CTA scans the whole table into shared memory -- filter,
+//    both cumulative sums, in-row source offsets -- so it knows the stream
+//    layout without waiting on anyone; CTA 0 also writes cu_seqlens,
+//    cu_seqlens_padded, pad_between_seqs and the info block.  Each CTA then
+//    moves an equal slice of stream rows.
+//  * two kernels (larger tables, and the explicit thd_meta / thd_gather
+//    calls): thd_meta_kernel runs the scan in one CTA and leaves the layout in
+//    the workspace; thd_gather_kernel (programmatic dependent launch) streams
+//    the layout into shared memory in batches and moves its slice.
+//
+// Moving a slice: sequence pieces are contiguous in the source row and in the
+// stream.  Fields whose rows are one aligned access of at most 16 bytes (ids,
+// labels, positions) go row by row -- one thread per row, every (field,
+// plane) load issued before any store.  Wide rows (embeddings) go piece by
+// piece as block copies with 16-byte streaming loads and stores.  The padding
+// mask of the slice is written by the same CTA.  Grids are sized from the
+// occupancy calculator so they run in a single wave.
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "common.cuh"
 
 namespace pseq {
 namespace {
 
 constexpr int kMetaThreads = 1024;
-constexpr int kMetaWarps = kMetaThreads / 32;
-constexpr int kGatherThreads = 512;
+constexpr int kRowThreads = 512;
+constexpr int kFusedMaxEntries = 2048;
+constexpr int kTableBatch = 1024;
+constexpr int kMaxJobs = 16;
 
 struct Header {
   int32_t status;
@@ -40,10 +53,10 @@ static_assert(sizeof(Header) == 128, "header is 128 bytes");
 
 struct Workspace {
   Header* hdr;
-  int64_t* seq_src;  // [E]  source token (b*S + o) of the sequence's first slot
-  int32_t* seq_cup;  // [E+1] stream start of each sequence; [n] = T
-  int32_t* seq_real; // [E]
-  int64_t* row_pfx;  // [B]  padded prefix at each row's first entry
+  int64_t* seq_src;   // [E]   source token (b*S + o) of the sequence's first slot
+  int32_t* seq_cup;   // [E+1] stream start of each sequence; [n] = T
+  int32_t* seq_real;  // [E]
+  int64_t* row_pfx;   // [B]   padded prefix at each row's first entry
 };
 
 size_t workspace_bytes(int64_t B, int64_t E) {
@@ -64,6 +77,7 @@ Workspace carve(P base_, int64_t B, int64_t E) {
   w.seq_real = reinterpret_cast<int32_t*>(p);
   p += round_up(4 * (size_t)E, 16);
   w.row_pfx = reinterpret_cast<int64_t*>(p);
+  (void)B;
   return w;
 }
 
@@ -75,169 +89,267 @@ struct MetaArgs {
   int64_t pad_value;
   int has_filler;
   int absorb;
-  int32_t* cu;          // may be NULL (mask-only use)
-  int32_t* cu_padded;   // may be NULL
-  uint8_t* pad_between; // may be NULL
+  int32_t* cu;           // may be NULL (mask-only use)
+  int32_t* cu_padded;    // may be NULL
+  uint8_t* pad_between;  // may be NULL
   pseq_info* info;
-  int64_t fixed_total;  // >= 0: mask length and info.total (thd_padding_mask)
+  int64_t fixed_total;   // >= 0: mask length and info.total (thd_padding_mask)
 };
 
-struct Triple {
-  int count;
+// ----------------------------------------------------------------------------
+// the length scan
+// ----------------------------------------------------------------------------
+struct ScanFlags {
+  int bad, mismatch, last_mismatch, max_real;
+};
+
+struct ScanResult {
+  int n;
   long long real, padded;
 };
 
-__device__ __forceinline__ Triple add(const Triple& a, const Triple& b) {
-  return {a.count + b.count, a.real + b.real, a.padded + b.padded};
-}
-
-// Exclusive scan of one Triple per thread over the whole block; `total`
-// receives the block sum.  Uses `scratch` (kMetaWarps entries).
-__device__ __forceinline__ Triple block_exclusive(Triple x, Triple* scratch, Triple& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  Triple inc = x;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    Triple o = {__shfl_up_sync(~0u, inc.count, d), __shfl_up_sync(~0u, inc.real, d),
-                __shfl_up_sync(~0u, inc.padded, d)};
-    if (lane >= d) inc = add(o, inc);
-  }
-  if (lane == 31) scratch[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    Triple w = scratch[lane];  // kMetaWarps == 32
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      Triple o = {__shfl_up_sync(~0u, w.count, d), __shfl_up_sync(~0u, w.real, d),
-                  __shfl_up_sync(~0u, w.padded, d)};
-      if (lane >= d) w = add(o, w);
-    }
-    scratch[lane] = w;
-  }
-  __syncthreads();
-  Triple ex = {__shfl_up_sync(~0u, inc.count, 1), __shfl_up_sync(~0u, inc.real, 1),
-               __shfl_up_sync(~0u, inc.padded, 1)};
-  if (lane == 0) ex = {0, 0, 0};
-  if (warp > 0) ex = add(scratch[warp - 1], ex);
-  total = scratch[kMetaWarps - 1];
-  return ex;
-}
-
-__global__ void __launch_bounds__(kMetaThreads) thd_meta_kernel(MetaArgs a, Workspace ws) {
-  static_assert(kMetaWarps == 32, "scan assumes 32 warps");
-  __shared__ Triple s_scan[kMetaWarps];
-  __shared__ int s_bad, s_mismatch, s_last_mismatch, s_max_real;
-  pdl_launch_dependents();  // the gather may start its prologue now
-
+// Walk the tables in row-major order, dropping filler entries, and call
+// put(k, b, o, real, padded, R, Pd) for kept entry k of row b at in-row
+// offset o, where R and Pd are the real and padded sums of the kept entries
+// before it.  Every thread returns the same totals; the flags are in *fl.
+template <int THREADS, typename Put>
+__device__ ScanResult scan_lengths(const MetaArgs& a, int64_t* row_pfx, Triple* scratch, ScanFlags* fl, Put put) {
   const int tid = threadIdx.x;
-  if (tid == 0) {
-    s_bad = 0;
-    s_mismatch = 0;
-    s_last_mismatch = -1;
-    s_max_real = 0;
-  }
+  if (tid == 0) *fl = {0, 0, -1, 0};
   __syncthreads();
   const int E = a.B * a.P;
   Triple carry = {0, 0, 0};
-  for (int base = 0; base < E; base += kMetaThreads) {
+  for (int base = 0; base < E; base += THREADS) {
     const int e = base + tid;
     const bool valid = e < E;
     long long real = 0, padded = 0;
     bool keep = false, bad = false;
     if (valid) {
-      real = a.real[e];
-      padded = a.padded ? a.padded[e] : real;
+      real = __ldg(a.real + e);
+      padded = a.padded ? __ldg(a.padded + e) : real;
       const bool real_filler = a.has_filler && real == a.pad_value;
       const bool padded_filler = a.has_filler && padded == a.pad_value;
-      if (real_filler != padded_filler) bad = true;
-      else if (!real_filler) {
+      if (real_filler != padded_filler) {
+        bad = true;
+      } else if (!real_filler) {
         keep = true;
         if (real < 0 || padded < real) bad = true;
       }
     }
     Triple total;
-    const Triple ex = block_exclusive({keep ? 1 : 0, keep ? real : 0, keep ? padded : 0}, s_scan, total);
+    const Triple ex = block_exclusive<THREADS / 32>({keep ? 1 : 0, keep ? real : 0, keep ? padded : 0}, scratch,
+                                                    total);
     const int k = carry.count + ex.count;
     const long long R = carry.real + ex.real;
     const long long Pd = carry.padded + ex.padded;
     const int b = valid ? e / a.P : 0;
-    if (valid && e % a.P == 0) ws.row_pfx[b] = Pd;
+    if (valid && e % a.P == 0) row_pfx[b] = Pd;
     __syncthreads();
     if (keep) {
-      const long long o = Pd - ws.row_pfx[b];
+      const long long o = Pd - row_pfx[b];
       if (o + padded > a.S) bad = true;
-      ws.seq_src[k] = (long long)b * a.S + o;
-      ws.seq_real[k] = (int32_t)real;
-      ws.seq_cup[k] = (int32_t)Pd;
-      if (a.cu) a.cu[k] = (int32_t)R;
-      if (a.cu_padded) a.cu_padded[k] = (int32_t)Pd;
+      put(k, b, o, real, padded, R, Pd);
       if (real != padded) {
-        atomicAdd(&s_mismatch, 1);
-        atomicMax(&s_last_mismatch, k);
+        atomicAdd(&fl->mismatch, 1);
+        atomicMax(&fl->last_mismatch, k);
       }
-      atomicMax(&s_max_real, (int)min(real, (long long)INT32_MAX));
+      atomicMax(&fl->max_real, (int)min(real, (long long)INT32_MAX));
     }
-    if (bad) s_bad = 1;
+    if (bad) fl->bad = 1;
     carry = add(carry, total);
     __syncthreads();
   }
-  if (tid != 0) return;
-  const int n = carry.count;
-  const long long T = carry.padded;
-  int status = s_bad ? PSEQ_ERR_VALUE : PSEQ_OK;
-  if (status == PSEQ_OK && T > INT32_MAX) status = PSEQ_ERR_OVERFLOW;
-  const bool absorbed =
-      a.absorb && n >= 1 && (s_mismatch == 0 || (s_mismatch == 1 && s_last_mismatch == n - 1));
-  const long long last = absorbed ? T : carry.real;
-  if (a.cu) a.cu[n] = (int32_t)last;
-  if (a.cu_padded) a.cu_padded[n] = (int32_t)T;
-  ws.seq_cup[n] = (int32_t)T;
-  if (a.pad_between) *a.pad_between = (a.padded && s_mismatch > 0 && !absorbed) ? 1 : 0;
-  long long longest = s_max_real;
-  if (absorbed) longest = max(longest, T - (carry.real - ws.seq_real[n - 1]));
-  if (n == 0) longest = 0;
-  const long long shown_total = a.fixed_total >= 0 ? a.fixed_total : T;
-  Header h = {};
-  h.status = status;
-  h.n = n;
-  h.T = (int32_t)T;
-  h.Tmask = (int32_t)shown_total;
-  *ws.hdr = h;
-  pseq_info out = {status, n, (int32_t)longest, (int32_t)shown_total};
-  if (status != PSEQ_OK) out = {status, 0, 0, 0};
-  *a.info = out;
+  return {carry.count, carry.real, carry.padded};
 }
 
+struct Summary {
+  int status, n;
+  long long T, cu_last, longest, shown_total;
+  int pad_between;
+};
+
+// Absorption gate, pad_between_seqs and max_seqlen from the scan totals.
+// last_real is the real length of kept sequence n-1 (0 when n == 0).
+__device__ __forceinline__ Summary summarize(const MetaArgs& a, const ScanResult& r, const ScanFlags& fl,
+                                             long long last_real) {
+  Summary s;
+  s.n = r.n;
+  s.T = r.padded;
+  s.status = fl.bad ? PSEQ_ERR_VALUE : PSEQ_OK;
+  if (s.status == PSEQ_OK && s.T > INT32_MAX) s.status = PSEQ_ERR_OVERFLOW;
+  const bool absorbed = a.absorb && r.n >= 1 && (fl.mismatch == 0 || (fl.mismatch == 1 && fl.last_mismatch == r.n - 1));
+  s.cu_last = absorbed ? s.T : r.real;
+  s.pad_between = (a.padded && fl.mismatch > 0 && !absorbed) ? 1 : 0;
+  long long longest = fl.max_real;
+  if (absorbed) longest = max(longest, s.T - (r.real - last_real));
+  s.longest = r.n ? longest : 0;
+  s.shown_total = a.fixed_total >= 0 ? a.fixed_total : s.T;
+  return s;
+}
+
+__device__ __forceinline__ void write_meta(const MetaArgs& a, const Summary& s) {
+  if (a.cu) a.cu[s.n] = (int32_t)s.cu_last;
+  if (a.cu_padded) a.cu_padded[s.n] = (int32_t)s.T;
+  if (a.pad_between) *a.pad_between = (uint8_t)s.pad_between;
+  *a.info = s.status == PSEQ_OK ? pseq_info{PSEQ_OK, s.n, (int32_t)s.longest, (int32_t)s.shown_total}
+                                : pseq_info{s.status, 0, 0, 0};
+}
+
+// ----------------------------------------------------------------------------
+// moving stream rows
+// ----------------------------------------------------------------------------
 struct Fields {
   const unsigned char* src[PSEQ_MAX_FIELDS];
   unsigned char* dst[PSEQ_MAX_FIELDS];
   int64_t row_bytes[PSEQ_MAX_FIELDS];
   int planes[PSEQ_MAX_FIELDS];
   int num;
+  int narrow;  // every row of every field is one aligned access of <= 16 bytes
+  int njobs;   // (field, plane) pairs, for the row-by-row path
+  unsigned char job_field[kMaxJobs];
+  unsigned char job_plane[kMaxJobs];
 };
 
-// Largest k in [0, n) with cup[k] <= x, given cup[0] <= x < cup[n].
-// The whole warp searches, 32 probes per round.
-__device__ __forceinline__ int warp_find(const int32_t* cup, int n, int64_t x) {
-  const int lane = threadIdx.x & 31;
-  int lo = 0, hi = n;
-  while (hi - lo > 1) {
-    const int step = (hi - lo + 31) / 32;
-    const int probe = lo + lane * step;
-    const bool ok = probe < hi && (int64_t)__ldcg(cup + probe) <= x;
-    const unsigned m = __ballot_sync(~0u, ok);
-    const int L = 31 - __clz(m);
-    lo = lo + L * step;
-    hi = min(lo + step, hi);
+// Move stream rows [lo, hi) of every field and write their mask bytes.
+// Sequences j = 0..cnt-1 of the table start at stream row cup[j] (cup[cnt]
+// ends the last one) and at source token src_tok[j]; cup[0] <= lo and
+// hi <= cup[cnt].
+__device__ void gather_rows(const Fields& f, int64_t B, int64_t S, int64_t T, uint8_t* mask, int64_t lo,
+                            int64_t hi, const int32_t* cup, const int32_t* src_tok, const int32_t* real, int cnt) {
+  if (lo >= hi) return;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int64_t plane_in = B * S;
+  if (f.narrow) {
+    for (int64_t r = lo + tid; r < hi; r += nt) {
+      const int j = seq_of(cup, cnt, r);
+      const int64_t off = r - cup[j];
+      const int64_t tok = (int64_t)src_tok[j] + off;
+      for (int g = 0; g < f.njobs; g += 8) {
+        int4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (g + q < f.njobs) {
+            const int i = f.job_field[g + q], p = f.job_plane[g + q];
+            const int64_t rb = f.row_bytes[i];
+            v[q] = load_row(f.src[i] + ((int64_t)p * plane_in + tok) * rb, (int)rb);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (g + q < f.njobs) {
+            const int i = f.job_field[g + q], p = f.job_plane[g + q];
+            const int64_t rb = f.row_bytes[i];
+            store_row(f.dst[i] + ((int64_t)p * T + r) * rb, v[q], (int)rb);
+          }
+        }
+      }
+      if (mask) mask[r] = off >= real[j] ? 1 : 0;
+    }
+    return;
   }
-  return lo;
+  for (int j = seq_of(cup, cnt, lo); j < cnt; ++j) {
+    const int64_t cs = cup[j];
+    if (cs >= hi) break;
+    const int64_t a0 = max(lo, cs), a1 = min(hi, (int64_t)cup[j + 1]);
+    if (a0 >= a1) continue;
+    const int64_t tok = (int64_t)src_tok[j] + (a0 - cs);
+    for (int i = 0; i < f.num; ++i) {
+      const int64_t rb = f.row_bytes[i];
+      for (int p = 0; p < f.planes[i]; ++p)
+        block_copy(f.dst[i] + ((int64_t)p * T + a0) * rb, f.src[i] + ((int64_t)p * plane_in + tok) * rb,
+                   (a1 - a0) * rb);
+    }
+    if (mask) {
+      const int64_t real_end = cs + real[j];
+      for (int64_t t = a0 + tid; t < a1; t += nt) mask[t] = t >= real_end ? 1 : 0;
+    }
+  }
 }
 
-__global__ void __launch_bounds__(kGatherThreads)
-    thd_gather_kernel(Fields f, int64_t B, int64_t S, uint8_t* __restrict__ mask, Workspace ws,
-                      int64_t max_seqs, int64_t max_rows) {
+// Rows [r0, r1) of a mask of length Tm that CTA blockIdx.x owns.
+__device__ __forceinline__ void slice_of(int64_t Tm, int64_t& r0, int64_t& r1) {
+  const int64_t G = gridDim.x;
+  const int64_t per = (Tm + G - 1) / G;
+  r0 = min((int64_t)blockIdx.x * per, Tm);
+  r1 = min(r0 + per, Tm);
+}
+
+// ----------------------------------------------------------------------------
+// kernels
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(kRowThreads, 2)
+    thd_fused_kernel(const __grid_constant__ MetaArgs a, const __grid_constant__ Fields f, uint8_t* mask,
+                     int64_t mask_cap) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ Triple scratch[kRowThreads / 32];
+  __shared__ ScanFlags fl;
+  pdl_enter();
+  const int E = a.B * a.P;
+  int64_t* s_row = reinterpret_cast<int64_t*>(smem);
+  int32_t* s_cup = reinterpret_cast<int32_t*>(s_row + (a.P > 0 ? a.B : 0));
+  int32_t* s_src = s_cup + E + 1;
+  int32_t* s_real = s_src + E;
+  const bool lead = blockIdx.x == 0;
+  auto put = [&](int k, int b, long long o, long long real, long long padded, long long R, long long Pd) {
+    s_cup[k] = (int32_t)Pd;
+    s_src[k] = (int32_t)(b * a.S + o);
+    s_real[k] = (int32_t)real;
+    if (lead) {
+      if (a.cu) a.cu[k] = (int32_t)R;
+      if (a.cu_padded) a.cu_padded[k] = (int32_t)Pd;
+    }
+  };
+  const ScanResult r = scan_lengths<kRowThreads>(a, s_row, scratch, &fl, put);
+  const Summary s = summarize(a, r, fl, r.n ? s_real[r.n - 1] : 0);
+  if (threadIdx.x == 0) {
+    s_cup[r.n] = (int32_t)s.T;
+    if (lead) write_meta(a, s);
+  }
+  __syncthreads();
+  if (s.status != PSEQ_OK) return;
+  const int64_t T = s.T, Tm = s.shown_total;
+  if (Tm > mask_cap || T > Tm || T > (int64_t)a.B * a.S) return;  // cannot happen for well-formed input
+  int64_t r0, r1;
+  slice_of(Tm, r0, r1);
+  gather_rows(f, a.B, a.S, T, mask, r0, min(r1, T), s_cup, s_src, s_real, r.n);
+  if (mask) {
+    const int64_t tail = max(r0, T);
+    if (tail < r1) block_fill_bytes(mask + tail, r1 - tail, 1);
+  }
+}
+
+__global__ void __launch_bounds__(kMetaThreads) thd_meta_kernel(const __grid_constant__ MetaArgs a, Workspace ws) {
+  __shared__ Triple scratch[kMetaThreads / 32];
+  __shared__ ScanFlags fl;
+  pdl_enter();
+  auto put = [&](int k, int b, long long o, long long real, long long padded, long long R, long long Pd) {
+    ws.seq_src[k] = (long long)b * a.S + o;
+    ws.seq_real[k] = (int32_t)real;
+    ws.seq_cup[k] = (int32_t)Pd;
+    if (a.cu) a.cu[k] = (int32_t)R;
+    if (a.cu_padded) a.cu_padded[k] = (int32_t)Pd;
+  };
+  const ScanResult r = scan_lengths<kMetaThreads>(a, ws.row_pfx, scratch, &fl, put);
+  if (threadIdx.x != 0) return;
+  const Summary s = summarize(a, r, fl, r.n ? ws.seq_real[r.n - 1] : 0);
+  ws.seq_cup[r.n] = (int32_t)s.T;
+  write_meta(a, s);
+  Header h = {};
+  h.status = s.status;
+  h.n = s.n;
+  h.T = (int32_t)s.T;
+  h.Tmask = (int32_t)s.shown_total;
+  *ws.hdr = h;
+}
+
+__global__ void __launch_bounds__(kRowThreads, 2)
+    thd_gather_kernel(const __grid_constant__ Fields f, int64_t B, int64_t S, uint8_t* __restrict__ mask,
+                      Workspace ws, int64_t max_seqs, int64_t max_rows) {
+  __shared__ int32_t s_cup[kTableBatch + 1];
+  __shared__ int32_t s_src[kTableBatch];
+  __shared__ int32_t s_real[kTableBatch];
   __shared__ int s_first;
-  pdl_wait();
+  pdl_enter();
   const int status = __ldcg(&ws.hdr->status);
   if (status != PSEQ_OK) return;
   const int n = __ldcg(&ws.hdr->n);
@@ -245,37 +357,39 @@ __global__ void __launch_bounds__(kGatherThreads)
   const int64_t Tm = __ldcg(&ws.hdr->Tmask);
   // a layout that does not fit the buffers did not come from thd_meta: write nothing
   if (n < 0 || n > max_seqs || T < 0 || T > B * S || Tm < T || Tm > max_rows) return;
-  const int64_t G = gridDim.x;
-  const int64_t per = (Tm + G - 1) / G;
-  const int64_t r0 = (int64_t)blockIdx.x * per;
-  const int64_t r1 = min(r0 + per, Tm);
+  int64_t r0, r1;
+  slice_of(Tm, r0, r1);
   if (r0 >= r1) return;
   const int64_t g1 = min(r1, T);
-  const int tid = threadIdx.x;
-  if (r0 < g1) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  int64_t lo = r0;
+  while (lo < g1) {
     if (tid < 32) {
-      const int k = warp_find(ws.seq_cup, n, r0);
-      if (tid == 0) s_first = k;
+      // largest k with cup[k] <= lo, 32 probes per round
+      int a = 0, b = n;
+      while (b - a > 1) {
+        const int step = (b - a + 31) / 32;
+        const int probe = a + lane * step;
+        const bool ok = probe < b && (int64_t)__ldcg(ws.seq_cup + probe) <= lo;
+        const unsigned m = __ballot_sync(~0u, ok);
+        a = a + (31 - __clz(m)) * step;
+        b = min(a + step, b);
+      }
+      if (tid == 0) s_first = a;
     }
     __syncthreads();
-    for (int k = s_first; k < n; ++k) {
-      const int64_t cs = __ldcg(ws.seq_cup + k);
-      if (cs >= g1) break;
-      const int64_t ce = __ldcg(ws.seq_cup + k + 1);
-      const int64_t lo = max(r0, cs), hi = min(g1, ce);
-      if (lo >= hi) continue;
-      const int64_t src_tok = __ldcg(ws.seq_src + k) + (lo - cs);
-      for (int i = 0; i < f.num; ++i) {
-        const int64_t rb = f.row_bytes[i];
-        for (int p = 0; p < f.planes[i]; ++p)
-          block_copy(f.dst[i] + ((int64_t)p * T + lo) * rb, f.src[i] + ((int64_t)p * B * S + src_tok) * rb,
-                     (hi - lo) * rb);
-      }
-      if (mask) {
-        const int64_t real_end = cs + __ldcg(ws.seq_real + k);
-        for (int64_t t = lo + tid; t < hi; t += kGatherThreads) mask[t] = t >= real_end ? 1 : 0;
-      }
+    const int k0 = s_first;
+    const int cnt = min(kTableBatch, n - k0);
+    for (int i = tid; i <= cnt; i += kRowThreads) s_cup[i] = __ldcg(ws.seq_cup + k0 + i);
+    for (int i = tid; i < cnt; i += kRowThreads) {
+      s_src[i] = (int32_t)__ldcg(ws.seq_src + k0 + i);
+      s_real[i] = __ldcg(ws.seq_real + k0 + i);
     }
+    __syncthreads();
+    const int64_t hi = min(g1, (int64_t)s_cup[cnt]);
+    gather_rows(f, B, S, T, mask, lo, hi, s_cup, s_src, s_real, cnt);
+    lo = hi;
+    __syncthreads();
   }
   if (mask) {
     const int64_t tail = max(r0, T);
@@ -283,12 +397,31 @@ __global__ void __launch_bounds__(kGatherThreads)
   }
 }
 
-int gather_grid(int64_t rows, int64_t bytes_per_row) {
-  // enough CTAs to keep every SM busy on large streams, fewer on tiny ones
-  const int64_t full = (int64_t)sm_count() * (2048 / kGatherThreads);
-  const int64_t by_bytes = (rows * (bytes_per_row + 1) + 8191) / 8192;
-  int64_t g = by_bytes < full ? by_bytes : full;
-  return (int)(g < 1 ? 1 : g);
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+int occupancy(const void* kernel, int threads, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, size_t>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto key = std::make_tuple(dev, kernel, smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
+  cache[key] = n;
+  return n;
+}
+
+// One wave of CTAs: about one row per thread on the row-by-row path, every
+// resident slot for wide rows.
+int row_grid(const void* kernel, size_t smem, int64_t rows, const Fields& f) {
+  const int64_t full = (int64_t)sm_count() * occupancy(kernel, kRowThreads, smem);
+  int64_t want = f.narrow ? (rows + kRowThreads - 1) / kRowThreads : full;
+  if (want > full) want = full;
+  return (int)(want < 1 ? 1 : want);
 }
 
 pseq_status check_lengths(const char* fn, int64_t B, int64_t S, int64_t P) {
@@ -300,7 +433,7 @@ pseq_status check_lengths(const char* fn, int64_t B, int64_t S, int64_t P) {
   return PSEQ_OK;
 }
 
-pseq_status launch_meta(const char* fn, MetaArgs a, void* workspace, size_t ws_bytes, cudaStream_t st) {
+pseq_status check_meta(const char* fn, const MetaArgs& a, const void* workspace, size_t ws_bytes) {
   const int64_t E = (int64_t)a.B * a.P;
   const size_t need = workspace_bytes(a.B, E);
   if (!workspace || ws_bytes < need || !aligned(workspace, 16))
@@ -309,47 +442,104 @@ pseq_status launch_meta(const char* fn, MetaArgs a, void* workspace, size_t ws_b
   if (!aligned(a.real, 8) || !aligned(a.padded, 8) || !aligned(a.cu, 4) || !aligned(a.cu_padded, 4) ||
       !aligned(a.info, 4))
     return fail(PSEQ_ERR_ARG, "%s: misaligned pointer", fn);
-  thd_meta_kernel<<<1, kMetaThreads, 0, st>>>(a, carve(workspace, a.B, E));
-  count_launches(1);
-  return check_launch(fn);
+  return PSEQ_OK;
 }
 
-pseq_status launch_gather(const char* fn, const pseq_field* fields, int num_fields, int64_t B, int64_t S,
-                          int64_t P, uint8_t* mask, const void* workspace, size_t ws_bytes, cudaStream_t st,
-                          int64_t mask_rows) {
+pseq_status build_fields(const char* fn, const pseq_field* fields, int num_fields, int64_t B, int64_t S,
+                         Fields& f) {
   if (num_fields < 0 || num_fields > PSEQ_MAX_FIELDS)
     return fail(PSEQ_ERR_ARG, "%s: num_fields must be in [0, %d]", fn, PSEQ_MAX_FIELDS);
   if (num_fields > 0 && !fields) return fail(PSEQ_ERR_ARG, "%s: fields is NULL", fn);
-  const int64_t E = B * P;
-  const size_t need = workspace_bytes(B, E);
-  if (!workspace || ws_bytes < need || !aligned(workspace, 16))
-    return fail(PSEQ_ERR_ARG, "%s: workspace needs %zu bytes, 16-byte aligned (got %zu)", fn, need, ws_bytes);
-  Fields f = {};
+  f = Fields{};
   f.num = num_fields;
-  int64_t bytes_per_row = 0;
+  f.narrow = 1;
+  int jobs = 0;
   for (int i = 0; i < num_fields; ++i) {
     const pseq_field& x = fields[i];
     if (x.elem_bytes != 1 && x.elem_bytes != 2 && x.elem_bytes != 4 && x.elem_bytes != 8)
       return fail(PSEQ_ERR_ARG, "%s: field %d: elem_bytes must be 1, 2, 4 or 8", fn, i);
-    if (x.planes < 1 || x.row_elems < 1) return fail(PSEQ_ERR_ARG, "%s: field %d: planes and row_elems must be >= 1", fn, i);
+    if (x.planes < 1 || x.row_elems < 1)
+      return fail(PSEQ_ERR_ARG, "%s: field %d: planes and row_elems must be >= 1", fn, i);
     if (B * S > 0 && (!x.src || !x.dst)) return fail(PSEQ_ERR_ARG, "%s: field %d: NULL src or dst", fn, i);
+    if (!aligned(x.src, (uintptr_t)x.elem_bytes) || !aligned(x.dst, (uintptr_t)x.elem_bytes))
+      return fail(PSEQ_ERR_ARG, "%s: field %d: misaligned pointer", fn, i);
+    const int64_t cells = B * S > 0 ? B * S * (int64_t)x.planes : 1;
+    if (x.row_elems > (INT64_MAX / 16) / cells) return fail(PSEQ_ERR_OVERFLOW, "%s: field %d is too large", fn, i);
     const int64_t rb = x.row_elems * x.elem_bytes;
-    if (x.row_elems > (INT64_MAX / 8) / (B * S > 0 ? B * S * x.planes : 1))
-      return fail(PSEQ_ERR_OVERFLOW, "%s: field %d is too large", fn, i);
     f.src[i] = static_cast<const unsigned char*>(x.src);
     f.dst[i] = static_cast<unsigned char*>(x.dst);
     f.row_bytes[i] = rb;
     f.planes[i] = x.planes;
-    bytes_per_row += rb * x.planes;
+    const bool one_access = (rb == 1 || rb == 2 || rb == 4 || rb == 8 || rb == 16) && aligned(x.src, (uintptr_t)rb) &&
+                            aligned(x.dst, (uintptr_t)rb);
+    if (!one_access) f.narrow = 0;
+    for (int p = 0; p < x.planes; ++p) {
+      if (jobs < kMaxJobs) {
+        f.job_field[jobs] = (unsigned char)i;
+        f.job_plane[jobs] = (unsigned char)p;
+      }
+      ++jobs;
+    }
   }
-  if (num_fields == 0 && !mask) return PSEQ_OK;
-  const int grid = gather_grid(mask_rows, bytes_per_row);
-  Workspace ws = carve(workspace, B, E);
-  cudaError_t e = launch_pdl(thd_gather_kernel, dim3(grid), dim3(kGatherThreads), 0, st, f, B, S, mask, ws, E,
-                             mask_rows);
+  if (jobs > kMaxJobs) f.narrow = 0;
+  f.njobs = f.narrow ? jobs : 0;
+  return PSEQ_OK;
+}
+
+size_t fused_smem(const MetaArgs& a) {
+  const size_t E = (size_t)a.B * a.P;
+  return round_up((a.P > 0 ? 8 * (size_t)a.B : 0) + 4 * (E + 1) + 8 * E, 16);
+}
+
+pseq_status launch_fused(const char* fn, const MetaArgs& a, const Fields& f, uint8_t* mask, int64_t mask_cap,
+                         cudaStream_t st) {
+  const size_t smem = fused_smem(a);
+  const int64_t rows = a.fixed_total >= 0 ? a.fixed_total : (int64_t)a.B * a.S;
+  const int grid = row_grid(reinterpret_cast<const void*>(thd_fused_kernel), smem, rows, f);
+  const cudaError_t e = launch_pdl(thd_fused_kernel, dim3(grid), dim3(kRowThreads), smem, st, a, f, mask, mask_cap);
   count_launches(1);
   if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
   return check_launch(fn);
+}
+
+pseq_status launch_meta(const char* fn, const MetaArgs& a, void* workspace, cudaStream_t st) {
+  const cudaError_t e =
+      launch_pdl(thd_meta_kernel, dim3(1), dim3(kMetaThreads), 0, st, a, carve(workspace, a.B, (int64_t)a.B * a.P));
+  count_launches(1);
+  if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  return check_launch(fn);
+}
+
+pseq_status launch_gather(const char* fn, const Fields& f, int64_t B, int64_t S, int64_t P, uint8_t* mask,
+                          const void* workspace, cudaStream_t st, int64_t mask_rows) {
+  if (f.num == 0 && !mask) return PSEQ_OK;
+  const int64_t E = B * P;
+  const int grid = row_grid(reinterpret_cast<const void*>(thd_gather_kernel), 0, mask_rows, f);
+  Workspace ws = carve(workspace, B, E);
+  cudaError_t e = launch_pdl(thd_gather_kernel, dim3(grid), dim3(kRowThreads), 0, st, f, B, S, mask, ws, E, mask_rows);
+  count_launches(1);
+  if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  return check_launch(fn);
+}
+
+MetaArgs thd_args(const int64_t* seq_lens, const int64_t* seq_lens_padded, int64_t B, int64_t S, int64_t P,
+                  int64_t pad_value, int32_t absorb, int32_t* cu, int32_t* cup, uint8_t* pad_between,
+                  pseq_info* info) {
+  MetaArgs a = {};
+  a.real = seq_lens;
+  a.padded = seq_lens_padded;
+  a.B = (int)B;
+  a.P = (int)P;
+  a.S = S;
+  a.pad_value = pad_value;
+  a.has_filler = 1;
+  a.absorb = absorb ? 1 : 0;
+  a.cu = cu;
+  a.cu_padded = seq_lens_padded ? cup : nullptr;
+  a.pad_between = pad_between;
+  a.info = info;
+  a.fixed_total = -1;
+  return a;
 }
 
 }  // namespace
@@ -369,34 +559,32 @@ extern "C" pseq_status thd_meta(const int64_t* seq_lens, const int64_t* seq_lens
                                 pseq_info* info, void* workspace, size_t workspace_bytes_,
                                 pseq_stream stream) {
   clear_error();
-  pseq_status s = check_lengths("thd_meta", B, S, num_packs);
+  const char* fn = "thd_meta";
+  pseq_status s = check_lengths(fn, B, S, num_packs);
   if (s != PSEQ_OK) return s;
-  if (!cu_seqlens) return fail(PSEQ_ERR_ARG, "thd_meta: cu_seqlens is required");
-  MetaArgs a = {};
-  a.real = seq_lens;
-  a.padded = seq_lens_padded;
-  a.B = (int)B;
-  a.P = (int)num_packs;
-  a.S = S;
-  a.pad_value = pad_value;
-  a.has_filler = 1;
-  a.absorb = absorb_trailing_pad ? 1 : 0;
-  a.cu = cu_seqlens;
-  a.cu_padded = seq_lens_padded ? cu_seqlens_padded : nullptr;
-  a.pad_between = pad_between_seqs;
-  a.info = info;
-  a.fixed_total = -1;
-  return launch_meta("thd_meta", a, workspace, workspace_bytes_, reinterpret_cast<cudaStream_t>(stream));
+  if (!cu_seqlens) return fail(PSEQ_ERR_ARG, "%s: cu_seqlens is required", fn);
+  const MetaArgs a = thd_args(seq_lens, seq_lens_padded, B, S, num_packs, pad_value, absorb_trailing_pad, cu_seqlens,
+                              cu_seqlens_padded, pad_between_seqs, info);
+  s = check_meta(fn, a, workspace, workspace_bytes_);
+  if (s != PSEQ_OK) return s;
+  return launch_meta(fn, a, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" pseq_status thd_gather(const pseq_field* fields, int32_t num_fields, int64_t B, int64_t S,
                                   int64_t num_packs, uint8_t* padding_mask, const void* workspace,
                                   size_t workspace_bytes_, pseq_stream stream) {
   clear_error();
-  pseq_status s = check_lengths("thd_gather", B, S, num_packs);
+  const char* fn = "thd_gather";
+  pseq_status s = check_lengths(fn, B, S, num_packs);
   if (s != PSEQ_OK) return s;
-  return launch_gather("thd_gather", fields, num_fields, B, S, num_packs, padding_mask, workspace,
-                       workspace_bytes_, reinterpret_cast<cudaStream_t>(stream), B * S);
+  const size_t need = workspace_bytes(B, B * num_packs);
+  if (!workspace || workspace_bytes_ < need || !aligned(workspace, 16))
+    return fail(PSEQ_ERR_ARG, "%s: workspace needs %zu bytes, 16-byte aligned (got %zu)", fn, need, workspace_bytes_);
+  Fields f;
+  s = build_fields(fn, fields, num_fields, B, S, f);
+  if (s != PSEQ_OK) return s;
+  return launch_gather(fn, f, B, S, num_packs, padding_mask, workspace, reinterpret_cast<cudaStream_t>(stream),
+                       B * S);
 }
 
 extern "C" pseq_status thd_from_batch(const int64_t* seq_lens, const int64_t* seq_lens_padded, int64_t B,
@@ -406,14 +594,22 @@ extern "C" pseq_status thd_from_batch(const int64_t* seq_lens, const int64_t* se
                                       uint8_t* pad_between_seqs, pseq_info* info, void* workspace,
                                       size_t workspace_bytes_, pseq_stream stream) {
   clear_error();
-  pseq_status s = check_lengths("thd_from_batch", B, S, num_packs);
+  const char* fn = "thd_from_batch";
+  pseq_status s = check_lengths(fn, B, S, num_packs);
   if (s != PSEQ_OK) return s;
-  if (num_fields < 0 || num_fields > PSEQ_MAX_FIELDS || (num_fields > 0 && !fields))
-    return fail(PSEQ_ERR_ARG, "thd_from_batch: bad fields / num_fields");
-  s = thd_meta(seq_lens, seq_lens_padded, B, S, num_packs, pad_value, absorb_trailing_pad, cu_seqlens,
-               cu_seqlens_padded, pad_between_seqs, info, workspace, workspace_bytes_, stream);
+  if (!cu_seqlens) return fail(PSEQ_ERR_ARG, "%s: cu_seqlens is required", fn);
+  Fields f;
+  s = build_fields(fn, fields, num_fields, B, S, f);
   if (s != PSEQ_OK) return s;
-  return thd_gather(fields, num_fields, B, S, num_packs, padding_mask, workspace, workspace_bytes_, stream);
+  const MetaArgs a = thd_args(seq_lens, seq_lens_padded, B, S, num_packs, pad_value, absorb_trailing_pad, cu_seqlens,
+                              cu_seqlens_padded, pad_between_seqs, info);
+  s = check_meta(fn, a, workspace, workspace_bytes_);
+  if (s != PSEQ_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (B * num_packs <= kFusedMaxEntries) return launch_fused(fn, a, f, padding_mask, B * S, st);
+  s = launch_meta(fn, a, workspace, st);
+  if (s != PSEQ_OK) return s;
+  return launch_gather(fn, f, B, S, num_packs, padding_mask, workspace, st, B * S);
 }
 
 extern "C" pseq_status thd_padding_mask(int64_t total_tokens, const int64_t* valid_seq_lens,
@@ -421,25 +617,22 @@ extern "C" pseq_status thd_padding_mask(int64_t total_tokens, const int64_t* val
                                         pseq_info* info, void* workspace, size_t workspace_bytes_,
                                         pseq_stream stream) {
   clear_error();
-  if (total_tokens < 0 || n < 0) return fail(PSEQ_ERR_ARG, "thd_padding_mask: negative size");
-  if (total_tokens > INT32_MAX) return fail(PSEQ_ERR_OVERFLOW, "thd_padding_mask: total_tokens exceeds INT32_MAX");
-  if (n > INT32_MAX - 1) return fail(PSEQ_ERR_OVERFLOW, "thd_padding_mask: n exceeds INT32_MAX");
-  if (total_tokens > 0 && !mask) return fail(PSEQ_ERR_ARG, "thd_padding_mask: mask is NULL");
-  MetaArgs a = {};
-  a.real = valid_seq_lens;
-  a.padded = valid_seq_lens_padded;
-  a.B = 1;
-  a.P = (int)n;
-  a.S = total_tokens;
-  a.pad_value = 0;
+  const char* fn = "thd_padding_mask";
+  if (total_tokens < 0 || n < 0) return fail(PSEQ_ERR_ARG, "%s: negative size", fn);
+  if (total_tokens > INT32_MAX) return fail(PSEQ_ERR_OVERFLOW, "%s: total_tokens exceeds INT32_MAX", fn);
+  if (n > INT32_MAX - 1) return fail(PSEQ_ERR_OVERFLOW, "%s: n exceeds INT32_MAX", fn);
+  if (total_tokens > 0 && !mask) return fail(PSEQ_ERR_ARG, "%s: mask is NULL", fn);
+  MetaArgs a = thd_args(valid_seq_lens, valid_seq_lens_padded, 1, total_tokens, n, 0, 0, nullptr, nullptr, nullptr,
+                        info);
   a.has_filler = 0;
-  a.absorb = 0;
-  a.info = info;
   a.fixed_total = total_tokens;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  pseq_status s = launch_meta("thd_padding_mask", a, workspace, workspace_bytes_, st);
+  pseq_status s = check_meta(fn, a, workspace, workspace_bytes_);
   if (s != PSEQ_OK) return s;
-  if (total_tokens == 0) return PSEQ_OK;
-  return launch_gather("thd_padding_mask", nullptr, 0, 1, total_tokens, n, mask, workspace, workspace_bytes_, st,
-                       total_tokens);
+  Fields f;
+  build_fields(fn, nullptr, 0, 1, total_tokens, f);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (n <= kFusedMaxEntries) return launch_fused(fn, a, f, mask, total_tokens, st);
+  s = launch_meta(fn, a, workspace, st);
+  if (s != PSEQ_OK || total_tokens == 0) return s;
+  return launch_gather(fn, f, 1, total_tokens, n, mask, workspace, st, total_tokens);
 }
