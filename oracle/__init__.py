@@ -80,6 +80,12 @@ def _declare(lib):
     lib.oracle_thd_gather.argtypes = [P, P, I32, I64, I64, I64, I64, I64, P, P, P, P, I64]
     lib.oracle_thd_padding_mask.restype = I32
     lib.oracle_thd_padding_mask.argtypes = [I64, P, P, I64, P]
+    lib.oracle_mask_from_token_ids.restype = I32
+    lib.oracle_mask_from_token_ids.argtypes = [P, I32, I64, I64, P]
+    lib.oracle_ffd.restype = I32
+    lib.oracle_ffd.argtypes = [P, I64, I64, P, P, P]
+    lib.oracle_doc_ids_to_lengths.restype = I32
+    lib.oracle_doc_ids_to_lengths.argtypes = [P, I32, I64, I64, I64, I64, P, P, P]
     lib.oracle_pack_squeeze.restype = I32
     lib.oracle_pack_squeeze.argtypes = [P, I64, I64, I32, P, P, P, I64, I64, I64, I32, I64, I64,
                                         P, P, P, P, P]
@@ -344,3 +350,117 @@ def pack_squeeze(src: np.ndarray, real_lens: np.ndarray, bin_offsets: np.ndarray
         "cu_flat": cu[: M + num_bins].copy(),
         "cu_padded_flat": cup[: M + num_bins].copy(),
     }
+
+
+# --------------------------------------------------------------------------
+# O6 thd_padding_mask_from_token_ids
+# --------------------------------------------------------------------------
+def mask_from_token_ids(input_ids: np.ndarray, padding_token_id: int, lib=None) -> np.ndarray:
+    """Value-compare padding mask, rejecting a pad id that is also content.
+
+    Follows thd_utils: ``thd_padding_mask_from_token_ids``.  Raises
+    ``OracleValueError`` when a pad token is followed by a non-pad token.
+    """
+    lib = lib or load_library()
+    ids = np.ascontiguousarray(input_ids).reshape(-1)
+    if ids.dtype not in (np.int32, np.int64):
+        raise ValueError("input_ids must be int32 or int64")
+    mask = np.zeros(max(ids.size, 1), np.uint8)
+    _check(lib.oracle_mask_from_token_ids(_ptr(ids if ids.size else np.zeros(1, ids.dtype)), ids.dtype.itemsize,
+                                          ids.size, padding_token_id, _ptr(mask)))
+    return mask[:ids.size].astype(bool)
+
+
+# --------------------------------------------------------------------------
+# O7 first-fit-decreasing bins
+# --------------------------------------------------------------------------
+def ffd(sizes: np.ndarray, capacity: int, lib=None):
+    """First-fit-decreasing bins of ``sizes`` at ``capacity``.
+
+    Follows "Who packs the sequences" (get_packer, First Fit Decreasing).
+    Returns ``(bin_offsets int32 [nb+1], bin_members int32 [n])``.
+    """
+    lib = lib or load_library()
+    sz = np.ascontiguousarray(sizes, np.int64).reshape(-1)
+    n = sz.size
+    offs = np.zeros(n + 2, np.int32)
+    mem = np.zeros(max(n, 1), np.int32)
+    nb = np.zeros(1, np.int64)
+    _check(lib.oracle_ffd(_ptr(sz if n else np.zeros(1, np.int64)), n, capacity, _ptr(offs), _ptr(mem), _ptr(nb)))
+    k = int(nb[0])
+    return offs[: k + 1].copy(), mem[:n].copy()
+
+
+# --------------------------------------------------------------------------
+# O8 doc_ids -> pack lengths and positions
+# --------------------------------------------------------------------------
+def doc_ids_to_lengths(doc_ids: np.ndarray, num_packs: int, pad_value: int = -1000, lib=None) -> dict:
+    """seq_lens, seq_lens_padded [B, num_packs] and position_ids [B, S] of a
+    neat-packing map (see the C function for the readings).  Raises
+    ``OracleCapacityError`` when a row holds more than num_packs sequences."""
+    lib = lib or load_library()
+    d = np.ascontiguousarray(doc_ids)
+    if d.ndim != 2 or d.dtype not in (np.int32, np.int64):
+        raise ValueError("doc_ids must be int32 or int64 [B, S]")
+    B, S = d.shape
+    real = np.zeros(max(B * num_packs, 1), np.int64)
+    padded = np.zeros(max(B * num_packs, 1), np.int64)
+    pos = np.zeros(max(B * S, 1), np.int64)
+    _check(lib.oracle_doc_ids_to_lengths(_ptr(d if d.size else np.zeros(1, d.dtype)), d.dtype.itemsize, B, S,
+                                         num_packs, pad_value, _ptr(real), _ptr(padded), _ptr(pos)))
+    return {"seq_lens": real[: B * num_packs].reshape(B, num_packs),
+            "seq_lens_padded": padded[: B * num_packs].reshape(B, num_packs),
+            "position_ids": pos[: B * S].reshape(B, S)}
+
+
+# --------------------------------------------------------------------------
+# O9 split_batch_into_thd_chunks
+# --------------------------------------------------------------------------
+def split_batch_into_thd_chunks(batch: dict, num_chunks: int, seq_lens_padding_value: int = -1000,
+                                absorb: bool = True, lib=None) -> dict:
+    """thd_utils ``split_batch_into_thd_chunks``: split the batch along its
+    first axis into ``num_chunks`` equal chunks, run process_input_for_thd on
+    each, stack every tensor result on a new leading axis, and pad the
+    cu_seqlens arrays to one length with ``seq_lens_padding_value``.
+
+    Readings: chunks whose streams have different lengths cannot be stacked
+    (``OracleValueError``); per-chunk scalars (max_seqlen, pad_between_seqs,
+    total_tokens) become arrays of length num_chunks; num_chunks <= 1 returns
+    process_input_for_thd unchanged.
+    """
+    lib = lib or load_library()
+    if num_chunks <= 1:
+        return process_input_for_thd(batch, seq_lens_padding_value, absorb, lib=lib)
+    B = batch["input_ids"].shape[0]
+    if B % num_chunks:
+        raise ValueError("num_chunks must evenly divide the batch size")
+    Bc = B // num_chunks
+    parts = []
+    for c in range(num_chunks):
+        sub = {}
+        for k, v in batch.items():
+            if not isinstance(v, np.ndarray):
+                sub[k] = v
+            elif k == "position_ids" and v.ndim == 3:
+                sub[k] = v[:, c * Bc:(c + 1) * Bc]
+            else:
+                sub[k] = v[c * Bc:(c + 1) * Bc]
+        parts.append(process_input_for_thd(sub, seq_lens_padding_value, absorb, lib=lib))
+    if len({p["total_tokens"] for p in parts}) != 1:
+        raise OracleValueError("chunks produce streams of different lengths and cannot be stacked")
+    out = {k: v for k, v in parts[0].items() if not isinstance(v, (np.ndarray, bool, int, np.bool_))}
+    for k in ("input_ids", "labels", "position_ids", "padding_mask"):
+        if k in parts[0]:
+            out[k] = np.stack([p[k] for p in parts])
+    for k in ("cu_seqlens", "cu_seqlens_padded"):
+        if k in parts[0]:
+            width = max(p[k].size for p in parts)
+            rows = np.full((num_chunks, width), seq_lens_padding_value, np.int32)
+            for c, p in enumerate(parts):
+                rows[c, : p[k].size] = p[k]
+            out[k] = rows
+    out["max_seqlen"] = np.array([p["max_seqlen"] for p in parts], np.int32)
+    out["pad_between_seqs"] = np.array([p["pad_between_seqs"] for p in parts], bool)
+    out["total_tokens"] = parts[0]["total_tokens"]
+    out["num_sequences"] = np.array([p["cu_seqlens"].size - 1 for p in parts], np.int32)
+    return out

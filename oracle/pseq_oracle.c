@@ -20,6 +20,7 @@
  *                 (NeMo-RL #4105 explainer page)
  */
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define ORC_OK 0
@@ -288,5 +289,138 @@ int oracle_pack_squeeze(const void* src, int64_t N, int64_t W, int elem_bytes,
     if (stretch) bcup[count] = (int32_t)capacity;
   }
   *max_total = widest;
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * O6  thd_padding_mask_from_token_ids
+ * [thd_utils] "thd_padding_mask_from_token_ids": padding is marked by
+ *   comparing token ids with padding_token_id, which is only correct when the
+ *   pad id fills a right-padded tail and appears nowhere else; anything else
+ *   is rejected (the page raises ValueError).
+ * Returns ORC_VALUE when a pad token is followed by a non-pad token.
+ * ---------------------------------------------------------------------- */
+int oracle_mask_from_token_ids(const void* ids, int elem_bytes, int64_t n,
+                               int64_t pad_id, uint8_t* mask) {
+  for (int64_t t = 0; t < n; ++t)
+    mask[t] = (read_int(ids, elem_bytes, t) == pad_id) ? 1 : 0;
+  int seen_pad = 0;
+  for (int64_t t = 0; t < n; ++t) {
+    if (mask[t]) seen_pad = 1;
+    else if (seen_pad) return ORC_VALUE; /* content after a pad token */
+  }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * O7  first-fit-decreasing bin assignment
+ * [who_packs] "get_packer picks which rows share a bin, by token budget"; the
+ *   page names First Fit Decreasing among the packers.  The textbook
+ *   algorithm: visit the items largest first (ties: smaller index first) and
+ *   put each into the first open bin with room; open a new bin when none has
+ *   room.  bin_members lists each bin's items in placement order, bin b
+ *   starting at bin_offsets[b].  A negative size is ORC_VALUE, one larger
+ *   than capacity ORC_CAPACITY.  *num_bins receives the bin count.
+ * ---------------------------------------------------------------------- */
+int oracle_ffd(const int64_t* sizes, int64_t n, int64_t capacity,
+               int32_t* bin_offsets, int32_t* bin_members, int64_t* num_bins) {
+  for (int64_t i = 0; i < n; ++i) {
+    if (sizes[i] < 0) return ORC_VALUE;
+    if (sizes[i] > capacity) return ORC_CAPACITY;
+  }
+  int64_t* order = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  int64_t* room = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  int64_t* bin_of = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n + 1));
+  /* order: selection sort on (size descending, index ascending) */
+  for (int64_t i = 0; i < n; ++i) order[i] = i;
+  for (int64_t i = 0; i < n; ++i) {
+    int64_t best = i;
+    for (int64_t j = i + 1; j < n; ++j) {
+      int64_t a = order[j], b = order[best];
+      if (sizes[a] > sizes[b] || (sizes[a] == sizes[b] && a < b)) best = j;
+    }
+    int64_t tmp = order[i];
+    order[i] = order[best];
+    order[best] = tmp;
+  }
+  /* first fit */
+  int64_t bins = 0;
+  for (int64_t k = 0; k < n; ++k) {
+    int64_t item = order[k];
+    int64_t b = 0;
+    while (b < bins && room[b] < sizes[item]) ++b;
+    if (b == bins) {
+      room[bins] = capacity;
+      bins += 1;
+    }
+    room[b] -= sizes[item];
+    bin_of[k] = b;
+  }
+  /* members of each bin, in placement order */
+  int64_t pos = 0;
+  for (int64_t b = 0; b < bins; ++b) {
+    bin_offsets[b] = (int32_t)pos;
+    for (int64_t k = 0; k < n; ++k)
+      if (bin_of[k] == b) bin_members[pos++] = (int32_t)order[k];
+  }
+  bin_offsets[bins] = (int32_t)pos;
+  *num_bins = bins;
+  free(order);
+  free(room);
+  free(bin_of);
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * O8  doc_ids -> seq_lens / seq_lens_padded / position_ids
+ * Joins the neat-packing map of [packed_seq] (1-based document index per
+ *   token, 0 = padding) to the pack-length format of [thd_utils]
+ *   process_input_for_thd (seq_lens and seq_lens_padded [B, num_packs], -1000
+ *   for unused slots).  Readings: within a row, every maximal run of one
+ *   non-zero index is a sequence whose real length is the run length; a
+ *   padding run that follows a document run belongs to that sequence's
+ *   padded length; a padding run at the start of a row is a sequence of real
+ *   length 0.  position_ids counts 0, 1, ... within each document run and is
+ *   0 on padding.  More sequences in a row than num_packs is ORC_CAPACITY.
+ * ---------------------------------------------------------------------- */
+int oracle_doc_ids_to_lengths(const void* doc_ids, int elem_bytes, int64_t B,
+                              int64_t S, int64_t num_packs, int64_t pad_value,
+                              int64_t* seq_lens, int64_t* seq_lens_padded,
+                              int64_t* position_ids) {
+  for (int64_t i = 0; i < B * num_packs; ++i) {
+    seq_lens[i] = pad_value;
+    seq_lens_padded[i] = pad_value;
+  }
+  for (int64_t b = 0; b < B; ++b) {
+    int64_t slot = -1; /* the sequence being filled in this row */
+    for (int64_t s = 0; s < S; ++s) {
+      int64_t t = b * S + s;
+      int64_t d = read_int(doc_ids, elem_bytes, t);
+      int64_t prev = s > 0 ? read_int(doc_ids, elem_bytes, t - 1) : 0;
+      int run_start = (s == 0) || (d != prev);
+      if (d != 0) {
+        if (run_start) { /* a new document run: a new sequence */
+          slot += 1;
+          if (slot >= num_packs) return ORC_CAPACITY;
+          seq_lens[b * num_packs + slot] = 0;
+          seq_lens_padded[b * num_packs + slot] = 0;
+          position_ids[t] = 0;
+        } else {
+          position_ids[t] = position_ids[t - 1] + 1;
+        }
+        seq_lens[b * num_packs + slot] += 1;
+        seq_lens_padded[b * num_packs + slot] += 1;
+      } else {
+        position_ids[t] = 0;
+        if (slot < 0) { /* padding before any document: an empty sequence */
+          slot = 0;
+          if (slot >= num_packs) return ORC_CAPACITY;
+          seq_lens[b * num_packs] = 0;
+          seq_lens_padded[b * num_packs] = 0;
+        }
+        seq_lens_padded[b * num_packs + slot] += 1;
+      }
+    }
+  }
   return ORC_OK;
 }

@@ -352,3 +352,174 @@ ALL_PINS = [
     pin_squeeze_closed_forms,
     pin_squeeze_errors,
 ]
+
+
+# --------------------------------------------------------------------------
+# O6 thd_padding_mask_from_token_ids
+# --------------------------------------------------------------------------
+def pin_mask_from_ids(lib):
+    """Hand cases from the page's rule, then brute force: accepted exactly
+    when the pad positions form a suffix (the mask never falls from True to
+    False), and then the mask is the value comparison."""
+    assert oracle.mask_from_token_ids(np.array([5, 6, 0, 0]), 0, lib=lib).tolist() == [False, False, True, True]
+    assert oracle.mask_from_token_ids(np.array([5, 6, 7]), 0, lib=lib).tolist() == [False] * 3
+    assert oracle.mask_from_token_ids(np.array([0, 0]), 0, lib=lib).tolist() == [True, True]
+    assert oracle.mask_from_token_ids(np.zeros(0, np.int64), 0, lib=lib).tolist() == []
+    for bad in ([5, 0, 6, 0], [0, 1], [3, 9, 9], [3, 3, 1, 3]):
+        pad = 0 if 0 in bad else 3
+        try:
+            oracle.mask_from_token_ids(np.array(bad), pad, lib=lib)
+        except oracle.OracleValueError:
+            continue
+        raise AssertionError(f"pad id inside content accepted: {bad}")
+    for n in range(0, 8):
+        for vals in itertools.product((0, 1, 2), repeat=n):
+            ids = np.asarray(vals, np.int64)
+            m = ids == 1
+            ok = bool(np.all(np.diff(m.astype(int)) >= 0)) if n > 1 else True
+            try:
+                got = oracle.mask_from_token_ids(ids, 1, lib=lib)
+                assert ok, (vals, "accepted")
+                assert np.array_equal(got, m)
+            except oracle.OracleValueError:
+                assert not ok, (vals, "rejected")
+
+
+# --------------------------------------------------------------------------
+# O7 first-fit-decreasing
+# --------------------------------------------------------------------------
+def _bins_of(offs, mem):
+    return [mem[offs[b]:offs[b + 1]].tolist() for b in range(len(offs) - 1)]
+
+
+def _optimal_bins(sizes, capacity):
+    """Brute force: fewest bins over every assignment (tiny inputs only)."""
+    n = len(sizes)
+    best = n
+    for assign in itertools.product(range(n), repeat=n):
+        if max(assign, default=-1) + 1 >= best:
+            continue
+        loads = [0] * n
+        for i, b in enumerate(assign):
+            loads[b] += sizes[i]
+        if all(x <= capacity for x in loads):
+            best = max(assign, default=-1) + 1
+    return best
+
+
+def pin_ffd(lib):
+    offs, mem = oracle.ffd(np.array([4, 8, 1, 4, 2, 1]), 10, lib=lib)
+    assert _bins_of(offs, mem) == [[1, 4], [0, 3, 2, 5]]
+    g = golden("ffd_johnson_worst_case.json")
+    offs, mem = oracle.ffd(np.array(g["sizes"]), g["capacity"], lib=lib)
+    assert len(offs) - 1 == g["ffd_bins"]
+    assert oracle.ffd(np.array([7, 7, 7]), 7, lib=lib)[0].size - 1 == 3
+    assert oracle.ffd(np.array([1, 2, 3]), 100, lib=lib)[1].tolist() == [2, 1, 0]
+    assert oracle.ffd(np.zeros(0, np.int64), 5, lib=lib)[0].tolist() == [0]
+    try:
+        oracle.ffd(np.array([3, 11]), 10, lib=lib)
+        raise AssertionError("oversized item accepted")
+    except oracle.OracleCapacityError:
+        pass
+    rng = np.random.default_rng(77)
+    for trial in range(40):
+        n = int(rng.integers(1, 7))
+        cap = int(rng.integers(4, 12))
+        sizes = rng.integers(1, cap + 1, size=n)
+        offs, mem = oracle.ffd(sizes, cap, lib=lib)
+        bins = _bins_of(offs, mem)
+        assert sorted(mem.tolist()) == list(range(n))
+        assert all(sum(sizes[i] for i in b) <= cap for b in bins)
+        opt = _optimal_bins(list(sizes), cap)
+        assert 9 * len(bins) <= 11 * opt + 6, (sizes, cap, bins, opt)  # FFD <= 11/9 OPT + 6/9
+        # within a bin, items appear largest first (the visiting order)
+        for b in bins:
+            assert all((sizes[b[k]], -b[k]) >= (sizes[b[k + 1]], -b[k + 1]) for k in range(len(b) - 1))
+
+
+# --------------------------------------------------------------------------
+# O8 doc_ids -> pack lengths
+# --------------------------------------------------------------------------
+def pin_doc_ids_to_lengths(lib):
+    r = oracle.doc_ids_to_lengths(np.array([[1, 1, 2, 2, 2, 0], [0, 0, 3, 3, 0, 4]], np.int32), 4, lib=lib)
+    assert r["seq_lens"].tolist() == [[2, 3, -1000, -1000], [0, 2, 1, -1000]]
+    assert r["seq_lens_padded"].tolist() == [[2, 4, -1000, -1000], [2, 3, 1, -1000]]
+    assert r["position_ids"].tolist() == [[0, 1, 0, 1, 2, 0], [0, 0, 0, 1, 0, 0]]
+    try:
+        oracle.doc_ids_to_lengths(np.array([[1, 2, 3]], np.int32), 2, lib=lib)
+        raise AssertionError("row over num_packs accepted")
+    except oracle.OracleCapacityError:
+        pass
+    # random maps: padded lengths tile each row; real lengths are the
+    # document runs (run-length encoding); the THD stream of the result is
+    # the row-major flattening; sequence starts are segment starts of O1
+    for seed in range(8):
+        rng = np.random.default_rng(900 + seed)
+        B, S = int(rng.integers(1, 4)), int(rng.integers(1, 30))
+        d = synth.random_doc_ids(rng, B, S, "runs", np.int32)
+        r = oracle.doc_ids_to_lengths(d, S, lib=lib)
+        real, padded = r["seq_lens"], r["seq_lens_padded"]
+        for b in range(B):
+            keep = real[b] != -1000
+            assert int(padded[b][keep].sum()) == S
+            key = torch.from_numpy(d[b].astype(np.int64))
+            vals, counts = torch.unique_consecutive(key, return_counts=True)
+            doc_runs = [int(c) for v, c in zip(vals.tolist(), counts.tolist()) if v != 0]
+            got = [int(x) for x in real[b][keep] if x > 0] if keep.any() else []
+            assert got == doc_runs, (d[b].tolist(), real[b].tolist())
+            for s in range(S):
+                if d[b, s] == 0:
+                    assert r["position_ids"][b, s] == 0
+                else:
+                    k = s
+                    while k > 0 and d[b, k - 1] == d[b, s]:
+                        k -= 1
+                    assert r["position_ids"][b, s] == s - k
+        out = oracle.process_input_for_thd({"input_ids": d.astype(np.int64), "seq_lens": real,
+                                            "seq_lens_padded": padded}, lib=lib)
+        assert np.array_equal(out["input_ids"], d.reshape(-1).astype(np.int64))
+        seg_cu, _ = oracle.from_doc_ids(d, lib=lib)
+        assert set(out["cu_seqlens_padded"][:-1].tolist()) <= set(seg_cu.tolist())
+
+
+# --------------------------------------------------------------------------
+# O9 split_batch_into_thd_chunks
+# --------------------------------------------------------------------------
+def pin_split_chunks(lib):
+    g = golden("thd_utils_split_example.json")
+    batch = {k: np.asarray(v, np.int64) for k, v in g["batch"].items()}
+    r = oracle.split_batch_into_thd_chunks(batch, g["num_chunks"], lib=lib)
+    assert r["input_ids"].tolist() == g["expected"]["input_ids"]
+    assert r["cu_seqlens"].tolist() == g["expected"]["cu_seqlens"]
+    assert r["labels"].shape == (2, 12) and r["padding_mask"].shape == (2, 12)
+    one = oracle.split_batch_into_thd_chunks(batch, 1, lib=lib)
+    assert one["cu_seqlens"].tolist() == [0, 6, 12, 18, 24]
+    # ragged chunk tables are padded with the filler value
+    batch2 = dict(batch)
+    batch2["seq_lens"] = np.array([[3, 3], [6, -1000], [2, 4], [1, 5]])
+    batch2["seq_lens_padded"] = np.array([[3, 3], [6, -1000], [2, 4], [1, 5]])
+    r2 = oracle.split_batch_into_thd_chunks(batch2, 2, lib=lib)
+    assert r2["cu_seqlens"].tolist() == [[0, 3, 6, 12, -1000], [0, 2, 6, 7, 12]]
+    assert r2["num_sequences"].tolist() == [3, 4]
+    for c in range(2):
+        sub = {k: (v[c * 2:(c + 1) * 2]) for k, v in batch2.items()}
+        single = oracle.process_input_for_thd(sub, lib=lib)
+        assert np.array_equal(r2["input_ids"][c], single["input_ids"])
+        assert r2["max_seqlen"][c] == single["max_seqlen"]
+    # chunks with different stream lengths cannot be stacked
+    batch3 = dict(batch2)
+    batch3["seq_lens"] = np.array([[3, 3], [5, -1000], [2, 4], [1, 5]])
+    batch3["seq_lens_padded"] = np.array([[3, 3], [5, -1000], [2, 4], [1, 5]])
+    try:
+        oracle.split_batch_into_thd_chunks(batch3, 2, lib=lib)
+        raise AssertionError("unequal chunk streams stacked")
+    except oracle.OracleValueError:
+        pass
+    try:
+        oracle.split_batch_into_thd_chunks(batch, 3, lib=lib)
+        raise AssertionError("num_chunks not dividing the batch accepted")
+    except ValueError:
+        pass
+
+
+ALL_PINS += [pin_mask_from_ids, pin_ffd, pin_doc_ids_to_lengths, pin_split_chunks]

@@ -43,6 +43,20 @@ MUTANTS = [
     ("o5_cu_from_padded", "run_real += real;\n      run_padded += padded;", "run_real += padded;\n      run_padded += padded;"),
     ("o5_source_row_is_bin", "in[(i * W + j) * elem_bytes + e]", "in[(b * W + j) * elem_bytes + e]"),
     ("o5_no_capacity_check", "if (run_padded + padded > capacity) return ORC_CAPACITY;", ""),
+    ("o6_inverted_compare", "mask[t] = (read_int(ids, elem_bytes, t) == pad_id) ? 1 : 0;",
+     "mask[t] = (read_int(ids, elem_bytes, t) != pad_id) ? 1 : 0;"),
+    ("o6_no_validation", "else if (seen_pad) return ORC_VALUE; /* content after a pad token */", ""),
+    ("o7_ascending", "if (sizes[a] > sizes[b] || (sizes[a] == sizes[b] && a < b)) best = j;",
+     "if (sizes[a] < sizes[b] || (sizes[a] == sizes[b] && a < b)) best = j;"),
+    ("o7_exact_fit_rejected", "while (b < bins && room[b] < sizes[item]) ++b;",
+     "while (b < bins && room[b] <= sizes[item]) ++b;"),
+    ("o7_ties_by_larger_index", "if (sizes[a] > sizes[b] || (sizes[a] == sizes[b] && a < b)) best = j;",
+     "if (sizes[a] > sizes[b] || (sizes[a] == sizes[b] && a > b)) best = j;"),
+    ("o8_pad_not_absorbed", "        seq_lens_padded[b * num_packs + slot] += 1;\n      }\n    }",
+     "      }\n    }"),
+    ("o8_positions_not_reset", "          position_ids[t] = 0;\n        } else {", "          position_ids[t] = s;\n        } else {"),
+    ("o8_leading_pad_dropped", "          slot = 0;\n          if (slot >= num_packs) return ORC_CAPACITY;\n          seq_lens[b * num_packs] = 0;\n          seq_lens_padded[b * num_packs] = 0;\n        }\n        seq_lens_padded[b * num_packs + slot] += 1;",
+     "          continue;\n        }\n        seq_lens_padded[b * num_packs + slot] += 1;"),
 ]
 
 
