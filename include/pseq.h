@@ -172,9 +172,10 @@ typedef struct pseq_field {
 
 size_t thd_workspace_size(int64_t B, int64_t num_packs);
 
-/* The whole conversion: thd_meta followed by thd_gather.  fields may be
- * NULL when num_fields == 0; padding_mask (one byte per stream slot, 1 =
- * padding; room for B*S) may be NULL. */
+/* The whole conversion: the work of thd_meta followed by thd_gather (one
+ * launch when B*num_packs <= 2048).  fields may be NULL when num_fields == 0;
+ * padding_mask (one byte per stream slot, 1 = padding; room for B*S) may be
+ * NULL. */
 pseq_status thd_from_batch(const int64_t* seq_lens,
                            const int64_t* seq_lens_padded, int64_t B,
                            int64_t S, int64_t num_packs, int64_t pad_value,
@@ -203,6 +204,104 @@ pseq_status thd_gather(const pseq_field* fields, int32_t num_fields,
                        int64_t B, int64_t S, int64_t num_packs,
                        uint8_t* padding_mask, const void* workspace,
                        size_t workspace_bytes, pseq_stream stream);
+
+/* ------------------------------------------------------------------------
+ * thd_chunks_from_batch -- split_batch_into_thd_chunks
+ * [thd_utils] "split_batch_into_thd_chunks": the batch is split along its
+ * rows into num_chunks equal chunks, each chunk is converted as by
+ * thd_from_batch, and the results are stacked; cu_seqlens arrays of
+ * different lengths are padded with pad_value.
+ * num_chunks must divide B; chunk c covers rows [c*B/num_chunks,
+ *   (c+1)*B/num_chunks).
+ * cu_seqlens, cu_seqlens_padded: int32 [num_chunks, B/num_chunks*num_packs+1];
+ *   row c holds the chunk's n_c+1 boundaries followed by pad_value.
+ *   cu_seqlens_padded may be NULL.
+ * fields: as for thd_from_batch (src rows are rows of the whole batch).  The
+ *   stream of chunk c starts planes*T_c*c rows into dst, so the results are
+ *   stacked [num_chunks, planes, T, row_elems] when every chunk has the same
+ *   stream length T.  dst room: planes * B * S * row_elems elements.
+ * padding_mask: chunk c's T_c bytes start at byte c*T_c (room B*S); may be
+ *   NULL.  pad_between_seqs: num_chunks bytes; may be NULL.
+ * infos: pseq_info [num_chunks], one per chunk (count n_c, max_seqlen,
+ *   total T_c).  Stacking needs every T_c equal; compare infos[c].total.
+ * workspace: thd_workspace_size(B / num_chunks, num_packs) bytes.
+ * ---------------------------------------------------------------------- */
+pseq_status thd_chunks_from_batch(const int64_t* seq_lens,
+                                  const int64_t* seq_lens_padded, int64_t B,
+                                  int64_t S, int64_t num_packs,
+                                  int64_t num_chunks, int64_t pad_value,
+                                  int32_t absorb_trailing_pad,
+                                  const pseq_field* fields, int32_t num_fields,
+                                  int32_t* cu_seqlens,
+                                  int32_t* cu_seqlens_padded,
+                                  uint8_t* padding_mask,
+                                  uint8_t* pad_between_seqs, pseq_info* infos,
+                                  void* workspace, size_t workspace_bytes,
+                                  pseq_stream stream);
+
+/* ------------------------------------------------------------------------
+ * thd_mask_from_token_ids -- thd_padding_mask_from_token_ids
+ * [thd_utils] "thd_padding_mask_from_token_ids": mask[t] = 1 where
+ *   input_ids[t] == padding_token_id.  A value comparison is only correct
+ *   when the pad id fills a right-padded tail and appears nowhere else, so a
+ *   pad token followed by any other token is PSEQ_ERR_VALUE (the page raises
+ *   ValueError).
+ * input_ids: n integers of id_bytes (4 or 8).  mask: n bytes.
+ * info: count = number of pad tokens, total = n.
+ * workspace: thd_mask_from_token_ids_workspace_size(n) bytes, ZERO-FILLED
+ *   before its first use; every completed call leaves its counter at zero.
+ *   Do not share it with pseq_from_doc_ids.
+ * ---------------------------------------------------------------------- */
+size_t thd_mask_from_token_ids_workspace_size(int64_t n);
+pseq_status thd_mask_from_token_ids(const void* input_ids, int32_t id_bytes,
+                                    int64_t n, int64_t padding_token_id,
+                                    uint8_t* mask, pseq_info* info,
+                                    void* workspace, size_t workspace_bytes,
+                                    pseq_stream stream);
+
+/* ------------------------------------------------------------------------
+ * pack_ffd -- first-fit-decreasing bins for pack_squeeze
+ * [who_packs] get_packer "picks which rows share a bin, by token budget";
+ *   First Fit Decreasing is one of the packers the page names.  Item i has
+ *   size lens[i] rounded up to `multiple`; items are visited largest first
+ *   (ties: smaller index first) and each goes into the first open bin with
+ *   room; a new bin opens when none has room.
+ * lens: int64 [n], n <= 8192.  bin_offsets: int32 [n+1] room (num_bins+1
+ *   written); bin_members: int32 [n], each bin's items in placement order --
+ *   the CSR input of pack_squeeze.
+ * info: count = num_bins, max_seqlen = fullest bin's load, total = sum of
+ *   the rounded sizes.
+ * Device errors: PSEQ_ERR_VALUE for a negative length, PSEQ_ERR_CAPACITY
+ *   for an item larger than capacity.
+ * ---------------------------------------------------------------------- */
+pseq_status pack_ffd(const int64_t* lens, int64_t n, int64_t multiple,
+                     int64_t capacity, int32_t* bin_offsets,
+                     int32_t* bin_members, pseq_info* info, pseq_stream stream);
+
+/* ------------------------------------------------------------------------
+ * pseq_doc_ids_to_lengths -- from the doc_ids map to pack lengths
+ * Joins [packed_seq]'s document map (1-based index per token, 0 = padding)
+ * to [thd_utils]' seq_lens / seq_lens_padded [B, num_packs] format (unused
+ * slots = pad_value).  Within a row, every maximal run of one non-zero index
+ * is a sequence (real length = run length); a padding run after a document
+ * run belongs to that sequence's padded length; a padding run at the start
+ * of a row is a sequence of real length 0.  position_ids [B, S] (int64, may
+ * be NULL) counts 0, 1, ... inside each document run and is 0 on padding.
+ * info: count = most sequences in one row, max_seqlen = longest document
+ *   run, total = sequences in all rows.
+ * Device errors: PSEQ_ERR_CAPACITY when a row holds more than num_packs
+ *   sequences (the slots that fit are written).
+ * workspace: pseq_doc_ids_to_lengths_workspace_size(B) bytes, ZERO-FILLED
+ *   before its first use; every completed call leaves its counter at zero.
+ * ---------------------------------------------------------------------- */
+size_t pseq_doc_ids_to_lengths_workspace_size(int64_t B);
+pseq_status pseq_doc_ids_to_lengths(const void* doc_ids, int32_t id_bytes,
+                                    int64_t B, int64_t S, int64_t num_packs,
+                                    int64_t pad_value, int64_t* seq_lens,
+                                    int64_t* seq_lens_padded,
+                                    int64_t* position_ids, pseq_info* info,
+                                    void* workspace, size_t workspace_bytes,
+                                    pseq_stream stream);
 
 /* ------------------------------------------------------------------------
  * thd_padding_mask

@@ -8,6 +8,14 @@ load it; the first call does, and raises if ``libpseq.so`` has not been built
 """
 from .api import (  # noqa: F401
     PackedSeqParams,
+    doc_ids_to_seq_lens,
+    first_fit_decreasing,
+    pack_ffd,
+    pseq_doc_ids_to_lengths,
+    split_batch_into_thd_chunks,
+    thd_chunks_from_batch,
+    thd_mask_from_token_ids,
+    thd_padding_mask_from_token_ids,
     _thd_padding_mask,
     check_info,
     pack_squeeze,

@@ -32,6 +32,14 @@ from . import _lib
 
 __all__ = [
     "PackedSeqParams",
+    "thd_chunks_from_batch",
+    "thd_mask_from_token_ids",
+    "pack_ffd",
+    "pseq_doc_ids_to_lengths",
+    "split_batch_into_thd_chunks",
+    "thd_padding_mask_from_token_ids",
+    "first_fit_decreasing",
+    "doc_ids_to_seq_lens",
     "pseq_from_doc_ids",
     "thd_from_batch",
     "thd_meta",
@@ -75,10 +83,14 @@ def _require_cuda(name: str, t: torch.Tensor, dtypes=None, device=None) -> torch
 class _WorkspaceCache:
     """One workspace buffer per (kind, device, stream), grown on demand.
 
-    ``kind == "scan"`` buffers are zero-filled when allocated; the doc_ids
-    scan leaves its workspace zero after every call, so reuse on the same
-    stream needs no further clearing.  Other kinds hold per-call scratch.
+    Kinds in ``ZEROED`` are zero-filled when allocated: those kernels need
+    a zeroed workspace and leave it zeroed after every call, so reuse on the
+    same stream needs no further clearing.  Each kind has its own buffer, so
+    one kernel's scratch never lands in another's.  Other kinds hold
+    per-call scratch.
     """
+
+    ZEROED = ("scan", "token_mask", "bridge")
 
     def __init__(self):
         self._bufs: dict = {}
@@ -91,7 +103,7 @@ class _WorkspaceCache:
             buf = self._bufs.get(key)
             if buf is None or buf.numel() < nbytes:
                 size = max(256, 1 << max(8, math.ceil(math.log2(max(nbytes, 1)))))
-                buf = (torch.zeros if kind == "scan" else torch.empty)(size, dtype=torch.uint8, device=device)
+                buf = (torch.zeros if kind in self.ZEROED else torch.empty)(size, dtype=torch.uint8, device=device)
                 self._bufs[key] = buf
             return buf
 
@@ -431,3 +443,177 @@ def squeeze_bins(input_ids: torch.Tensor, input_lengths: torch.Tensor, bins, mul
         "cu_seqlens_flat": cu[: r["num_members"] + r["num_bins"]],
         "cu_seqlens_padded_flat": cup[: r["num_members"] + r["num_bins"]],
     }
+
+
+# ----------------------------------------------------------------------------
+# chunked THD, value mask, bin packing, doc_ids bridge (C entry points)
+# ----------------------------------------------------------------------------
+def thd_chunks_from_batch(seq_lens: torch.Tensor, seq_lens_padded: torch.Tensor | None, S: int, num_chunks: int,
+                          fields=(), pad_value: int = -1000, absorb_trailing_pad: bool = True, want_mask: bool = True):
+    """Enqueue the chunked conversion.  Returns device buffers sized for the
+    worst case, ``infos`` (num_chunks x 16 bytes) and ``pad_between``
+    (num_chunks bytes)."""
+    lib = _lib.load()
+    _require_cuda("seq_lens", seq_lens, (torch.int64,))
+    dev = seq_lens.device
+    if seq_lens_padded is not None:
+        _require_cuda("seq_lens_padded", seq_lens_padded, (torch.int64,), dev)
+        if seq_lens_padded.shape != seq_lens.shape:
+            raise ValueError("seq_lens_padded must have the shape of seq_lens")
+    B, P = seq_lens.shape
+    if num_chunks < 1 or B % num_chunks:
+        raise ValueError("num_chunks must evenly divide the batch size")
+    Bc = B // num_chunks
+    arr, dsts = _fields(fields, B, S, dev)
+    width = Bc * P + 1
+    cu = torch.empty((num_chunks, width), dtype=torch.int32, device=dev)
+    cup = torch.empty((num_chunks, width), dtype=torch.int32, device=dev) if seq_lens_padded is not None else None
+    mask = torch.empty(B * S, dtype=torch.bool, device=dev) if want_mask else None
+    infos = torch.empty((num_chunks, 4), dtype=torch.int32, device=dev)
+    pbs = torch.empty(num_chunks, dtype=torch.uint8, device=dev)
+    ws = _workspaces.get("thd", lib.thd_workspace_size(Bc, P), dev)
+    _lib.check(lib.thd_chunks_from_batch(_p(seq_lens), _p(seq_lens_padded), B, S, P, num_chunks, pad_value,
+                                         1 if absorb_trailing_pad else 0, arr if fields else None, len(fields),
+                                         _p(cu), _p(cup), _p(mask), _p(pbs), _p(infos), _p(ws), ws.numel(),
+                                         _stream(dev)))
+    return {"cu_seqlens": cu, "cu_seqlens_padded": cup, "padding_mask": mask, "dst": dsts, "infos": infos,
+            "pad_between": pbs}
+
+
+def thd_mask_from_token_ids(input_ids: torch.Tensor, padding_token_id: int):
+    """Enqueue the value-compare mask.  Returns ``(mask, info)``."""
+    lib = _lib.load()
+    _require_cuda("input_ids", input_ids, (torch.int32, torch.int64))
+    dev = input_ids.device
+    n = input_ids.numel()
+    mask = torch.empty(n, dtype=torch.bool, device=dev)
+    info = _new_info(dev)
+    ws = _workspaces.get("token_mask", lib.thd_mask_from_token_ids_workspace_size(n), dev)
+    _lib.check(lib.thd_mask_from_token_ids(_p(input_ids), input_ids.element_size(), n, int(padding_token_id),
+                                           _p(mask), _p(info), _p(ws), ws.numel(), _stream(dev)))
+    return mask.view(input_ids.shape), info
+
+
+def pack_ffd(lens: torch.Tensor, capacity: int, multiple: int = 1):
+    """Enqueue first-fit-decreasing.  Returns ``(bin_offsets [n+1],
+    bin_members [n], info)``; the first ``info.count + 1`` offsets are valid."""
+    lib = _lib.load()
+    _require_cuda("lens", lens, (torch.int64,))
+    dev = lens.device
+    n = lens.numel()
+    offs = torch.empty(n + 1, dtype=torch.int32, device=dev)
+    mem = torch.empty(max(n, 1), dtype=torch.int32, device=dev)
+    info = _new_info(dev)
+    _lib.check(lib.pack_ffd(_p(lens), n, multiple, capacity, _p(offs), _p(mem), _p(info), _stream(dev)))
+    return offs, mem[:n], info
+
+
+def pseq_doc_ids_to_lengths(doc_ids: torch.Tensor, num_packs: int, pad_value: int = -1000,
+                            with_positions: bool = True):
+    """Enqueue the doc_ids -> pack lengths bridge.  Returns ``(seq_lens,
+    seq_lens_padded, position_ids or None, info)``."""
+    lib = _lib.load()
+    _require_cuda("doc_ids", doc_ids, (torch.int32, torch.int64))
+    if doc_ids.dim() != 2:
+        raise ValueError("doc_ids must be [batch, sequence]")
+    dev = doc_ids.device
+    B, S = doc_ids.shape
+    real = torch.empty((B, num_packs), dtype=torch.int64, device=dev)
+    padded = torch.empty((B, num_packs), dtype=torch.int64, device=dev)
+    pos = torch.empty((B, S), dtype=torch.int64, device=dev) if with_positions else None
+    info = _new_info(dev)
+    ws = _workspaces.get("bridge", lib.pseq_doc_ids_to_lengths_workspace_size(B), dev)
+    _lib.check(lib.pseq_doc_ids_to_lengths(_p(doc_ids), doc_ids.element_size(), B, S, num_packs, pad_value, _p(real),
+                                           _p(padded), _p(pos), _p(info), _p(ws), ws.numel(), _stream(dev)))
+    return real, padded, pos, info
+
+
+# ----------------------------------------------------------------------------
+# the pages' functions for those rows
+# ----------------------------------------------------------------------------
+def split_batch_into_thd_chunks(batch: dict, num_chunks: int, seq_lens_padding_value: int = -1000,
+                                padding_token_id: int = 0) -> dict:
+    """NeMo AutoModel v0.5 thd_utils, ``split_batch_into_thd_chunks``.
+
+    Splits the batch along its rows into ``num_chunks`` chunks, converts each
+    as ``process_input_for_thd`` does and stacks the results on a new leading
+    axis; ``cu_seqlens`` / ``cu_seqlens_padded`` rows are padded with
+    ``seq_lens_padding_value``.  ``max_seqlen`` becomes an int32 tensor
+    [num_chunks] and ``pad_between_seqs`` a bool tensor [num_chunks].
+    Chunks whose streams differ in length cannot be stacked: ValueError.
+    """
+    if num_chunks <= 1:
+        return process_input_for_thd(batch, seq_lens_padding_value, padding_token_id)
+    ids = batch["input_ids"]
+    B, S = int(ids.shape[0]), int(ids.shape[1])
+    fields = [(ids, 1)]
+    names = ["input_ids"]
+    if batch.get("labels") is not None:
+        fields.append((batch["labels"], 1))
+        names.append("labels")
+    pos = batch.get("position_ids")
+    if pos is not None:
+        fields.append((pos, int(pos.shape[0]) if pos.dim() == 3 else 1))
+        names.append("position_ids")
+    r = thd_chunks_from_batch(batch["seq_lens"], batch.get("seq_lens_padded"), S, num_chunks, fields,
+                              seq_lens_padding_value, True)
+    infos = r["infos"].tolist()
+    for c, (st, _, _, _) in enumerate(infos):
+        if st != _lib.PSEQ_OK:
+            name = _lib.STATUS_NAMES.get(st, str(st))
+            raise (ValueError if st in (_lib.PSEQ_ERR_VALUE, _lib.PSEQ_ERR_CAPACITY) else RuntimeError)(
+                f"split_batch_into_thd_chunks: chunk {c}: device reported {name}")
+    totals = {t for _, _, _, t in infos}
+    if len(totals) != 1:
+        raise ValueError(f"split_batch_into_thd_chunks: chunk streams have different lengths {sorted(totals)} "
+                         "and cannot be stacked")
+    T = totals.pop()
+    width = max(n for _, n, _, _ in infos) + 1
+    out = {k: v for k, v in batch.items() if not isinstance(v, torch.Tensor) and k not in _THD_KEYS}
+    for name, (dst, planes, row) in zip(names, r["dst"]):
+        flat = dst[: num_chunks * planes * T * (math.prod(row) if row else 1)]
+        if name == "position_ids" and planes > 1:
+            out[name] = flat.view(num_chunks, planes, 1, T)
+        else:
+            out[name] = flat.view(num_chunks, T, *row)
+    out["cu_seqlens"] = r["cu_seqlens"][:, :width]
+    if r["cu_seqlens_padded"] is not None:
+        out["cu_seqlens_padded"] = r["cu_seqlens_padded"][:, :width]
+    out["pad_between_seqs"] = r["pad_between"].view(torch.bool)
+    out["max_seqlen"] = r["infos"][:, 2]
+    out["padding_mask"] = r["padding_mask"][: num_chunks * T].view(num_chunks, T)
+    return out
+
+
+def thd_padding_mask_from_token_ids(input_ids: torch.Tensor, padding_token_id: int) -> torch.Tensor:
+    """NeMo AutoModel v0.5 thd_utils, ``thd_padding_mask_from_token_ids``:
+    bool mask (True = padding) by value; ValueError when the pad id also
+    occurs as content (anywhere before the right-padded tail)."""
+    mask, info = thd_mask_from_token_ids(input_ids, padding_token_id)
+    st = _info_view(info).tolist()[0]
+    if st != _lib.PSEQ_OK:
+        raise ValueError(f"padding_token_id {padding_token_id} also occurs as content")
+    return mask
+
+
+def first_fit_decreasing(lens: torch.Tensor, capacity: int, multiple: int = 1):
+    """First-fit-decreasing bins ("Who packs the sequences": get_packer, by
+    token budget).  Returns ``(bin_offsets, bin_members)`` int32 CUDA tensors,
+    ready for ``pack_squeeze``."""
+    offs, mem, info = pack_ffd(lens, capacity, multiple)
+    _, nb, _, _ = check_info(info, "first_fit_decreasing")
+    return offs[: nb + 1], mem
+
+
+def doc_ids_to_seq_lens(doc_ids: torch.Tensor, num_packs: int | None = None, pad_value: int = -1000) -> dict:
+    """From a neat-packing document map to ``seq_lens``, ``seq_lens_padded``
+    [B, num_packs] and ``position_ids`` [B, S] for ``process_input_for_thd``.
+    ``num_packs`` defaults to the most sequences any row holds."""
+    if num_packs is None:
+        # first pass sizes the table: the most sequences any row holds
+        S = int(doc_ids.shape[1]) if doc_ids.dim() == 2 else 0
+        _, _, _, info = pseq_doc_ids_to_lengths(doc_ids, S, pad_value, with_positions=False)
+        _, num_packs, _, _ = check_info(info, "doc_ids_to_seq_lens")
+    real, padded, pos, info = pseq_doc_ids_to_lengths(doc_ids, num_packs, pad_value)
+    check_info(info, "doc_ids_to_seq_lens")
+    return {"seq_lens": real, "seq_lens_padded": padded, "position_ids": pos}

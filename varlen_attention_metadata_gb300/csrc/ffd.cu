@@ -1,0 +1,200 @@
+// pack_ffd: first-fit-decreasing bin assignment for the trainer-side squeeze.
+//
+// "Who packs the sequences: the loader, or the trainer?" has get_packer pick
+// which rows share a bin by token budget and names First Fit Decreasing among
+// the packers.  The textbook algorithm: visit the items largest first (ties:
+// smaller index first) and put each into the first open bin with room.
+//
+// One CTA.  Each item becomes a 64-bit key (inverted size, index) so an
+// ascending bitonic sort in shared memory yields the visiting order.  First
+// fit is inherently sequential over items, so one warp walks them in order;
+// for each item the 32 lanes test 32 bins at a time against the remaining
+// room and a ballot picks the first that fits.  Bins are numbered in the order
+// they open, members keep their placement order, and a block scan of the bin
+// counts turns the placements into CSR arrays.
+#include "common.cuh"
+
+namespace pseq {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kMaxItems = 8192;
+
+__global__ void __launch_bounds__(kThreads)
+    ffd_kernel(const int64_t* __restrict__ lens, int n, int64_t multiple, int64_t capacity, int32_t* bin_offsets,
+               int32_t* bin_members, pseq_info* info) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int pow2 = n <= 1 ? 1 : 1 << (32 - __clz(n - 1));
+  unsigned long long* key = reinterpret_cast<unsigned long long*>(smem);  // [pow2]
+  int32_t* room = reinterpret_cast<int32_t*>(key + pow2);               // [n] per bin
+  int32_t* bin_of = room + (n > 0 ? n : 1);                              // [n] per sorted item
+  int32_t* slot_of = bin_of + (n > 0 ? n : 1);                           // [n] per sorted item
+  int32_t* count = slot_of + (n > 0 ? n : 1);                            // [n] per bin
+  __shared__ int s_bad, s_big, s_bins;
+  __shared__ long long s_total, s_fullest;
+  pdl_enter();
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_bad = s_big = 0;
+    s_total = 0;
+    s_fullest = 0;
+  }
+  __syncthreads();
+  // keys: (INT32_MAX - size) in the high word sorts sizes descending, the
+  // index in the low word breaks ties toward the smaller index
+  for (int i = tid; i < pow2; i += kThreads) {
+    unsigned long long k = ~0ull;  // padding sorts last
+    if (i < n) {
+      const long long real = lens[i];
+      long long size = 0;
+      if (real < 0) {
+        s_bad = 1;
+      } else if (real > capacity) {
+        s_big = 1;
+      } else {
+        size = (real + multiple - 1) / multiple * multiple;
+        if (size > capacity) s_big = 1;
+        atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), (unsigned long long)size);
+      }
+      if (size > INT32_MAX) size = INT32_MAX;
+      k = ((unsigned long long)(INT32_MAX - size) << 32) | (unsigned)i;
+    }
+    key[i] = k;
+  }
+  __syncthreads();
+  for (int width = 2; width <= pow2; width <<= 1) {
+    for (int stride = width >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < pow2; i += kThreads) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool up = (i & width) == 0;
+          const unsigned long long a = key[i], b = key[j];
+          if ((a > b) == up) {
+            key[i] = b;
+            key[j] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (s_bad || s_big) {
+    if (tid == 0) *info = {s_bad ? PSEQ_ERR_VALUE : PSEQ_ERR_CAPACITY, 0, 0, 0};
+    return;
+  }
+  // first fit, one warp, items in visiting order
+  if (tid < 32) {
+    const int lane = tid;
+    int bins = 0;
+    for (int k = 0; k < n; ++k) {
+      const long long size = INT32_MAX - (long long)(key[k] >> 32);
+      int chosen = -1;
+      for (int base = 0; base < bins && chosen < 0; base += 32) {
+        const int b = base + lane;
+        const unsigned fits = __ballot_sync(~0u, b < bins && room[b] >= size);
+        if (fits) chosen = base + __ffs(fits) - 1;
+      }
+      if (chosen < 0) {
+        chosen = bins;
+        if (lane == 0) {
+          room[chosen] = (int32_t)capacity;
+          count[chosen] = 0;
+        }
+        bins += 1;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        room[chosen] -= (int32_t)size;
+        bin_of[k] = chosen;
+        slot_of[k] = count[chosen];
+        count[chosen] += 1;
+      }
+      __syncwarp();
+    }
+    if (lane == 0) s_bins = bins;
+  }
+  __syncthreads();
+  const int bins = s_bins;
+  // bin_offsets = [0] + cumsum(count): a block scan, the bins in chunks
+  __shared__ int s_warp[kThreads / 32];
+  __shared__ int s_carry;
+  if (tid == 0) s_carry = 0;
+  __syncthreads();
+  for (int base = 0; base < bins; base += kThreads) {
+    const int b = base + tid;
+    const int c = b < bins ? count[b] : 0;
+    int inc = c;
+    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(~0u, inc, d);
+      if (lane >= d) inc += o;
+    }
+    if (lane == 31) s_warp[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+      int w = s_warp[lane];
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(~0u, w, d);
+        if (lane >= d) w += o;
+      }
+      s_warp[lane] = w;
+    }
+    __syncthreads();
+    const int excl = s_carry + inc - c + (warp > 0 ? s_warp[warp - 1] : 0);
+    if (b < bins) {
+      bin_offsets[b] = excl;
+      count[b] = excl;  // reuse as the bin's first member position
+      const long long load = capacity - room[b];
+      atomicMax(reinterpret_cast<unsigned long long*>(&s_fullest), (unsigned long long)load);
+    }
+    __syncthreads();
+    if (tid == 0) s_carry += s_warp[kThreads / 32 - 1];
+    __syncthreads();
+  }
+  for (int k = tid; k < n; k += kThreads) bin_members[count[bin_of[k]] + slot_of[k]] = (int32_t)(key[k] & 0xffffffffu);
+  if (tid == 0) {
+    bin_offsets[bins] = n;
+    *info = {PSEQ_OK, bins, (int32_t)min(s_fullest, (long long)INT32_MAX), (int32_t)min(s_total, (long long)INT32_MAX)};
+  }
+}
+
+size_t ffd_smem(int n) {
+  int pow2 = 1;
+  while (pow2 < n) pow2 <<= 1;
+  const size_t m = n > 0 ? (size_t)n : 1;
+  return round_up(8 * (size_t)pow2 + 4 * m * 4, 16);
+}
+
+}  // namespace
+}  // namespace pseq
+
+using namespace pseq;
+
+extern "C" pseq_status pack_ffd(const int64_t* lens, int64_t n, int64_t multiple, int64_t capacity,
+                                int32_t* bin_offsets, int32_t* bin_members, pseq_info* info, pseq_stream stream) {
+  clear_error();
+  const char* fn = "pack_ffd";
+  if (n < 0 || n > kMaxItems) return fail(PSEQ_ERR_ARG, "%s: n must be in [0, %d]", fn, kMaxItems);
+  if (multiple < 1 || multiple > INT32_MAX) return fail(PSEQ_ERR_ARG, "%s: multiple must be in [1, INT32_MAX]", fn);
+  if (capacity < 0 || capacity > INT32_MAX) return fail(PSEQ_ERR_ARG, "%s: capacity must be in [0, INT32_MAX]", fn);
+  if (!bin_offsets || !info || (n > 0 && (!lens || !bin_members))) return fail(PSEQ_ERR_ARG, "%s: NULL pointer", fn);
+  if (!aligned(lens, 8) || !aligned(bin_offsets, 4) || !aligned(bin_members, 4) || !aligned(info, 4))
+    return fail(PSEQ_ERR_ARG, "%s: misaligned pointer", fn);
+  const size_t smem = ffd_smem((int)n);
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(ffd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ffd_smem(kMaxItems));
+    if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    attr_set[dev] = true;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = launch_pdl(ffd_kernel, dim3(1), dim3(kThreads), smem, st, lens, (int)n, multiple, capacity,
+                                   bin_offsets, bin_members, info);
+  count_launches(1);
+  if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  return check_launch(fn);
+}

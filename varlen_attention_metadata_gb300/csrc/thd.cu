@@ -94,6 +94,9 @@ struct MetaArgs {
   uint8_t* pad_between;  // may be NULL
   pseq_info* info;
   int64_t fixed_total;   // >= 0: mask length and info.total (thd_padding_mask)
+  int row0;              // source row of this table's first row (chunks)
+  int chunks;            // > 1: blockIdx.y selects a chunk of B rows (fused kernel)
+  int64_t cu_pad_to;     // > 0: fill cu arrays from n+1 up to this length with pad_value
 };
 
 // ----------------------------------------------------------------------------
@@ -190,6 +193,10 @@ __device__ __forceinline__ Summary summarize(const MetaArgs& a, const ScanResult
 __device__ __forceinline__ void write_meta(const MetaArgs& a, const Summary& s) {
   if (a.cu) a.cu[s.n] = (int32_t)s.cu_last;
   if (a.cu_padded) a.cu_padded[s.n] = (int32_t)s.T;
+  for (int64_t k = s.n + 1; k < a.cu_pad_to; ++k) {
+    if (a.cu) a.cu[k] = (int32_t)a.pad_value;
+    if (a.cu_padded) a.cu_padded[k] = (int32_t)a.pad_value;
+  }
   if (a.pad_between) *a.pad_between = (uint8_t)s.pad_between;
   *a.info = s.status == PSEQ_OK ? pseq_info{PSEQ_OK, s.n, (int32_t)s.longest, (int32_t)s.shown_total}
                                 : pseq_info{s.status, 0, 0, 0};
@@ -213,9 +220,11 @@ struct Fields {
 // Move stream rows [lo, hi) of every field and write their mask bytes.
 // Sequences j = 0..cnt-1 of the table start at stream row cup[j] (cup[cnt]
 // ends the last one) and at source token src_tok[j]; cup[0] <= lo and
-// hi <= cup[cnt].
+// hi <= cup[cnt].  B is the source's rows per plane; stream `chunk` of a
+// stacked result starts chunk * planes * T rows into each destination.
 __device__ void gather_rows(const Fields& f, int64_t B, int64_t S, int64_t T, uint8_t* mask, int64_t lo,
-                            int64_t hi, const int32_t* cup, const int32_t* src_tok, const int32_t* real, int cnt) {
+                            int64_t hi, const int32_t* cup, const int32_t* src_tok, const int32_t* real, int cnt,
+                            int64_t chunk) {
   if (lo >= hi) return;
   const int tid = threadIdx.x, nt = blockDim.x;
   const int64_t plane_in = B * S;
@@ -239,7 +248,7 @@ __device__ void gather_rows(const Fields& f, int64_t B, int64_t S, int64_t T, ui
           if (g + q < f.njobs) {
             const int i = f.job_field[g + q], p = f.job_plane[g + q];
             const int64_t rb = f.row_bytes[i];
-            store_row(f.dst[i] + ((int64_t)p * T + r) * rb, v[q], (int)rb);
+            store_row(f.dst[i] + ((chunk * f.planes[i] + p) * T + r) * rb, v[q], (int)rb);
           }
         }
       }
@@ -256,8 +265,8 @@ __device__ void gather_rows(const Fields& f, int64_t B, int64_t S, int64_t T, ui
     for (int i = 0; i < f.num; ++i) {
       const int64_t rb = f.row_bytes[i];
       for (int p = 0; p < f.planes[i]; ++p)
-        block_copy(f.dst[i] + ((int64_t)p * T + a0) * rb, f.src[i] + ((int64_t)p * plane_in + tok) * rb,
-                   (a1 - a0) * rb);
+        block_copy(f.dst[i] + ((chunk * f.planes[i] + p) * T + a0) * rb,
+                   f.src[i] + ((int64_t)p * plane_in + tok) * rb, (a1 - a0) * rb);
     }
     if (mask) {
       const int64_t real_end = cs + real[j];
@@ -284,37 +293,51 @@ __global__ void __launch_bounds__(kRowThreads, 2)
   __shared__ Triple scratch[kRowThreads / 32];
   __shared__ ScanFlags fl;
   pdl_enter();
-  const int E = a.B * a.P;
+  // chunk blockIdx.y: rows [c*B, (c+1)*B) of a batch of chunks*B rows
+  const int c = blockIdx.y;
+  MetaArgs ac = a;
+  if (a.chunks > 1) {
+    const int64_t e0 = (int64_t)c * a.B * a.P;
+    ac.real = a.real + e0;
+    ac.padded = a.padded ? a.padded + e0 : nullptr;
+    ac.row0 = c * a.B;
+    ac.cu = a.cu ? a.cu + c * a.cu_pad_to : nullptr;
+    ac.cu_padded = a.cu_padded ? a.cu_padded + c * a.cu_pad_to : nullptr;
+    ac.pad_between = a.pad_between ? a.pad_between + c : nullptr;
+    ac.info = a.info + c;
+  }
+  const int E = ac.B * ac.P;
   int64_t* s_row = reinterpret_cast<int64_t*>(smem);
-  int32_t* s_cup = reinterpret_cast<int32_t*>(s_row + (a.P > 0 ? a.B : 0));
+  int32_t* s_cup = reinterpret_cast<int32_t*>(s_row + (ac.P > 0 ? ac.B : 0));
   int32_t* s_src = s_cup + E + 1;
   int32_t* s_real = s_src + E;
   const bool lead = blockIdx.x == 0;
   auto put = [&](int k, int b, long long o, long long real, long long padded, long long R, long long Pd) {
     s_cup[k] = (int32_t)Pd;
-    s_src[k] = (int32_t)(b * a.S + o);
+    s_src[k] = (int32_t)((ac.row0 + b) * ac.S + o);
     s_real[k] = (int32_t)real;
     if (lead) {
-      if (a.cu) a.cu[k] = (int32_t)R;
-      if (a.cu_padded) a.cu_padded[k] = (int32_t)Pd;
+      if (ac.cu) ac.cu[k] = (int32_t)R;
+      if (ac.cu_padded) ac.cu_padded[k] = (int32_t)Pd;
     }
   };
-  const ScanResult r = scan_lengths<kRowThreads>(a, s_row, scratch, &fl, put);
-  const Summary s = summarize(a, r, fl, r.n ? s_real[r.n - 1] : 0);
+  const ScanResult r = scan_lengths<kRowThreads>(ac, s_row, scratch, &fl, put);
+  const Summary s = summarize(ac, r, fl, r.n ? s_real[r.n - 1] : 0);
   if (threadIdx.x == 0) {
     s_cup[r.n] = (int32_t)s.T;
-    if (lead) write_meta(a, s);
+    if (lead) write_meta(ac, s);
   }
   __syncthreads();
   if (s.status != PSEQ_OK) return;
   const int64_t T = s.T, Tm = s.shown_total;
-  if (Tm > mask_cap || T > Tm || T > (int64_t)a.B * a.S) return;  // cannot happen for well-formed input
+  if (Tm > mask_cap || T > Tm || T > (int64_t)ac.B * ac.S) return;  // cannot happen for well-formed input
   int64_t r0, r1;
   slice_of(Tm, r0, r1);
-  gather_rows(f, a.B, a.S, T, mask, r0, min(r1, T), s_cup, s_src, s_real, r.n);
-  if (mask) {
+  uint8_t* m = mask ? mask + (int64_t)c * Tm : nullptr;
+  gather_rows(f, (int64_t)ac.B * a.chunks, ac.S, T, m, r0, min(r1, T), s_cup, s_src, s_real, r.n, c);
+  if (m) {
     const int64_t tail = max(r0, T);
-    if (tail < r1) block_fill_bytes(mask + tail, r1 - tail, 1);
+    if (tail < r1) block_fill_bytes(m + tail, r1 - tail, 1);
   }
 }
 
@@ -323,7 +346,7 @@ __global__ void __launch_bounds__(kMetaThreads) thd_meta_kernel(const __grid_con
   __shared__ ScanFlags fl;
   pdl_enter();
   auto put = [&](int k, int b, long long o, long long real, long long padded, long long R, long long Pd) {
-    ws.seq_src[k] = (long long)b * a.S + o;
+    ws.seq_src[k] = (long long)(a.row0 + b) * a.S + o;
     ws.seq_real[k] = (int32_t)real;
     ws.seq_cup[k] = (int32_t)Pd;
     if (a.cu) a.cu[k] = (int32_t)R;
@@ -344,7 +367,7 @@ __global__ void __launch_bounds__(kMetaThreads) thd_meta_kernel(const __grid_con
 
 __global__ void __launch_bounds__(kRowThreads, 2)
     thd_gather_kernel(const __grid_constant__ Fields f, int64_t B, int64_t S, uint8_t* __restrict__ mask,
-                      Workspace ws, int64_t max_seqs, int64_t max_rows) {
+                      Workspace ws, int64_t max_seqs, int64_t max_rows, int64_t plane_rows, int64_t chunk) {
   __shared__ int32_t s_cup[kTableBatch + 1];
   __shared__ int32_t s_src[kTableBatch];
   __shared__ int32_t s_real[kTableBatch];
@@ -360,6 +383,7 @@ __global__ void __launch_bounds__(kRowThreads, 2)
   int64_t r0, r1;
   slice_of(Tm, r0, r1);
   if (r0 >= r1) return;
+  if (mask) mask += chunk * Tm;
   const int64_t g1 = min(r1, T);
   const int tid = threadIdx.x, lane = tid & 31;
   int64_t lo = r0;
@@ -387,7 +411,7 @@ __global__ void __launch_bounds__(kRowThreads, 2)
     }
     __syncthreads();
     const int64_t hi = min(g1, (int64_t)s_cup[cnt]);
-    gather_rows(f, B, S, T, mask, lo, hi, s_cup, s_src, s_real, cnt);
+    gather_rows(f, plane_rows, S, T, mask, lo, hi, s_cup, s_src, s_real, cnt, chunk);
     lo = hi;
     __syncthreads();
   }
@@ -496,7 +520,8 @@ pseq_status launch_fused(const char* fn, const MetaArgs& a, const Fields& f, uin
   const size_t smem = fused_smem(a);
   const int64_t rows = a.fixed_total >= 0 ? a.fixed_total : (int64_t)a.B * a.S;
   const int grid = row_grid(reinterpret_cast<const void*>(thd_fused_kernel), smem, rows, f);
-  const cudaError_t e = launch_pdl(thd_fused_kernel, dim3(grid), dim3(kRowThreads), smem, st, a, f, mask, mask_cap);
+  const cudaError_t e = launch_pdl(thd_fused_kernel, dim3(grid, (unsigned)a.chunks), dim3(kRowThreads), smem, st, a,
+                                   f, mask, mask_cap);
   count_launches(1);
   if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
   return check_launch(fn);
@@ -510,13 +535,17 @@ pseq_status launch_meta(const char* fn, const MetaArgs& a, void* workspace, cuda
   return check_launch(fn);
 }
 
+// plane_rows: source rows per plane (B unless this is one chunk of a larger
+// batch); chunk: position of this stream in a stacked result.
 pseq_status launch_gather(const char* fn, const Fields& f, int64_t B, int64_t S, int64_t P, uint8_t* mask,
-                          const void* workspace, cudaStream_t st, int64_t mask_rows) {
+                          const void* workspace, cudaStream_t st, int64_t mask_rows, int64_t plane_rows = -1,
+                          int64_t chunk = 0) {
   if (f.num == 0 && !mask) return PSEQ_OK;
   const int64_t E = B * P;
   const int grid = row_grid(reinterpret_cast<const void*>(thd_gather_kernel), 0, mask_rows, f);
   Workspace ws = carve(workspace, B, E);
-  cudaError_t e = launch_pdl(thd_gather_kernel, dim3(grid), dim3(kRowThreads), 0, st, f, B, S, mask, ws, E, mask_rows);
+  cudaError_t e = launch_pdl(thd_gather_kernel, dim3(grid), dim3(kRowThreads), 0, st, f, B, S, mask, ws, E, mask_rows,
+                             plane_rows < 0 ? B : plane_rows, chunk);
   count_launches(1);
   if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
   return check_launch(fn);
@@ -539,6 +568,9 @@ MetaArgs thd_args(const int64_t* seq_lens, const int64_t* seq_lens_padded, int64
   a.pad_between = pad_between;
   a.info = info;
   a.fixed_total = -1;
+  a.row0 = 0;
+  a.chunks = 1;
+  a.cu_pad_to = 0;
   return a;
 }
 
@@ -635,4 +667,53 @@ extern "C" pseq_status thd_padding_mask(int64_t total_tokens, const int64_t* val
   s = launch_meta(fn, a, workspace, st);
   if (s != PSEQ_OK || total_tokens == 0) return s;
   return launch_gather(fn, f, 1, total_tokens, n, mask, workspace, st, total_tokens);
+}
+
+extern "C" pseq_status thd_chunks_from_batch(const int64_t* seq_lens, const int64_t* seq_lens_padded, int64_t B,
+                                             int64_t S, int64_t num_packs, int64_t num_chunks, int64_t pad_value,
+                                             int32_t absorb_trailing_pad, const pseq_field* fields,
+                                             int32_t num_fields, int32_t* cu_seqlens, int32_t* cu_seqlens_padded,
+                                             uint8_t* padding_mask, uint8_t* pad_between_seqs, pseq_info* infos,
+                                             void* workspace, size_t workspace_bytes_, pseq_stream stream) {
+  clear_error();
+  const char* fn = "thd_chunks_from_batch";
+  pseq_status s = check_lengths(fn, B, S, num_packs);
+  if (s != PSEQ_OK) return s;
+  if (num_chunks < 1 || B % num_chunks != 0)
+    return fail(PSEQ_ERR_ARG, "%s: num_chunks must be >= 1 and divide B (B=%lld, num_chunks=%lld)", fn, (long long)B,
+                (long long)num_chunks);
+  if (num_chunks > 65535) return fail(PSEQ_ERR_ARG, "%s: at most 65535 chunks", fn);
+  if (!cu_seqlens || !infos) return fail(PSEQ_ERR_ARG, "%s: cu_seqlens and infos are required", fn);
+  const int64_t Bc = B / num_chunks;
+  Fields f;
+  s = build_fields(fn, fields, num_fields, B, S, f);
+  if (s != PSEQ_OK) return s;
+  MetaArgs a = thd_args(seq_lens, seq_lens_padded, Bc, S, num_packs, pad_value, absorb_trailing_pad, cu_seqlens,
+                        cu_seqlens_padded, pad_between_seqs, infos);
+  a.cu_pad_to = Bc * num_packs + 1;
+  s = check_meta(fn, a, workspace, workspace_bytes_);
+  if (s != PSEQ_OK) return s;
+  if (!aligned(seq_lens, 8) || !aligned(seq_lens_padded, 8)) return fail(PSEQ_ERR_ARG, "%s: misaligned pointer", fn);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (Bc * num_packs <= kFusedMaxEntries) {
+    a.chunks = (int)num_chunks;
+    return launch_fused(fn, a, f, padding_mask, Bc * S, st);
+  }
+  // large tables: each chunk through the two-kernel path, one after another
+  for (int64_t c = 0; c < num_chunks; ++c) {
+    MetaArgs ac = a;
+    const int64_t e0 = c * Bc * num_packs;
+    ac.real = seq_lens + e0;
+    ac.padded = seq_lens_padded ? seq_lens_padded + e0 : nullptr;
+    ac.row0 = (int)(c * Bc);
+    ac.cu = cu_seqlens + c * a.cu_pad_to;
+    ac.cu_padded = a.cu_padded ? a.cu_padded + c * a.cu_pad_to : nullptr;
+    ac.pad_between = pad_between_seqs ? pad_between_seqs + c : nullptr;
+    ac.info = infos + c;
+    s = launch_meta(fn, ac, workspace, st);
+    if (s != PSEQ_OK) return s;
+    s = launch_gather(fn, f, Bc, S, num_packs, padding_mask, workspace, st, Bc * S, B, c);
+    if (s != PSEQ_OK) return s;
+  }
+  return PSEQ_OK;
 }

@@ -1,0 +1,181 @@
+// thd_mask_from_token_ids: padding by token value, rejecting a pad id that
+// also occurs as content.
+//
+// Follows NeMo AutoModel v0.5 "nemo_automodel.components.distributed.thd_utils",
+// thd_padding_mask_from_token_ids: a value comparison is only correct when the
+// pad id fills a right-padded tail and appears nowhere else, so exactly that
+// is validated and a colliding id is an error.
+//
+// One pass.  Each thread compares eight consecutive ids (16-byte loads) and
+// stores their eight mask bytes at once; each CTA reduces the first pad
+// position, the last non-pad position and the pad count of its part and
+// writes them to its own workspace slot.  The CTA that finishes last (an
+// acq_rel counter that wraps back to zero) folds the slots: the input is
+// valid exactly when the last content position precedes the first pad.
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "common.cuh"
+
+namespace pseq {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kGroup = 8;  // ids per thread and step
+
+struct Header {
+  unsigned int finished;
+  unsigned int pad[31];
+};
+
+struct Part {
+  long long first_pad;     // smallest pad position, or n when none
+  long long last_content;  // largest non-pad position, or -1 when none
+  long long pads;
+  long long unused;
+};
+
+size_t workspace_bytes(int64_t ctas) { return sizeof(Header) + sizeof(Part) * (size_t)ctas; }
+
+__device__ __forceinline__ unsigned inc_acq_rel(unsigned* p, unsigned limit) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(limit) : "memory");
+  return old;
+}
+
+template <typename Id, bool kVector>
+__global__ void __launch_bounds__(kThreads)
+    token_mask_kernel(const Id* __restrict__ ids, int64_t n, Id pad, uint8_t* __restrict__ mask,
+                      pseq_info* __restrict__ info, Header* hdr, Part* parts) {
+  __shared__ long long s_first[kThreads / 32], s_last[kThreads / 32], s_pads[kThreads / 32];
+  __shared__ int s_last_cta;
+  pdl_enter();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t groups = (n + kGroup - 1) / kGroup;
+  long long first_pad = n, last_content = -1, pads = 0;
+  for (int64_t g = (int64_t)blockIdx.x * kThreads + tid; g < groups; g += (int64_t)gridDim.x * kThreads) {
+    const int64_t t0 = g * kGroup;
+    Id v[kGroup];
+    if (kVector && t0 + kGroup <= n) {
+      constexpr int kVec = kGroup * sizeof(Id) / 16;
+      const int4* p = reinterpret_cast<const int4*>(ids + t0);
+      int4 q[kVec];
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) q[k] = ld_stream(p + k);
+      memcpy(v, q, sizeof(v));
+    } else {
+#pragma unroll
+      for (int k = 0; k < kGroup; ++k) v[k] = t0 + k < n ? ids[t0 + k] : pad;
+    }
+    unsigned long long bytes = 0;
+#pragma unroll
+    for (int k = 0; k < kGroup; ++k) {
+      const int64_t t = t0 + k;
+      if (t >= n) break;
+      const bool is_pad = v[k] == pad;
+      bytes |= (unsigned long long)(is_pad ? 1 : 0) << (8 * k);
+      if (is_pad) {
+        pads += 1;
+        first_pad = min(first_pad, (long long)t);
+      } else {
+        last_content = max(last_content, (long long)t);
+      }
+    }
+    if (kVector && t0 + kGroup <= n) {
+      *reinterpret_cast<unsigned long long*>(mask + t0) = bytes;
+    } else {
+      for (int k = 0; k < kGroup && t0 + k < n; ++k) mask[t0 + k] = (uint8_t)(bytes >> (8 * k));
+    }
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    first_pad = min(first_pad, __shfl_xor_sync(~0u, first_pad, d));
+    last_content = max(last_content, __shfl_xor_sync(~0u, last_content, d));
+    pads += __shfl_xor_sync(~0u, pads, d);
+  }
+  if (lane == 0) {
+    s_first[warp] = first_pad;
+    s_last[warp] = last_content;
+    s_pads[warp] = pads;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    Part p = {(long long)n, -1, 0, 0};
+    for (int w = 0; w < kThreads / 32; ++w) {
+      p.first_pad = min(p.first_pad, s_first[w]);
+      p.last_content = max(p.last_content, s_last[w]);
+      p.pads += s_pads[w];
+    }
+    parts[blockIdx.x] = p;
+    s_last_cta = inc_acq_rel(&hdr->finished, gridDim.x - 1) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last_cta || tid != 0) return;
+  long long f = n, l = -1, total = 0;
+  for (unsigned c = 0; c < gridDim.x; ++c) {
+    const Part p = parts[c];
+    f = min(f, p.first_pad);
+    l = max(l, p.last_content);
+    total += p.pads;
+  }
+  const bool ok = l < f;
+  *info = ok ? pseq_info{PSEQ_OK, (int32_t)total, 0, (int32_t)n} : pseq_info{PSEQ_ERR_VALUE, 0, 0, (int32_t)n};
+}
+
+int grid_for(int64_t n) {
+  const int64_t groups = (n + kGroup - 1) / kGroup;
+  const int64_t want = (groups + kThreads - 1) / kThreads;
+  const int64_t full = (int64_t)sm_count() * (2048 / kThreads);
+  const int64_t g = want < full ? want : full;
+  return (int)(g < 1 ? 1 : g);
+}
+
+}  // namespace
+}  // namespace pseq
+
+using namespace pseq;
+
+extern "C" size_t thd_mask_from_token_ids_workspace_size(int64_t n) {
+  if (n < 0) return 0;
+  return workspace_bytes(grid_for(n));
+}
+
+extern "C" pseq_status thd_mask_from_token_ids(const void* input_ids, int32_t id_bytes, int64_t n,
+                                               int64_t padding_token_id, uint8_t* mask, pseq_info* info,
+                                               void* workspace, size_t workspace_bytes_, pseq_stream stream) {
+  clear_error();
+  const char* fn = "thd_mask_from_token_ids";
+  if (n < 0) return fail(PSEQ_ERR_ARG, "%s: negative length", fn);
+  if (n > INT32_MAX) return fail(PSEQ_ERR_OVERFLOW, "%s: length exceeds INT32_MAX", fn);
+  if (id_bytes != 4 && id_bytes != 8) return fail(PSEQ_ERR_ARG, "%s: id_bytes must be 4 or 8", fn);
+  if (!info || (n > 0 && (!input_ids || !mask))) return fail(PSEQ_ERR_ARG, "%s: NULL pointer", fn);
+  if (!aligned(input_ids, (uintptr_t)id_bytes) || !aligned(info, 4)) return fail(PSEQ_ERR_ARG, "%s: misaligned pointer", fn);
+  if (id_bytes == 4 && (padding_token_id < INT32_MIN || padding_token_id > INT32_MAX))
+    return fail(PSEQ_ERR_ARG, "%s: padding_token_id does not fit 32-bit ids", fn);
+  const int grid = grid_for(n);
+  const size_t need = workspace_bytes(grid);
+  if (!workspace || workspace_bytes_ < need || !aligned(workspace, 16))
+    return fail(PSEQ_ERR_ARG, "%s: workspace needs %zu bytes, 16-byte aligned (got %zu)", fn, need, workspace_bytes_);
+  Header* hdr = static_cast<Header*>(workspace);
+  Part* parts = reinterpret_cast<Part*>(static_cast<unsigned char*>(workspace) + sizeof(Header));
+  const bool vec = aligned(input_ids, 16) && aligned(mask, 8);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (id_bytes == 4) {
+    const int32_t* p = static_cast<const int32_t*>(input_ids);
+    e = vec ? launch_pdl(token_mask_kernel<int32_t, true>, dim3(grid), dim3(kThreads), 0, st, p, n,
+                         (int32_t)padding_token_id, mask, info, hdr, parts)
+            : launch_pdl(token_mask_kernel<int32_t, false>, dim3(grid), dim3(kThreads), 0, st, p, n,
+                         (int32_t)padding_token_id, mask, info, hdr, parts);
+  } else {
+    const int64_t* p = static_cast<const int64_t*>(input_ids);
+    e = vec ? launch_pdl(token_mask_kernel<int64_t, true>, dim3(grid), dim3(kThreads), 0, st, p, n,
+                         (int64_t)padding_token_id, mask, info, hdr, parts)
+            : launch_pdl(token_mask_kernel<int64_t, false>, dim3(grid), dim3(kThreads), 0, st, p, n,
+                         (int64_t)padding_token_id, mask, info, hdr, parts);
+  }
+  count_launches(1);
+  if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  return check_launch(fn);
+}
