@@ -313,6 +313,108 @@ class NativeStep:
             h.copy_(d.view(self.torch.uint8)[:n], non_blocking=True)
 
 
+def time_next_rows(dev, stream, seed: int, flush_l2, reps: int = 60) -> dict:
+    """Per-call device time of the entry points beyond the step, each on a
+    workload of the same family (event-timed medians, L2 flushed before every
+    call, prebuilt ctypes arguments)."""
+    import torch
+
+    import varlen_attention_metadata_gb300 as v
+
+    lib = v.load_library()
+    P = lambda t, off=0: ctypes.c_void_p(t.data_ptr() + off)  # noqa: E731
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    keep = []
+
+    def dev_t(a):
+        t = torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        keep.append(t)
+        return t
+
+    def timed(fn, args):
+        ts = []
+        with torch.cuda.stream(stream):
+            for i in range(reps + 5):
+                flush_l2()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn(*args)
+                b.record(stream)
+                ts.append((a, b))
+        torch.cuda.synchronize(dev)
+        return statistics.median(x.elapsed_time(y) * 1e3 for x, y in ts[5:])
+
+    out = {}
+    # split_batch_into_thd_chunks: the B=8 S=8192 batch as 4 chunks of 2 rows
+    c1 = synth.thd_ids(seed)
+    B, S = c1["input_ids"].shape
+    Pk = c1["seq_lens"].shape[1]
+    fields = (v._lib.PseqField * 3)()
+    dsts = []
+    for k, (a, planes) in enumerate(((c1["input_ids"], 1), (c1["labels"], 1), (c1["position_ids"], 3))):
+        src = dev_t(a)
+        dst = torch.empty(planes * B * S, dtype=torch.int64, device=dev)
+        keep.append(dst)
+        fields[k].src, fields[k].dst, fields[k].elem_bytes, fields[k].planes, fields[k].row_elems = \
+            src.data_ptr(), dst.data_ptr(), 8, planes, 1
+    nc = 4
+    real, pad = dev_t(c1["seq_lens"]), dev_t(c1["seq_lens_padded"])
+    cu = torch.empty(nc * (B // nc * Pk + 1), dtype=torch.int32, device=dev)
+    cup = torch.empty_like(cu)
+    mask = torch.empty(B * S, dtype=torch.uint8, device=dev)
+    infos = torch.empty(nc * 4, dtype=torch.int32, device=dev)
+    pbs = torch.empty(nc, dtype=torch.uint8, device=dev)
+    ws = torch.empty(lib.thd_workspace_size(B // nc, Pk), dtype=torch.uint8, device=dev)
+    keep += [cu, cup, mask, infos, pbs, ws]
+    us = timed(lib.thd_chunks_from_batch, (P(real), P(pad), B, S, Pk, nc, -1000, 1, fields, 3, P(cu), P(cup), P(mask),
+                                           P(pbs), P(infos), P(ws), ws.numel(), sh))
+    T = int(infos.view(nc, 4)[:, 3].sum().item())
+    nbytes = 2 * T * 5 * 8 + T + 16 * B * Pk
+    out["split_batch_into_thd_chunks"] = {"workload": "B=8 S=8192 ids/labels/mRoPE, 4 chunks", "us": round(us, 2),
+                                          "bytes": nbytes, "gbs": round(nbytes / us / 1e3, 1)}
+    # thd_padding_mask_from_token_ids: a 2M-token id stream with a padded tail
+    rng = np.random.default_rng(seed)
+    n = 1 << 21
+    ids_np = rng.integers(1, 32000, size=n).astype(np.int64)
+    ids_np[n - 4096:] = 0
+    ids = dev_t(ids_np)
+    tmask = torch.empty(n, dtype=torch.uint8, device=dev)
+    tinfo = torch.empty(4, dtype=torch.int32, device=dev)
+    tws = torch.zeros(lib.thd_mask_from_token_ids_workspace_size(n), dtype=torch.uint8, device=dev)
+    keep += [tmask, tinfo, tws]
+    us = timed(lib.thd_mask_from_token_ids, (P(ids), 8, n, 0, P(tmask), P(tinfo), P(tws), tws.numel(), sh))
+    nbytes = 9 * n
+    out["thd_padding_mask_from_token_ids"] = {"workload": "int64 ids [2097152], 4096-token pad tail",
+                                              "us": round(us, 2), "bytes": nbytes, "gbs": round(nbytes / us / 1e3, 1)}
+    # first-fit-decreasing: the squeeze workload's 256 lengths at capacity 32768
+    c3 = synth.squeeze(seed)
+    lens = dev_t(c3["real_lens"])
+    offs = torch.empty(len(c3["real_lens"]) + 1, dtype=torch.int32, device=dev)
+    mem = torch.empty(len(c3["real_lens"]), dtype=torch.int32, device=dev)
+    finfo = torch.empty(4, dtype=torch.int32, device=dev)
+    keep += [offs, mem, finfo]
+    us = timed(lib.pack_ffd, (P(lens), len(c3["real_lens"]), c3["multiple"], c3["capacity"], P(offs), P(mem),
+                              P(finfo), sh))
+    out["first_fit_decreasing"] = {"workload": "256 lengths, multiple 64, capacity 32768", "us": round(us, 2),
+                                   "bytes": 8 * 256 + 4 * 513, "bound": "latency (sequential first fit)"}
+    # doc_ids -> seq_lens bridge: the stress map [64, 32768]
+    d4 = dev_t(synth.doc_map_stress(seed))
+    Bm, Sm = d4.shape
+    np_ = 8192
+    r_ = torch.empty(Bm * np_, dtype=torch.int64, device=dev)
+    p_ = torch.empty_like(r_)
+    pos = torch.empty(Bm * Sm, dtype=torch.int64, device=dev)
+    binfo = torch.empty(4, dtype=torch.int32, device=dev)
+    bws = torch.zeros(lib.pseq_doc_ids_to_lengths_workspace_size(Bm, Sm), dtype=torch.uint8, device=dev)
+    keep += [r_, p_, pos, binfo, bws]
+    us = timed(lib.pseq_doc_ids_to_lengths, (P(d4), 4, Bm, Sm, np_, -1000, P(r_), P(p_), P(pos), P(binfo), P(bws),
+                                             bws.numel(), sh))
+    nbytes = 4 * Bm * Sm + 8 * Bm * Sm + 2 * 8 * Bm * np_
+    out["doc_ids_to_seq_lens"] = {"workload": "doc_ids [64,32768] -> seq_lens [64,8192] x2 + positions [64,32768]",
+                                  "us": round(us, 2), "bytes": nbytes, "gbs": round(nbytes / us / 1e3, 1)}
+    return out
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "varlen_attention_metadata_gb300", "csrc")
@@ -554,6 +656,8 @@ def run_native(args, dist: Dist):
     torch.cuda.synchronize(dev)
     pipe_ms = dist.max(p_ev[0].elapsed_time(p_ev[1]), dev) / Ke
 
+    next_rows = time_next_rows(dev, stream, args.seed + dist.rank, flush_l2) if dist.rank == 0 else None
+
     peak, peak_kind = measured_peak()
     emb_avg_ms = statistics.mean(emb_ms)
     achieved = step.emb_bytes / (emb_avg_ms / 1e3) / 1e9
@@ -605,6 +709,7 @@ def run_native(args, dist: Dist):
                            "steps pipelined over two buffer sets (copy-in, compute, copy-out streams)",
                     "serial": {"value": round(all_tokens / (serial_ms / 1e3), 1), "ms_per_step": round(serial_ms, 4),
                                "how": "copy-in, compute, copy-out back to back on one stream"}},
+            "next_rows": next_rows,
             "gpu_launches": int(launches),
             "gpu_launches_per_step": per_step_launches,
             "clocks": clocks.summary(),

@@ -291,10 +291,11 @@ pseq_status pack_ffd(const int64_t* lens, int64_t n, int64_t multiple,
  *   run, total = sequences in all rows.
  * Device errors: PSEQ_ERR_CAPACITY when a row holds more than num_packs
  *   sequences (the slots that fit are written).
- * workspace: pseq_doc_ids_to_lengths_workspace_size(B) bytes, ZERO-FILLED
- *   before its first use; every completed call leaves its counter at zero.
+ * workspace: pseq_doc_ids_to_lengths_workspace_size(B, S) bytes, 16-byte
+ *   aligned (per-chunk scratch; no initial contents needed).  At most 65535
+ *   rows per call.
  * ---------------------------------------------------------------------- */
-size_t pseq_doc_ids_to_lengths_workspace_size(int64_t B);
+size_t pseq_doc_ids_to_lengths_workspace_size(int64_t B, int64_t S);
 pseq_status pseq_doc_ids_to_lengths(const void* doc_ids, int32_t id_bytes,
                                     int64_t B, int64_t S, int64_t num_packs,
                                     int64_t pad_value, int64_t* seq_lens,

@@ -76,7 +76,7 @@ SIGNATURES = {
     "thd_mask_from_token_ids_workspace_size": (_SZ, [_I64]),
     "thd_mask_from_token_ids": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _P, _SZ, _P]),
     "pack_ffd": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
-    "pseq_doc_ids_to_lengths_workspace_size": (_SZ, [_I64]),
+    "pseq_doc_ids_to_lengths_workspace_size": (_SZ, [_I64, _I64]),
     "pseq_doc_ids_to_lengths": (ctypes.c_int, [_P, _I32, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "pack_squeeze_workspace_size": (_SZ, [_I64, _I64]),
     "pack_squeeze": (ctypes.c_int, [_P, _I64, _I64, _I32, _P, _P, _P, _I64, _I64, _I64, _I64, _I32,

@@ -90,7 +90,7 @@ class _WorkspaceCache:
     per-call scratch.
     """
 
-    ZEROED = ("scan", "token_mask", "bridge")
+    ZEROED = ("scan", "token_mask")
 
     def __init__(self):
         self._bufs: dict = {}
@@ -522,7 +522,7 @@ def pseq_doc_ids_to_lengths(doc_ids: torch.Tensor, num_packs: int, pad_value: in
     padded = torch.empty((B, num_packs), dtype=torch.int64, device=dev)
     pos = torch.empty((B, S), dtype=torch.int64, device=dev) if with_positions else None
     info = _new_info(dev)
-    ws = _workspaces.get("bridge", lib.pseq_doc_ids_to_lengths_workspace_size(B), dev)
+    ws = _workspaces.get("bridge", lib.pseq_doc_ids_to_lengths_workspace_size(B, S), dev)
     _lib.check(lib.pseq_doc_ids_to_lengths(_p(doc_ids), doc_ids.element_size(), B, S, num_packs, pad_value, _p(real),
                                            _p(padded), _p(pos), _p(info), _p(ws), ws.numel(), _stream(dev)))
     return real, padded, pos, info

@@ -7,9 +7,9 @@
 //
 // One CTA.  Each item becomes a 64-bit key (inverted size, index) so an
 // ascending bitonic sort in shared memory yields the visiting order.  First
-// fit is inherently sequential over items, so one warp walks them in order;
-// for each item the 32 lanes test 32 bins at a time against the remaining
-// room and a ballot picks the first that fits.  Bins are numbered in the order
+// fit is inherently sequential over items, so one warp walks them in order
+// with the open bins' remaining room held in registers across its lanes: one
+// ballot per 32 bins picks the first that fits.  Bins are numbered in the order
 // they open, members keep their placement order, and a block scan of the bin
 // counts turns the placements into CSR arrays.
 #include "common.cuh"
@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
   // keys: (INT32_MAX - size) in the high word sorts sizes descending, the
   // index in the low word breaks ties toward the smaller index
+  long long my_total = 0;
   for (int i = tid; i < pow2; i += kThreads) {
     unsigned long long k = ~0ull;  // padding sorts last
     if (i < n) {
@@ -54,13 +55,16 @@ __global__ void __launch_bounds__(kThreads)
       } else {
         size = (real + multiple - 1) / multiple * multiple;
         if (size > capacity) s_big = 1;
-        atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), (unsigned long long)size);
+        my_total += size;
       }
       if (size > INT32_MAX) size = INT32_MAX;
       k = ((unsigned long long)(INT32_MAX - size) << 32) | (unsigned)i;
     }
     key[i] = k;
   }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) my_total += __shfl_xor_sync(~0u, my_total, d);
+  if ((tid & 31) == 0 && my_total) atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), (unsigned long long)my_total);
   __syncthreads();
   for (int width = 2; width <= pow2; width <<= 1) {
     for (int stride = width >> 1; stride > 0; stride >>= 1) {
@@ -82,35 +86,127 @@ __global__ void __launch_bounds__(kThreads)
     if (tid == 0) *info = {s_bad ? PSEQ_ERR_VALUE : PSEQ_ERR_CAPACITY, 0, 0, 0};
     return;
   }
-  // first fit, one warp, items in visiting order
+  // sizes in visiting order, as int32 (room and count arrays are free yet)
+  for (int k = tid; k < n; k += kThreads) bin_of[k] = INT32_MAX - (int)(key[k] >> 32);
+  __syncthreads();
+  // first fit, one warp, items in visiting order.  The remaining room and
+  // member count of bin b live in register b / 32 of lane b % 32 for the first
+  // kRegBins * 32 bins (one ballot per 32 bins finds the first that fits), in
+  // shared memory beyond that.
   if (tid < 32) {
+    constexpr int kRegBins = 8;
     const int lane = tid;
-    int bins = 0;
-    for (int k = 0; k < n; ++k) {
-      const long long size = INT32_MAX - (long long)(key[k] >> 32);
-      int chosen = -1;
-      for (int base = 0; base < bins && chosen < 0; base += 32) {
-        const int b = base + lane;
-        const unsigned fits = __ballot_sync(~0u, b < bins && room[b] >= size);
-        if (fits) chosen = base + __ffs(fits) - 1;
-      }
-      if (chosen < 0) {
-        chosen = bins;
-        if (lane == 0) {
-          room[chosen] = (int32_t)capacity;
-          count[chosen] = 0;
-        }
-        bins += 1;
-      }
-      __syncwarp();
-      if (lane == 0) {
-        room[chosen] -= (int32_t)size;
-        bin_of[k] = chosen;
-        slot_of[k] = count[chosen];
-        count[chosen] += 1;
-      }
-      __syncwarp();
+    int room_r[kRegBins], count_r[kRegBins];
+#pragma unroll
+    for (int r = 0; r < kRegBins; ++r) {
+      room_r[r] = 0;
+      count_r[r] = 0;
     }
+    int bins = 0;
+    int next = n > 0 ? bin_of[0] : 0;
+    int k = 0;
+    // while at most 32 bins are open: one register per lane, one ballot per item
+    {
+      int room = 0, cnt = 0;
+      for (; k < n; ++k) {
+        const int size = next;
+        const unsigned fits = __ballot_sync(~0u, lane < bins && room >= size);
+        int chosen;
+        if (fits) {
+          chosen = __ffs(fits) - 1;
+        } else {
+          if (bins == 32) break;  // a 33rd bin: continue on the general path below
+          chosen = bins++;
+          if (lane == chosen) {
+            room = (int)capacity;
+            cnt = 0;
+          }
+        }
+        if (k + 1 < n) next = bin_of[k + 1];
+        int mine = 0;
+        if (lane == chosen) {
+          room -= size;
+          mine = cnt++;
+        }
+        const int slot = __shfl_sync(~0u, mine, chosen);
+        if (lane == 0) {
+          slot_of[k] = slot;
+          bin_of[k] = chosen;  // its size was read already; the look-ahead reads k + 1
+        }
+      }
+      room_r[0] = room;
+      count_r[0] = cnt;
+    }
+    for (; k < n; ++k) {
+      const int size = next;
+      if (k + 1 < n) next = bin_of[k + 1];
+      const int groups = (min(bins, kRegBins * 32) + 31) >> 5;
+      int chosen = -1;
+#pragma unroll
+      for (int r = 0; r < kRegBins; ++r) {
+        if (r < groups && chosen < 0) {
+          const unsigned fits = __ballot_sync(~0u, r * 32 + lane < bins && room_r[r] >= size);
+          if (fits) chosen = r * 32 + __ffs(fits) - 1;
+        }
+      }
+      int slot = 0;
+      if (chosen < 0 && bins > kRegBins * 32) {  // bins that live in shared memory
+        for (int base = kRegBins * 32; chosen < 0 && base < bins; base += 32) {
+          const unsigned fits = __ballot_sync(~0u, base + lane < bins && room[base + lane] >= size);
+          if (fits) chosen = base + __ffs(fits) - 1;
+        }
+        if (chosen >= 0) {
+          __syncwarp();
+          if (lane == 0) {
+            room[chosen] -= size;
+            slot = count[chosen];
+            count[chosen] += 1;
+          }
+          slot = __shfl_sync(~0u, slot, 0);
+          __syncwarp();
+        }
+      }
+      if (chosen < 0) {  // open a new bin
+        chosen = bins;
+        bins += 1;
+        if (chosen >= kRegBins * 32) {
+          if (lane == 0) {
+            room[chosen] = (int32_t)capacity - size;
+            count[chosen] = 1;
+          }
+          __syncwarp();
+        } else {
+#pragma unroll
+          for (int r = 0; r < kRegBins; ++r)
+            if (chosen == r * 32 + lane) {
+              room_r[r] = (int)capacity;
+              count_r[r] = 0;
+            }
+        }
+      }
+      if (chosen < kRegBins * 32) {
+        int mine = 0;
+#pragma unroll
+        for (int r = 0; r < kRegBins; ++r)
+          if (chosen == r * 32 + lane) {
+            room_r[r] -= size;
+            mine = count_r[r];
+            count_r[r] += 1;
+          }
+        slot = __shfl_sync(~0u, mine, chosen & 31);
+      }
+      if (lane == 0) {
+        slot_of[k] = slot;
+        bin_of[k] = chosen;  // its size was read already; the look-ahead reads k + 1
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < kRegBins; ++r)
+      if (r * 32 + lane < bins) {
+        room[r * 32 + lane] = room_r[r];
+        count[r * 32 + lane] = count_r[r];
+      }
     if (lane == 0) s_bins = bins;
   }
   __syncthreads();

@@ -12,10 +12,6 @@
 // writes them to its own workspace slot.  The CTA that finishes last (an
 // acq_rel counter that wraps back to zero) folds the slots: the input is
 // valid exactly when the last content position precedes the first pad.
-#include <map>
-#include <mutex>
-#include <tuple>
-
 #include "common.cuh"
 
 namespace pseq {
@@ -111,13 +107,33 @@ __global__ void __launch_bounds__(kThreads)
     s_last_cta = inc_acq_rel(&hdr->finished, gridDim.x - 1) == gridDim.x - 1;
   }
   __syncthreads();
-  if (!s_last_cta || tid != 0) return;
+  if (!s_last_cta) return;
+  // fold every CTA's part with the whole block
   long long f = n, l = -1, total = 0;
-  for (unsigned c = 0; c < gridDim.x; ++c) {
-    const Part p = parts[c];
-    f = min(f, p.first_pad);
-    l = max(l, p.last_content);
-    total += p.pads;
+  for (unsigned c = tid; c < gridDim.x; c += kThreads) {
+    // L2 loads: the parts were released by the counter that thread 0 acquired
+    f = min(f, __ldcg(&parts[c].first_pad));
+    l = max(l, __ldcg(&parts[c].last_content));
+    total += __ldcg(&parts[c].pads);
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) {
+    f = min(f, __shfl_xor_sync(~0u, f, d));
+    l = max(l, __shfl_xor_sync(~0u, l, d));
+    total += __shfl_xor_sync(~0u, total, d);
+  }
+  __syncthreads();
+  if (lane == 0) {
+    s_first[warp] = f;
+    s_last[warp] = l;
+    s_pads[warp] = total;
+  }
+  __syncthreads();
+  if (tid != 0) return;
+  for (int w = 1; w < kThreads / 32; ++w) {
+    f = min(f, s_first[w]);
+    l = max(l, s_last[w]);
+    total += s_pads[w];
   }
   const bool ok = l < f;
   *info = ok ? pseq_info{PSEQ_OK, (int32_t)total, 0, (int32_t)n} : pseq_info{PSEQ_ERR_VALUE, 0, 0, (int32_t)n};
