@@ -312,6 +312,30 @@ def test_thd_ids_workload(seed):
     check_thd(synth.thd_ids(seed))
 
 
+@pytest.mark.parametrize("H", [128, 200, 2048])
+def test_thd_wide_rows_bulk_copy(H):
+    """Rows of >= 256 bytes at 16-byte alignment go through the bulk-copy
+    engine; check them on ragged layouts, with and without the mask, and as
+    chunks of a split batch."""
+    rng = np.random.default_rng(H)
+    B, S, P = 3, 1500, 20
+    real, padded = synth.random_thd(rng, B, S, P, multiple=8, interleave_filler=True)
+    batch = {"input_ids": np.zeros((B, S), np.int64), "seq_lens": real, "seq_lens_padded": padded}
+    v = V()
+    hidden = torch.randn(B, S, H, device=DEV).to(torch.bfloat16)
+    r = v.thd_from_batch(dev(real), dev(padded), S, [(hidden, 1)])
+    st, n, mx, T = info_of(r["info"])
+    meta = oracle.thd_meta(real, padded, S)
+    assert st == 0 and T == meta["total_tokens"]
+    want = oracle.thd_gather(hidden.cpu().view(torch.int16).numpy(), meta, B, S)
+    got = r["dst"][0][0][: T * H].view(torch.int16).cpu().numpy().reshape(T, H)
+    np.testing.assert_array_equal(got, want)
+    np.testing.assert_array_equal(r["padding_mask"][:T].cpu().numpy(),
+                                  oracle.thd_padding_mask(T, meta["seq_real"], meta["seq_padded"]))
+    r2 = v.thd_from_batch(dev(real), dev(padded), S, [(hidden, 1)], want_mask=False)
+    np.testing.assert_array_equal(r2["dst"][0][0][: T * H].view(torch.int16).cpu().numpy().reshape(T, H), want)
+
+
 def test_thd_embeddings_workload():
     c = synth.thd_embeddings(0)
     hidden = c["hidden"].to(DEV)

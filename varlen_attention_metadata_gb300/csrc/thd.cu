@@ -212,6 +212,7 @@ struct Fields {
   int planes[PSEQ_MAX_FIELDS];
   int num;
   int narrow;  // every row of every field is one aligned access of <= 16 bytes
+  int bulk;    // every row of every field is >= 256 bytes, a multiple of 16, 16-byte aligned
   int njobs;   // (field, plane) pairs, for the row-by-row path
   unsigned char job_field[kMaxJobs];
   unsigned char job_plane[kMaxJobs];
@@ -286,17 +287,35 @@ __device__ __forceinline__ void slice_of(int64_t Tm, int64_t& r0, int64_t& r1) {
 // ----------------------------------------------------------------------------
 // kernels
 // ----------------------------------------------------------------------------
-__global__ void __launch_bounds__(kRowThreads, 2)
-    thd_fused_kernel(const __grid_constant__ MetaArgs a, const __grid_constant__ Fields f, uint8_t* mask,
-                     int64_t mask_cap) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ Triple scratch[kRowThreads / 32];
-  __shared__ ScanFlags fl;
-  pdl_enter();
-  // chunk blockIdx.y: rows [c*B, (c+1)*B) of a batch of chunks*B rows
-  const int c = blockIdx.y;
+// Shared-memory tables of one chunk's layout (see fused_scan).
+struct Tables {
+  int64_t* row;  // [B]
+  int32_t* cup;  // [E+1]
+  int32_t* src;  // [E]
+  int32_t* real; // [E]
+};
+
+__device__ __forceinline__ Tables carve_tables(unsigned char* base, int B, int P) {
+  const int E = B * P;
+  Tables t;
+  t.row = reinterpret_cast<int64_t*>(base);
+  t.cup = reinterpret_cast<int32_t*>(t.row + (P > 0 ? B : 0));
+  t.src = t.cup + E + 1;
+  t.real = t.src + E;
+  return t;
+}
+
+size_t table_bytes(int B, int P) {
+  const size_t E = (size_t)B * P;
+  return round_up((P > 0 ? 8 * (size_t)B : 0) + 4 * (E + 1) + 8 * E, 16);
+}
+
+// The per-chunk view of the arguments: chunk blockIdx.y covers rows
+// [c*B, (c+1)*B) of a batch of chunks*B rows.
+__device__ __forceinline__ MetaArgs chunk_view(const MetaArgs& a) {
   MetaArgs ac = a;
   if (a.chunks > 1) {
+    const int c = blockIdx.y;
     const int64_t e0 = (int64_t)c * a.B * a.P;
     ac.real = a.real + e0;
     ac.padded = a.padded ? a.padded + e0 : nullptr;
@@ -306,36 +325,184 @@ __global__ void __launch_bounds__(kRowThreads, 2)
     ac.pad_between = a.pad_between ? a.pad_between + c : nullptr;
     ac.info = a.info + c;
   }
-  const int E = ac.B * ac.P;
-  int64_t* s_row = reinterpret_cast<int64_t*>(smem);
-  int32_t* s_cup = reinterpret_cast<int32_t*>(s_row + (ac.P > 0 ? ac.B : 0));
-  int32_t* s_src = s_cup + E + 1;
-  int32_t* s_real = s_src + E;
+  return ac;
+}
+
+// Every CTA scans its chunk's whole length table into shared memory; CTA 0
+// of the chunk also writes cu_seqlens, cu_seqlens_padded, pad_between_seqs
+// and the info block.  Returns the summary (the same in every thread).
+__device__ __forceinline__ Summary fused_scan(const MetaArgs& ac, const Tables& t, Triple* scratch, ScanFlags* fl,
+                                              int& n) {
   const bool lead = blockIdx.x == 0;
   auto put = [&](int k, int b, long long o, long long real, long long padded, long long R, long long Pd) {
-    s_cup[k] = (int32_t)Pd;
-    s_src[k] = (int32_t)((ac.row0 + b) * ac.S + o);
-    s_real[k] = (int32_t)real;
+    t.cup[k] = (int32_t)Pd;
+    t.src[k] = (int32_t)((ac.row0 + b) * ac.S + o);
+    t.real[k] = (int32_t)real;
     if (lead) {
       if (ac.cu) ac.cu[k] = (int32_t)R;
       if (ac.cu_padded) ac.cu_padded[k] = (int32_t)Pd;
     }
   };
-  const ScanResult r = scan_lengths<kRowThreads>(ac, s_row, scratch, &fl, put);
-  const Summary s = summarize(ac, r, fl, r.n ? s_real[r.n - 1] : 0);
+  const ScanResult r = scan_lengths<kRowThreads>(ac, t.row, scratch, fl, put);
+  const Summary s = summarize(ac, r, *fl, r.n ? t.real[r.n - 1] : 0);
   if (threadIdx.x == 0) {
-    s_cup[r.n] = (int32_t)s.T;
+    t.cup[r.n] = (int32_t)s.T;
     if (lead) write_meta(ac, s);
   }
   __syncthreads();
+  n = r.n;
+  return s;
+}
+
+__global__ void __launch_bounds__(kRowThreads, 2)
+    thd_fused_kernel(const __grid_constant__ MetaArgs a, const __grid_constant__ Fields f, uint8_t* mask,
+                     int64_t mask_cap) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ Triple scratch[kRowThreads / 32];
+  __shared__ ScanFlags fl;
+  pdl_enter();
+  const int c = blockIdx.y;
+  const MetaArgs ac = chunk_view(a);
+  const Tables t = carve_tables(smem, ac.B, ac.P);
+  int n;
+  const Summary s = fused_scan(ac, t, scratch, &fl, n);
   if (s.status != PSEQ_OK) return;
   const int64_t T = s.T, Tm = s.shown_total;
   if (Tm > mask_cap || T > Tm || T > (int64_t)ac.B * ac.S) return;  // cannot happen for well-formed input
   int64_t r0, r1;
   slice_of(Tm, r0, r1);
   uint8_t* m = mask ? mask + (int64_t)c * Tm : nullptr;
-  gather_rows(f, (int64_t)ac.B * a.chunks, ac.S, T, m, r0, min(r1, T), s_cup, s_src, s_real, r.n, c);
+  gather_rows(f, (int64_t)ac.B * a.chunks, ac.S, T, m, r0, min(r1, T), t.cup, t.src, t.real, n, c);
   if (m) {
+    const int64_t tail = max(r0, T);
+    if (tail < r1) block_fill_bytes(m + tail, r1 - tail, 1);
+  }
+}
+
+// Wide rows through the bulk-copy engine: after the table scan, one thread
+// streams the CTA's slice global -> shared -> global through a ring of
+// kStages buffers of kStage bytes (each load tracked by an mbarrier, each
+// store by a bulk group), so the copy needs almost no registers or threads
+// while the other threads write the mask.  Every row of every field is a
+// multiple of 16 bytes at 16-byte aligned addresses (checked on the host).
+#ifndef PSEQ_BULK_STAGES
+#define PSEQ_BULK_STAGES 4
+#endif
+#ifndef PSEQ_BULK_STAGE_KB
+#define PSEQ_BULK_STAGE_KB 32
+#endif
+constexpr int kStages = PSEQ_BULK_STAGES;
+constexpr int kStage = PSEQ_BULK_STAGE_KB * 1024;
+
+__global__ void __launch_bounds__(kRowThreads, 1)
+    thd_fused_bulk_kernel(const __grid_constant__ MetaArgs a, const __grid_constant__ Fields f, uint8_t* mask,
+                          int64_t mask_cap, int64_t wait_ns) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ Triple scratch[kRowThreads / 32];
+  __shared__ ScanFlags fl;
+  __shared__ __align__(8) uint64_t bar[kStages];
+  pdl_enter();
+  const int c = blockIdx.y;
+  const MetaArgs ac = chunk_view(a);
+  unsigned char* ring = smem;
+  const Tables t = carve_tables(smem + (size_t)kStages * kStage, ac.B, ac.P);
+  int n;
+  const Summary s = fused_scan(ac, t, scratch, &fl, n);
+  if (s.status != PSEQ_OK) return;
+  const int64_t T = s.T, Tm = s.shown_total;
+  if (Tm > mask_cap || T > Tm || T > (int64_t)ac.B * ac.S) return;  // cannot happen for well-formed input
+  int64_t r0, r1;
+  slice_of(Tm, r0, r1);
+  const int64_t lo = r0, hi = min(r1, T);
+  uint8_t* m = mask ? mask + (int64_t)c * Tm : nullptr;
+  if (threadIdx.x == 0 && lo < hi) {
+    const int64_t plane_in = (int64_t)ac.B * a.chunks * ac.S;
+    // the slice's chunks: sequence pieces x fields x planes, cut at kStage bytes
+    int j = seq_of(t.cup, n, lo), i = 0, p = 0;
+    int64_t off = 0;
+    auto next = [&](const unsigned char*& src, unsigned char*& dst, uint32_t& bytes) -> bool {
+      while (j < n) {
+        const int64_t cs = t.cup[j];
+        if (cs >= hi) return false;
+        const int64_t a0 = max(lo, cs), a1 = min(hi, (int64_t)t.cup[j + 1]);
+        while (a0 < a1 && i < f.num) {
+          const int64_t rb = f.row_bytes[i];
+          const int64_t piece = (a1 - a0) * rb;
+          if (p < f.planes[i]) {
+            if (off < piece) {
+              const int64_t tok = (int64_t)t.src[j] + (a0 - cs);
+              src = f.src[i] + ((int64_t)p * plane_in + tok) * rb + off;
+              dst = f.dst[i] + (((int64_t)c * f.planes[i] + p) * T + a0) * rb + off;
+              bytes = (uint32_t)min(piece - off, (int64_t)kStage);
+              off += bytes;
+              return true;
+            }
+            off = 0;
+            ++p;
+            continue;
+          }
+          p = 0;
+          ++i;
+        }
+        i = 0;
+        p = 0;
+        off = 0;
+        ++j;
+      }
+      return false;
+    };
+    for (int k = 0; k < kStages; ++k) mbar_init(&bar[k], 1);
+    fence_mbar_init();
+    unsigned char* dst_of[kStages];
+    uint32_t bytes_of[kStages];
+    const unsigned char* src;
+    unsigned char* dst;
+    uint32_t bytes;
+    int loaded = 0;
+    for (int k = 0; k < kStages && next(src, dst, bytes); ++k, ++loaded) {
+      mbar_expect_tx(&bar[k], bytes);
+      bulk_load(ring + (size_t)k * kStage, src, bytes, &bar[k]);
+      dst_of[k] = dst;
+      bytes_of[k] = bytes;
+    }
+    bool failed = false;
+    for (int q = 0; q < loaded; ++q) {
+      const int k = q % kStages;
+      if (!mbar_wait(&bar[k], (uint32_t)((q / kStages) & 1), wait_ns)) {
+        failed = true;
+        break;
+      }
+      bulk_store(dst_of[k], ring + (size_t)k * kStage, bytes_of[k]);
+      bulk_commit();
+      // refill the buffer of chunk q - 1 once its store has read it
+      if (q >= 1 && next(src, dst, bytes)) {
+        const int k1 = (q - 1) % kStages;
+        bulk_wait_read<1>();
+        mbar_expect_tx(&bar[k1], bytes);
+        bulk_load(ring + (size_t)k1 * kStage, src, bytes, &bar[k1]);
+        dst_of[k1] = dst;
+        bytes_of[k1] = bytes;
+        ++loaded;
+      }
+    }
+    if (failed) {
+      // a load never arrived: report, then give the loads in flight a bounded
+      // chance to land before the shared memory goes away
+      atomicMax(&ac.info->status, (int)PSEQ_ERR_TIMEOUT);
+      for (int q = 0; q < loaded; ++q) mbar_wait(&bar[q % kStages], (uint32_t)((q / kStages) & 1), wait_ns);
+    }
+    bulk_wait<0>();
+  } else if (m && threadIdx.x > 0) {
+    const int nt = blockDim.x - 1, tid = threadIdx.x - 1;
+    for (int j = seq_of(t.cup, n, lo); j < n && t.cup[j] < hi; ++j) {
+      const int64_t cs = t.cup[j];
+      const int64_t a0 = max(lo, cs), a1 = min(hi, (int64_t)t.cup[j + 1]);
+      const int64_t real_end = cs + t.real[j];
+      for (int64_t x = a0 + tid; x < a1; x += nt) m[x] = x >= real_end ? 1 : 0;
+    }
+  }
+  if (m) {
+    __syncthreads();
     const int64_t tail = max(r0, T);
     if (tail < r1) block_fill_bytes(m + tail, r1 - tail, 1);
   }
@@ -507,21 +674,38 @@ pseq_status build_fields(const char* fn, const pseq_field* fields, int num_field
   }
   if (jobs > kMaxJobs) f.narrow = 0;
   f.njobs = f.narrow ? jobs : 0;
+  f.bulk = num_fields > 0;
+  for (int i = 0; i < num_fields; ++i) {
+    const int64_t rb = f.row_bytes[i];
+    if (rb < 256 || rb % 16 != 0 || !aligned(f.src[i], 16) || !aligned(f.dst[i], 16)) f.bulk = 0;
+  }
   return PSEQ_OK;
 }
 
-size_t fused_smem(const MetaArgs& a) {
-  const size_t E = (size_t)a.B * a.P;
-  return round_up((a.P > 0 ? 8 * (size_t)a.B : 0) + 4 * (E + 1) + 8 * E, 16);
-}
 
 pseq_status launch_fused(const char* fn, const MetaArgs& a, const Fields& f, uint8_t* mask, int64_t mask_cap,
                          cudaStream_t st) {
-  const size_t smem = fused_smem(a);
   const int64_t rows = a.fixed_total >= 0 ? a.fixed_total : (int64_t)a.B * a.S;
-  const int grid = row_grid(reinterpret_cast<const void*>(thd_fused_kernel), smem, rows, f);
-  const cudaError_t e = launch_pdl(thd_fused_kernel, dim3(grid, (unsigned)a.chunks), dim3(kRowThreads), smem, st, a,
-                                   f, mask, mask_cap);
+  cudaError_t e;
+  if (f.bulk) {
+    // one CTA per SM; the ring of bulk-copy buffers sits in front of the tables
+    const size_t smem = (size_t)kStages * kStage + table_bytes(a.B, a.P);
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+      e = cudaFuncSetAttribute(thd_fused_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)((size_t)kStages * kStage + table_bytes(kFusedMaxEntries, 1)));
+      if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+      attr_set[dev] = true;
+    }
+    e = launch_pdl(thd_fused_bulk_kernel, dim3((unsigned)sm_count(), (unsigned)a.chunks), dim3(kRowThreads), smem, st,
+                   a, f, mask, mask_cap, wait_limit_ns());
+  } else {
+    const size_t smem = table_bytes(a.B, a.P);
+    const int grid = row_grid(reinterpret_cast<const void*>(thd_fused_kernel), smem, rows, f);
+    e = launch_pdl(thd_fused_kernel, dim3(grid, (unsigned)a.chunks), dim3(kRowThreads), smem, st, a, f, mask, mask_cap);
+  }
   count_launches(1);
   if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
   return check_launch(fn);
