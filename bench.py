@@ -458,9 +458,9 @@ def measured_peak():
 
 
 def profiled_traffic():
-    """DRAM bytes per launch of the gather from the committed ncu summary,
-    or None when the kernels changed since that capture."""
-    path = os.path.join(ROOT, "profiles", "thd_gather_embeddings.md")
+    """DRAM bytes per launch of the embedding conversion from the committed
+    ncu summary, or None when the kernels changed since that capture."""
+    path = os.path.join(ROOT, "profiles", "thd_fused_bulk_embeddings.md")
     try:
         with open(path) as f:
             text = f.read()
@@ -731,7 +731,7 @@ def run_native(args, dist: Dist):
                 "ms_per_step_one_stream": round(one_stream_ms, 6),
             },
             "roofline": {
-                "kernel": "thd_fused_kernel via thd_from_batch (bf16 hidden [4,8192,4096] -> [T,4096], cu arrays, mask)",
+                "kernel": "thd_fused_bulk_kernel via thd_from_batch (bf16 hidden [4,8192,4096] -> [T,4096], cu arrays, mask)",
                 "bound": "hbm",
                 "achieved": round(achieved, 1),
                 "peak": peak,
