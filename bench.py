@@ -27,6 +27,7 @@ import ctypes
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -131,7 +132,7 @@ class NativeStep:
     the pinned host copy of every input for the end-to-end leg.
     """
 
-    def __init__(self, host: dict, device, stream, host_pinned=None, side_stream=None):
+    def __init__(self, host: dict, device, stream, host_pinned=None, side_stream=None, only=None):
         import torch
 
         import varlen_attention_metadata_gb300 as v
@@ -156,6 +157,7 @@ class NativeStep:
         self._keep = []
         self._fork = self.torch.cuda.Event()
         self._join = self.torch.cuda.Event()
+        self.only = set(only) if only else None
         self._build()
 
     def _in(self, key, a):
@@ -252,18 +254,30 @@ class NativeStep:
         self.tokens[name] = nb * width
         self._finish[name] = lambda: (info, cu, cup, mask, out, M + nb)
 
+    def _want(self, name):
+        return name in self.host and (self.only is None or name in self.only)
+
     def _build(self):
         h = self.host
-        self._map("map_small", h["map_small"])
-        t0 = h["thd_small"]
-        self._thd("thd_small", t0, [("input_ids", t0["input_ids"], 1), ("labels", t0["labels"], 1),
-                                    ("position_ids", t0["position_ids"], 1)])
-        t1 = h["thd_ids"]
-        self._thd("thd_ids", t1, [("input_ids", t1["input_ids"], 1), ("labels", t1["labels"], 1),
-                                  ("position_ids", t1["position_ids"], 3)])
-        self._thd("thd_emb", h["thd_emb"], [], hidden=h["thd_emb"]["hidden"])
-        self._squeeze("squeeze", h["squeeze"])
-        self._map("map_stress", h["map_stress"])
+        if self._want("map_small"):
+            self._map("map_small", h["map_small"])
+        if self._want("thd_small"):
+            t0 = h["thd_small"]
+            self._thd("thd_small", t0, [("input_ids", t0["input_ids"], 1), ("labels", t0["labels"], 1),
+                                        ("position_ids", t0["position_ids"], 1)])
+        if self._want("thd_ids"):
+            t1 = h["thd_ids"]
+            self._thd("thd_ids", t1, [("input_ids", t1["input_ids"], 1), ("labels", t1["labels"], 1),
+                                      ("position_ids", t1["position_ids"], 3)])
+        if self._want("thd_emb"):
+            self._thd("thd_emb", h["thd_emb"], [], hidden=h["thd_emb"]["hidden"])
+        if self._want("squeeze"):
+            self._squeeze("squeeze", h["squeeze"])
+        if self._want("map_stress"):
+            self._map("map_stress", h["map_stress"])
+        # a larger squeeze, timed on its own only (never part of the step)
+        if self.only is not None and self._want("squeeze_scaled"):
+            self._squeeze("squeeze_scaled", h["squeeze_scaled"])
         self.torch.cuda.synchronize(self.dev)
 
     def run(self, emb_events=None, two_streams=False):
@@ -319,10 +333,10 @@ class NativeStep:
             else:
                 _, cu, cup, mask, out, ncu = res
                 self.outputs += [(cu, 4 * ncu), (cup, 4 * ncu), (mask, mask.numel()), (out, out.numel() * 8)]
-                c = self.host["squeeze"]
+                c = self.host[name]
                 real_bytes = 8 * int(c["real_lens"].sum())
                 self.alg_bytes[name] = real_bytes + out.numel() * 8 + mask.numel() + 8 * ncu
-        self.emb_bytes = self.alg_bytes["thd_emb"]
+        self.emb_bytes = self.alg_bytes.get("thd_emb")
         self.h2d_bytes = sum(h.numel() * h.element_size() for _, h in self.inputs)
         self.d2h_bytes = sum(n for _, n in self.outputs)
         self.host_out = [torch.empty(n, dtype=torch.uint8, pin_memory=True) for _, n in self.outputs]
@@ -697,12 +711,18 @@ def run_native(args, dist: Dist):
     next_rows = time_next_rows(dev, stream, args.seed + dist.rank, flush_l2) if dist.rank == 0 else None
 
     peak, peak_kind = measured_peak()
+    per_config = None
+    if dist.rank == 0:
+        host["squeeze_scaled"] = synth.squeeze(args.seed, N=16384)
+        per_config = time_per_config(step, host, dev, stream, flush_l2, peak)
     emb_avg_ms = statistics.mean(emb_ms)
     achieved = step.emb_bytes / (emb_avg_ms / 1e3) / 1e9
     traffic = profiled_traffic()
     cpu = None
     if dist.rank == 0:
         cpu = cpu_baseline(host, budget_s=10.0)
+        cpu.update(cpu_description())
+        cpu["per_config_full_size"] = oracle_per_config(host)
     dist.barrier()
     if dist.rank == 0:
         line = {
@@ -738,6 +758,7 @@ def run_native(args, dist: Dist):
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
                 "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
+                "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                 "traffic": traffic,
                 "algorithmic_bytes_per_launch": step.emb_bytes,
                 "avg_launch_us": round(emb_avg_ms * 1e3, 3),
@@ -751,6 +772,7 @@ def run_native(args, dist: Dist):
                     "serial": {"value": round(all_tokens / (serial_ms / 1e3), 1), "ms_per_step": round(serial_ms, 4),
                                "how": "copy-in, compute, copy-out back to back on one stream"}},
             "next_rows": next_rows,
+            "per_config": per_config,
             "gpu_launches": int(launches),
             "gpu_launches_per_step": per_step_launches,
             "clocks": clocks.summary(),
@@ -758,6 +780,172 @@ def run_native(args, dist: Dist):
         }
         print(json.dumps(line), flush=True)
     dist.close()
+
+
+NOMINAL_HBM_GBS = 8000.0  # the nominal GB300 HBM3e figure (~8 TB/s)
+
+PER_CONFIG = (
+    ("map_small", "C0 doc_ids int32 [4,2048] -> cu_seqlens, max_seqlen"),
+    ("thd_small", "C0 THD of int64 input_ids/labels/position_ids [4,2048]"),
+    ("thd_ids", "C1 THD B=8 S=8192, 64 packs: int64 input_ids, labels, mRoPE [3,8,8192]"),
+    ("thd_emb", "C2 THD of bf16 hidden [4,8192,4096]"),
+    ("squeeze", "C3 squeeze int64 [256,4096] -> FFD bins x 32768, stretched"),
+    ("map_stress", "C4 doc_ids int32 [64,32768], ~250k segments"),
+    ("squeeze_scaled", "scaled squeeze (labelled extra, not a config): int64 [16384,4096] -> FFD bins x 32768"),
+)
+ROTATE_MAX_SETS = 4096
+
+
+def _graph_us(calls, dev, stream, flush_l2, replays=10):
+    """Mean device time of one replay of a CUDA graph holding ``calls`` in
+    order (L2 flushed before every replay)."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for fn, args in calls:
+            st = fn(*args)
+            if st != 0:
+                raise RuntimeError(f"status {st} during graph capture")
+    ev = []
+    with torch.cuda.stream(stream):
+        for i in range(3 + replays):
+            flush_l2()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            if i >= 3:
+                ev.append((a, b))
+    torch.cuda.synchronize(dev)
+    us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in ev)
+    del g
+    return us
+
+
+def time_per_config(step, host, dev, stream, flush_l2, peak, warm=20, reps=200) -> dict:
+    """Per ABI call of every configuration, three ways:
+
+    - ``cold_us``: median of ``reps`` event-timed calls after ``warm`` warm-up
+      calls, L2 flushed before every call (the state a training step sees);
+    - ``graph_us``: back-to-back calls on one buffer set, captured in one CUDA
+      graph (launch gaps removed; small inputs then sit in L2);
+    - ``rotated``: one graph of calls over k independent buffer sets holding
+      together at least 4x L2 of algorithmic bytes (k capped at 4096), so that
+      HBM, not L2, serves them.
+    """
+    import torch
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    out = {}
+    for name, label in PER_CONFIG:
+        if name not in host:
+            continue
+        if name in step.alg_bytes:
+            base = step
+        else:
+            base = NativeStep(host, dev, stream, host_pinned=step.pinned, only=(name,))
+            with torch.cuda.stream(stream):
+                base.run()
+            base.resolve()
+        fn, args = next((f, a) for n, f, a in base.calls if n == name)
+        nbytes = base.alg_bytes[name]
+        tokens = base.tokens[name]
+        ts = []
+        with torch.cuda.stream(stream):
+            for i in range(warm + reps):
+                flush_l2()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn(*args)
+                b.record(stream)
+                if i >= warm:
+                    ts.append((a, b))
+        torch.cuda.synchronize(dev)
+        cold = statistics.median(a.elapsed_time(b) * 1e3 for a, b in ts)
+        G = 200 if nbytes < (64 << 20) else 20
+        graph = _graph_us([(fn, args)] * G, dev, stream, flush_l2) / G
+        k = int(min(ROTATE_MAX_SETS, max(1, -(-4 * l2 // nbytes))))
+        sets = [base] + [NativeStep(host, dev, stream, host_pinned=step.pinned, only=(name,)) for _ in range(k - 1)]
+        calls = [next((f, a) for n, f, a in s.calls if n == name) for s in sets]
+        rot = _graph_us(calls, dev, stream, flush_l2, replays=5) / k
+        del sets, calls
+        torch.cuda.empty_cache()
+        gbs = nbytes / rot / 1e3
+        out[name] = {
+            "what": label,
+            "algorithmic_bytes": int(nbytes),
+            "tokens": int(tokens),
+            "cold_us": round(cold, 2),
+            "cold_gbs": round(nbytes / cold / 1e3, 1),
+            "cold_tokens_per_s": round(tokens / cold * 1e6, 1),
+            "graph_us": round(graph, 2),
+            "rotated": {"sets": k, "set_bytes_over_l2": round(k * nbytes / l2, 2), "us_per_call": round(rot, 2),
+                        "gbs": round(gbs, 1), "frac_of_measured": round(gbs / peak, 4),
+                        "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4)},
+        }
+        if base is not step:
+            del base
+            torch.cuda.empty_cache()
+    return out
+
+
+def cpu_description() -> dict:
+    model = None
+    try:
+        res = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in res.stdout.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        model = platform.processor() or platform.machine()
+    return {"cpu_model": model, "os_cpu_count": os.cpu_count(), "cores_used": 1}
+
+
+def oracle_per_config(host: dict) -> dict:
+    """Wall-clock time of the oracle on every configuration at full size,
+    single-threaded: median of 5 runs (3 for the embedding batch)."""
+    import oracle
+    import torch
+
+    def map_call(d):
+        return lambda: oracle.from_doc_ids(d)
+
+    def thd_call(bt):
+        return lambda: oracle.process_input_for_thd(bt)
+
+    def emb_call(emb):
+        h = emb["hidden"].view(torch.int16).numpy()
+
+        def run():
+            meta = oracle.thd_meta(emb["seq_lens"], emb["seq_lens_padded"], h.shape[1])
+            oracle.thd_gather(h, meta, h.shape[0], h.shape[1])
+            oracle.thd_padding_mask(meta["total_tokens"], meta["seq_real"], meta["seq_padded"])
+        return run
+
+    def squeeze_call(sq):
+        return lambda: oracle.pack_squeeze(sq["src"], sq["real_lens"], sq["bin_offsets"], sq["bin_members"],
+                                           sq["multiple"], sq["capacity"], sq["stretch"], sq["width"],
+                                           sq["pad_value"])
+
+    calls = {"map_small": map_call(host["map_small"]), "thd_small": thd_call(host["thd_small"]),
+             "thd_ids": thd_call(host["thd_ids"]), "thd_emb": emb_call(host["thd_emb"]),
+             "squeeze": squeeze_call(host["squeeze"]), "map_stress": map_call(host["map_stress"])}
+    if "squeeze_scaled" in host:
+        calls["squeeze_scaled"] = squeeze_call(host["squeeze_scaled"])
+    out = {}
+    for name, fn in calls.items():
+        n = 3 if name in ("thd_emb", "squeeze_scaled") else 5
+        ts = []
+        for _ in range(n):
+            t0 = time.perf_counter()
+            fn()
+            ts.append(time.perf_counter() - t0)
+        out[name] = {"ms": round(statistics.median(ts) * 1e3, 3), "runs": n}
+    return out
 
 
 # ----------------------------------------------------------------------------

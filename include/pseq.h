@@ -348,7 +348,12 @@ pseq_status thd_padding_mask(int64_t total_tokens,
  *   width is not checked (size a trainer-style row from info.total).
  * info: count = num_members, max_seqlen = largest real length, total = the
  *   largest padded total over bins before stretching.
- * workspace: pack_squeeze_workspace_size(num_members, num_bins) bytes.
+ * workspace: pack_squeeze_workspace_size(num_members, num_bins) bytes,
+ *   16-byte aligned, zero-filled before the first call; every call leaves it
+ *   zero again (a counter of finished bins wraps back to 0).  Calls that
+ *   share a workspace must be ordered (one stream).
+ * Host errors: PSEQ_ERR_OVERFLOW when a size exceeds the int32 range or
+ *   width exceeds 2^31 - 2^16; PSEQ_ERR_ARG for more than 65535 bins.
  * Device errors: PSEQ_ERR_CAPACITY when a bin's padded total exceeds
  *   capacity (or width, when out is given); PSEQ_ERR_VALUE for an empty bin,
  *   non-monotone offsets, a member outside [0, N) or a length outside [0, W].

@@ -476,13 +476,39 @@ def test_squeeze_random(dtype):
         check_squeeze(prob, m, cap, stretch, width, pad_value=int(rng.integers(-5, 5)))
 
 
-def test_squeeze_many_members_two_kernel_path():
+def test_squeeze_many_members():
     rng = np.random.default_rng(8)
     prob = synth.random_squeeze(rng, 1500, 40, 30)
     m = 8
     need = max(sum(-(-int(prob["real_lens"][i]) // m) * m for i in b) for b in prob["bins"])
     check_squeeze(prob, m, need + 16, True, need + 16, pad_value=3)
     check_squeeze(prob, m, need, False, need)
+
+
+def test_squeeze_bins_denser_than_a_window():
+    # multiple 1 and lengths 0..3: a window of output slots meets up to one
+    # member per slot, and zero-length members own no slot at all
+    rng = np.random.default_rng(9)
+    prob = synth.random_squeeze(rng, 6000, 4, 2)
+    need = max(sum(int(prob["real_lens"][i]) for i in b) for b in prob["bins"])
+    check_squeeze(prob, 1, need, False, need, pad_value=-1)
+    check_squeeze(prob, 1, need + 5, True, need + 7, pad_value=2)
+    one = synth.random_squeeze(rng, 5000, 2, 1)
+    need = int(one["real_lens"].sum())
+    check_squeeze(one, 1, need, False, need)
+
+
+def test_squeeze_wide_windows():
+    # enough (window, bin) CTAs that the 16-slot-per-thread kernel runs
+    c = synth.squeeze(3, N=2048)
+    check_squeeze(c, c["multiple"], c["capacity"], c["stretch"], c["width"], c["pad_value"])
+    d = synth.squeeze(4, N=2048, W=1024, multiple=8, capacity=8192)
+    check_squeeze(d, d["multiple"], d["capacity"], False, d["capacity"] + 8, pad_value=7)
+
+
+def test_squeeze_scaled_workload():
+    c = synth.squeeze(0, N=16384)
+    check_squeeze(c, c["multiple"], c["capacity"], c["stretch"], c["width"], c["pad_value"])
 
 
 def test_squeeze_workload():

@@ -96,12 +96,6 @@ __device__ __forceinline__ void st_word(unsigned long long* p, unsigned long lon
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 // Increment that wraps back to 0 after `limit`, with acquire-release order.
-__device__ __forceinline__ unsigned inc_acq_rel(unsigned* p, unsigned limit) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(limit) : "memory");
-  return old;
-}
-
 struct Header {
   unsigned int finished;  // tiles done with their look-back; wraps back to 0 after each call
   unsigned int gave_up;   // nonzero when some wait hit its time limit

@@ -6,224 +6,51 @@
 // lengths) and "Loader packs" (the last padded boundary stretched to the pack
 // capacity).
 //
-// Fused path (up to kFusedMaxMembers members, one launch): a grid of
-// (row chunk, bin) CTAs.  Every CTA scans its own bin's members into shared
-// memory -- padded lengths, both cumulative sums, the slot where each member
-// starts -- and then writes each slot of its chunk once: one thread per slot
-// looks its member up in the table and either loads the source token or
-// writes pad_value, with the padding mask alongside.  The first chunk of a bin
-// writes the bin's cu arrays; CTA (0, 0) also makes one pass over all members
-// to fold every bin's checks into the info block.
+// One launch over (slot window, bin) CTAs.  Every CTA scans its bin's members
+// (padded lengths, both cumulative sums) and keeps in shared memory only the
+// members whose padded range meets its window of output slots.  Those ranges
+// are disjoint and non-empty, so the table never holds more entries than the
+// window has slots, whatever the number of members.  Each thread then owns
+// kSlots slots of the window (interleaved across the CTA, so that a warp's
+// accesses are contiguous): it looks up the member of each slot, issues every
+// load before any store, and writes the token or pad_value with its mask
+// byte.  Every output slot is written exactly once.
 //
-// Two-kernel path (larger inputs): squeeze_meta_kernel gives each bin one
-// warp (chunked warp scan); squeeze_copy_kernel (programmatic dependent
-// launch) walks the members of its chunk: real tokens are one contiguous
-// block copy from the source row, padding slots one block fill.  Every
-// output slot is written exactly once.
+// The first window of every bin also writes the bin's cu arrays and its
+// status record; the last of those CTAs to finish (a wrapping acq_rel
+// counter) folds all records into the info block.
 #include "common.cuh"
 
 namespace pseq {
 namespace {
 
-constexpr int kMetaThreads = 256;
-constexpr int kMetaWarps = kMetaThreads / 32;
-constexpr int kCopyThreads = 512;
-constexpr int kFusedThreads = 512;
-constexpr int kFusedMaxMembers = 1024;
-constexpr int kSlotsPerThread = 4;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kSlotsWide = 16;   // slots per thread on large outputs
+constexpr int kSlotsNarrow = 4;  // slots per thread when the grid would be small
 
-struct Workspace {
-  int4* bin_stat;    // [num_bins] {status, padded total, largest real, members}
-  int32_t* mem_dst;  // [M] slot where the member starts in its bin
-  int32_t* mem_real; // [M]
-  int32_t* mem_src;  // [M] source row
+struct Header {
+  unsigned finished;
+  unsigned pad[31];
 };
 
-size_t workspace_bytes(int64_t M, int64_t num_bins) {
-  return round_up(16 * (size_t)num_bins, 16) + 3 * round_up(4 * (size_t)M, 16);
-}
-
-template <typename P>
-Workspace carve(P base_, int64_t M, int64_t num_bins) {
-  unsigned char* p = (unsigned char*)(base_);
-  Workspace w;
-  w.bin_stat = reinterpret_cast<int4*>(p);
-  p += round_up(16 * (size_t)num_bins, 16);
-  w.mem_dst = reinterpret_cast<int32_t*>(p);
-  p += round_up(4 * (size_t)M, 16);
-  w.mem_real = reinterpret_cast<int32_t*>(p);
-  p += round_up(4 * (size_t)M, 16);
-  w.mem_src = reinterpret_cast<int32_t*>(p);
-  return w;
-}
-
-struct MetaArgs {
-  const int64_t* real;
-  const int32_t* off;
-  const int32_t* mem;
-  int num_bins, M;
-  int64_t N, W, multiple, capacity, width;
-  int stretch, check_width;
-  int32_t* cu;
-  int32_t* cup;
+struct BinRec {
+  int status, total, longest, members;
 };
 
-__global__ void __launch_bounds__(kMetaThreads) squeeze_meta_kernel(MetaArgs a, Workspace ws) {
-  pdl_enter();
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int b = blockIdx.x * kMetaWarps + warp;
-  if (b >= a.num_bins) return;
-  const int lo = __ldg(a.off + b), hi = __ldg(a.off + b + 1);
-  const bool bad_offsets = (b == 0 && lo != 0) || (b == a.num_bins - 1 && hi != a.M) || lo < 0 || hi > a.M ||
-                           hi <= lo;
-  if (bad_offsets) {
-    if (lane == 0) ws.bin_stat[b] = make_int4(PSEQ_ERR_VALUE, 0, 0, 0);
-    return;
-  }
-  long long run_real = 0, run_padded = 0;
-  int longest = 0;
-  bool bad = false;
-  for (int base = lo; base < hi; base += 32) {
-    const int e = base + lane;
-    long long real = 0, padded = 0;
-    int src = 0;
-    if (e < hi) {
-      src = __ldg(a.mem + e);
-      if (src < 0 || src >= a.N) {
-        bad = true;
-      } else {
-        real = __ldg(a.real + src);
-        if (real < 0 || real > a.W) {
-          bad = true;
-          real = 0;
-        }
-      }
-      padded = (real + a.multiple - 1) / a.multiple * a.multiple;
-      longest = max(longest, (int)real);
-    }
-    long long ir = real, ip = padded;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const long long r = __shfl_up_sync(~0u, ir, d), q = __shfl_up_sync(~0u, ip, d);
-      if (lane >= d) {
-        ir += r;
-        ip += q;
-      }
-    }
-    if (e < hi) {
-      const long long R = run_real + ir - real, Pd = run_padded + ip - padded;
-      a.cu[e + b] = (int32_t)R;
-      a.cup[e + b] = (int32_t)Pd;
-      ws.mem_dst[e] = (int32_t)Pd;
-      ws.mem_real[e] = (int32_t)real;
-      ws.mem_src[e] = src;
-    }
-    run_real += __shfl_sync(~0u, ir, 31);
-    run_padded += __shfl_sync(~0u, ip, 31);
-  }
-  bad = __any_sync(~0u, bad);
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) longest = max(longest, __shfl_xor_sync(~0u, longest, d));
-  if (lane == 0) {
-    int status = PSEQ_OK;
-    if (bad) status = PSEQ_ERR_VALUE;
-    else if (run_padded > a.capacity || (a.check_width && run_padded > a.width)) status = PSEQ_ERR_CAPACITY;
-    a.cu[hi + b] = (int32_t)run_real;
-    a.cup[hi + b] = a.stretch ? (int32_t)a.capacity : (int32_t)run_padded;
-    ws.bin_stat[b] = make_int4(status, (int)min(run_padded, (long long)INT32_MAX), longest, hi - lo);
-  }
+size_t workspace_bytes(int64_t num_bins) { return sizeof(Header) + sizeof(BinRec) * (size_t)num_bins; }
+
+template <int SLOTS>
+__host__ __device__ constexpr int window() {
+  return kThreads * SLOTS;
 }
 
-struct CopyArgs {
-  const unsigned char* src;
-  int64_t W;
-  int elem_bytes;
-  const int32_t* off;
-  int num_bins, M;
-  int64_t width, chunk, pad_value;
-  unsigned char* out;   // may be NULL (metadata only)
-  uint8_t* mask;        // may be NULL
-  pseq_info* info;
-};
-
-// Largest k in [lo, hi) with dst[k] <= x, given dst[lo] <= x.
-__device__ __forceinline__ int warp_find(const int32_t* dst, int lo, int hi, int64_t x) {
-  const int lane = threadIdx.x & 31;
-  while (hi - lo > 1) {
-    const int step = (hi - lo + 31) / 32;
-    const int probe = lo + lane * step;
-    const bool ok = probe < hi && (int64_t)__ldcg(dst + probe) <= x;
-    const unsigned m = __ballot_sync(~0u, ok);
-    lo = lo + (31 - __clz(m)) * step;
-    hi = min(lo + step, hi);
-  }
-  return lo;
+template <int SLOTS>
+__host__ __device__ constexpr size_t table_bytes() {
+  return 3 * sizeof(int32_t) * (size_t)window<SLOTS>();
 }
 
-__global__ void __launch_bounds__(kCopyThreads) squeeze_copy_kernel(CopyArgs c, Workspace ws) {
-  __shared__ int s_value, s_capacity, s_longest, s_widest, s_first;
-  pdl_enter();
-  const int tid = threadIdx.x;
-  const int b = blockIdx.y;
-  if (blockIdx.x == 0 && b == 0) {
-    if (tid == 0) s_value = s_capacity = s_longest = s_widest = 0;
-    __syncthreads();
-    for (int i = tid; i < c.num_bins; i += kCopyThreads) {
-      const int4 st = __ldcg(ws.bin_stat + i);
-      if (st.x == PSEQ_ERR_VALUE) s_value = 1;
-      if (st.x == PSEQ_ERR_CAPACITY) s_capacity = 1;
-      atomicMax(&s_longest, st.z);
-      atomicMax(&s_widest, st.y);
-    }
-    __syncthreads();
-    if (tid == 0) {
-      const int status = s_value ? PSEQ_ERR_VALUE : (s_capacity ? PSEQ_ERR_CAPACITY : PSEQ_OK);
-      *c.info = status == PSEQ_OK ? pseq_info{PSEQ_OK, c.M, s_longest, s_widest} : pseq_info{status, 0, 0, 0};
-    }
-  }
-  if (!c.out || b >= c.num_bins) return;
-  const int4 st = __ldcg(ws.bin_stat + b);
-  if (st.x != PSEQ_OK) return;
-  const int64_t c0 = (int64_t)blockIdx.x * c.chunk;
-  const int64_t c1 = min(c0 + c.chunk, c.width);
-  if (c0 >= c1) return;
-  const int eb = c.elem_bytes;
-  const int64_t total = st.y;
-  unsigned char* row = c.out + (int64_t)b * c.width * eb;
-  uint8_t* mrow = c.mask ? c.mask + (int64_t)b * c.width : nullptr;
-  if (c0 < total) {
-    const int lo = __ldg(c.off + b), hi = __ldg(c.off + b + 1);
-    if (tid < 32) {
-      const int k = warp_find(ws.mem_dst, lo, hi, c0);
-      if (tid == 0) s_first = k;
-    }
-    __syncthreads();
-    for (int k = s_first; k < hi; ++k) {
-      const int64_t s = __ldcg(ws.mem_dst + k);
-      if (s >= c1) break;
-      const int64_t real_end = s + __ldcg(ws.mem_real + k);
-      const int64_t e = (k + 1 < hi) ? (int64_t)__ldcg(ws.mem_dst + k + 1) : total;
-      const int64_t a0 = max(s, c0), a1 = min(real_end, c1);
-      if (a0 < a1) {
-        const int64_t i = __ldcg(ws.mem_src + k);
-        block_copy(row + a0 * eb, c.src + (i * c.W + (a0 - s)) * eb, (a1 - a0) * eb);
-        if (mrow) block_fill_bytes(mrow + a0, a1 - a0, 0);
-      }
-      const int64_t p0 = max(real_end, c0), p1 = min(e, c1);
-      if (p0 < p1) {
-        block_fill(row + p0 * eb, p1 - p0, eb, c.pad_value);
-        if (mrow) block_fill_bytes(mrow + p0, p1 - p0, 1);
-      }
-    }
-  }
-  const int64_t t0 = max(total, c0);
-  if (t0 < c1) {
-    block_fill(row + t0 * eb, c1 - t0, eb, c.pad_value);
-    if (mrow) block_fill_bytes(mrow + t0, c1 - t0, 1);
-  }
-}
-
-struct FusedArgs {
+struct Args {
   const unsigned char* src;
   const int64_t* real;
   const int32_t* off;
@@ -236,146 +63,266 @@ struct FusedArgs {
   int32_t* cu;
   int32_t* cup;
   pseq_info* info;
+  Header* hdr;
+  BinRec* rec;
 };
 
-__device__ __forceinline__ bool offsets_bad(const FusedArgs& a, int b, int lo, int hi) {
+__device__ __forceinline__ bool offsets_bad(const Args& a, int b, int lo, int hi) {
   return (b == 0 && lo != 0) || (b == a.num_bins - 1 && hi != a.M) || lo < 0 || hi > a.M || hi <= lo;
 }
 
-// CTA (0, 0): one pass over every member to fold all bins' checks into info.
-__device__ void squeeze_info_pass(const FusedArgs& a, int32_t* s_off, unsigned long long* s_tot) {
-  __shared__ int s_value, s_capacity, s_longest, s_widest;
-  const int tid = threadIdx.x;
-  if (tid == 0) s_value = s_capacity = s_longest = s_widest = 0;
-  for (int i = tid; i <= a.num_bins; i += kFusedThreads) s_off[i] = __ldg(a.off + i);
-  for (int i = tid; i < a.num_bins; i += kFusedThreads) s_tot[i] = 0ull;
+// Exclusive count of set flags over the block; `total` gets the block count.
+__device__ __forceinline__ int block_count_exclusive(bool flag, int* s_warp, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned m = __ballot_sync(~0u, flag);
+  if (lane == 0) s_warp[warp] = __popc(m);
   __syncthreads();
-  for (int b = tid; b < a.num_bins; b += kFusedThreads)
-    if (offsets_bad(a, b, s_off[b], s_off[b + 1])) s_value = 1;
-  for (int e = tid; e < a.M; e += kFusedThreads) {
-    const int b = seq_of(s_off, a.num_bins, e);
-    const int i = __ldg(a.mem + e);
-    if (i < 0 || i >= a.N) {
-      s_value = 1;
-      continue;
-    }
-    const long long real = __ldg(a.real + i);
-    if (real < 0 || real > a.W) {
-      s_value = 1;
-      continue;
-    }
-    atomicAdd(&s_tot[b], (unsigned long long)((real + a.multiple - 1) / a.multiple * a.multiple));
-    atomicMax(&s_longest, (int)real);
+  int before = 0, sum = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int c = s_warp[w];
+    before += w < warp ? c : 0;
+    sum += c;
   }
+  total = sum;
   __syncthreads();
-  for (int b = tid; b < a.num_bins; b += kFusedThreads) {
-    const unsigned long long t = s_tot[b];
-    if (t > (unsigned long long)a.capacity || (a.out && t > (unsigned long long)a.width)) s_capacity = 1;
-    atomicMax(&s_widest, (int)min(t, (unsigned long long)INT32_MAX));
-  }
-  __syncthreads();
-  if (tid == 0) {
-    const int status = s_value ? PSEQ_ERR_VALUE : (s_capacity ? PSEQ_ERR_CAPACITY : PSEQ_OK);
-    *a.info = status == PSEQ_OK ? pseq_info{PSEQ_OK, a.M, s_longest, s_widest} : pseq_info{status, 0, 0, 0};
-  }
-  __syncthreads();
+  return before + __popc(m & ((1u << lane) - 1u));
 }
 
-__global__ void __launch_bounds__(kFusedThreads) squeeze_fused_kernel(const __grid_constant__ FusedArgs a) {
-  __shared__ int32_t s_dst[kFusedMaxMembers + 1];
-  __shared__ int32_t s_real[kFusedMaxMembers];
-  __shared__ int32_t s_src[kFusedMaxMembers];
-  __shared__ int32_t s_off[kFusedMaxMembers + 1];
-  __shared__ unsigned long long s_tot[kFusedMaxMembers];
-  __shared__ Triple scratch[kFusedThreads / 32];
-  __shared__ int s_bad;
+template <int EB>
+struct Elem;
+template <>
+struct Elem<1> {
+  using T = unsigned char;
+};
+template <>
+struct Elem<2> {
+  using T = unsigned short;
+};
+template <>
+struct Elem<4> {
+  using T = unsigned int;
+};
+template <>
+struct Elem<8> {
+  using T = unsigned long long;
+};
+
+// The last bin record to arrive: fold every bin's record into info.
+__device__ __noinline__ void fold_records(const Args& a) {
+  __shared__ int f_value, f_capacity, f_longest, f_widest;
+  const int tid = threadIdx.x;
+  if (tid == 0) f_value = f_capacity = f_longest = f_widest = 0;
+  __syncthreads();
+  int value = 0, capacity = 0, longest = 0, widest = 0;
+  for (int i = tid; i < a.num_bins; i += kThreads) {
+    // L2 loads: the records were released by the counter that thread 0 acquired
+    const int4 r = __ldcg(reinterpret_cast<const int4*>(a.rec + i));
+    value |= r.x == PSEQ_ERR_VALUE;
+    capacity |= r.x == PSEQ_ERR_CAPACITY;
+    widest = max(widest, r.y);
+    longest = max(longest, r.z);
+  }
+  if (value) f_value = 1;
+  if (capacity) f_capacity = 1;
+  atomicMax(&f_longest, longest);
+  atomicMax(&f_widest, widest);
+  __syncthreads();
+  if (tid == 0) {
+    const int status = f_value ? PSEQ_ERR_VALUE : (f_capacity ? PSEQ_ERR_CAPACITY : PSEQ_OK);
+    *a.info = status == PSEQ_OK ? pseq_info{PSEQ_OK, a.M, f_longest, f_widest} : pseq_info{status, 0, 0, 0};
+  }
+}
+
+template <int SLOTS, int EB, bool VEC>
+__global__ void __launch_bounds__(kThreads, SLOTS >= 16 ? 3 : 4) squeeze_kernel(const __grid_constant__ Args a) {
+  extern __shared__ __align__(16) int32_t s_table[];
+  constexpr int kWindow = window<SLOTS>();
+  int32_t* s_dst = s_table;
+  int32_t* s_real = s_table + kWindow;
+  int32_t* s_src = s_table + 2 * kWindow;
+  __shared__ Triple scratch[kWarps];
+  __shared__ int s_count[kWarps];
+  __shared__ int s_bad, s_longest, s_last;
   pdl_enter();
   const int tid = threadIdx.x;
   const int b = blockIdx.y;
-  if (blockIdx.x == 0 && b == 0) squeeze_info_pass(a, s_off, s_tot);
+  const bool first = blockIdx.x == 0;
   const int lo = __ldg(a.off + b), hi = __ldg(a.off + b + 1);
-  if (offsets_bad(a, b, lo, hi) || hi - lo > kFusedMaxMembers) return;
-  const int n = hi - lo;
-  if (tid == 0) s_bad = 0;
+  const bool bad_offsets = offsets_bad(a, b, lo, hi);
+  const int64_t c0 = (int64_t)blockIdx.x * kWindow;
+  const int64_t c1 = min(c0 + (int64_t)kWindow, a.width);
+  if (tid == 0) {
+    s_bad = 0;
+    s_longest = 0;
+  }
   __syncthreads();
-  // scan the bin's members: slot where each starts, both cumulative sums
+  // the bin's members: both cumulative sums; keep the ones meeting the window
   Triple carry = {0, 0, 0};
-  for (int base = 0; base < n; base += kFusedThreads) {
-    const int j = base + tid;
-    long long real = 0, padded = 0;
-    int src = 0;
-    if (j < n) {
-      src = __ldg(a.mem + lo + j);
-      if (src < 0 || src >= a.N) {
-        s_bad = 1;
-      } else {
-        real = __ldg(a.real + src);
-        if (real < 0 || real > a.W) {
+  int held = 0;
+  if (!bad_offsets) {
+    const int n = hi - lo;
+    for (int base = 0; base < n; base += kThreads) {
+      const int j = base + tid;
+      long long real = 0, padded = 0;
+      int src = 0;
+      if (j < n) {
+        src = __ldg(a.mem + lo + j);
+        if (src < 0 || src >= a.N) {
           s_bad = 1;
-          real = 0;
+        } else {
+          real = __ldg(a.real + src);
+          if (real < 0 || real > a.W) {
+            s_bad = 1;
+            real = 0;
+          }
         }
+        // real <= W and multiple <= INT32_MAX: the rounding fits 32 bits
+        const uint32_t m = (uint32_t)a.multiple;
+        padded = (long long)(((uint32_t)real + m - 1u) / m) * m;
+        atomicMax(&s_longest, (int)real);
       }
-      padded = (real + a.multiple - 1) / a.multiple * a.multiple;
-    }
-    Triple total;
-    const Triple ex = block_exclusive<kFusedThreads / 32>({0, real, padded}, scratch, total);
-    if (j < n) {
+      Triple total;
+      const Triple ex = block_exclusive<kWarps>({0, real, padded}, scratch, total);
       const long long R = carry.real + ex.real, Pd = carry.padded + ex.padded;
-      s_dst[j] = (int32_t)Pd;
-      s_real[j] = (int32_t)real;
-      s_src[j] = src;
-      if (blockIdx.x == 0) {
+      if (first && j < n) {
         a.cu[lo + b + j] = (int32_t)R;
         a.cup[lo + b + j] = (int32_t)Pd;
       }
-    }
-    carry = add(carry, total);
-  }
-  const long long total_pad = carry.padded;
-  if (tid == 0) {
-    s_dst[n] = (int32_t)min(total_pad, (long long)INT32_MAX);
-    if (blockIdx.x == 0) {
-      a.cu[hi + b] = (int32_t)carry.real;
-      a.cup[hi + b] = a.stretch ? (int32_t)a.capacity : (int32_t)total_pad;
+      const bool keep = j < n && padded > 0 && Pd < c1 && Pd + padded > c0;
+      int kept;
+      const int pos = held + block_count_exclusive(keep, s_count, kept);
+      if (keep) {
+        s_dst[pos] = (int32_t)Pd;
+        s_real[pos] = (int32_t)real;
+        s_src[pos] = src;
+      }
+      held += kept;
+      carry = add(carry, total);
     }
   }
   __syncthreads();
-  if (s_bad || total_pad > a.capacity || !a.out || total_pad > a.width) return;
-  // every slot of this chunk, once
-  const int eb = a.elem_bytes;
-  const int64_t chunk = (int64_t)kFusedThreads * kSlotsPerThread;
-  const int64_t c0 = (int64_t)blockIdx.x * chunk;
-  const int64_t c1 = min(c0 + chunk, a.width);
-  unsigned char* row = a.out + (int64_t)b * a.width * eb;
-  uint8_t* mrow = a.mask ? a.mask + (int64_t)b * a.width : nullptr;
-  int4 v[kSlotsPerThread];
-  bool pad[kSlotsPerThread];
-  int4 pv = make_int4(0, 0, 0, 0);
-  {
-    const uint64_t p = (uint64_t)a.pad_value;
-    pv.x = (int)(uint32_t)p;
-    pv.y = (int)(uint32_t)(p >> 32);
+  const long long total_pad = carry.padded;
+  int status = PSEQ_OK;
+  if (bad_offsets || s_bad) status = PSEQ_ERR_VALUE;
+  else if (total_pad > a.capacity || (a.out && total_pad > a.width)) status = PSEQ_ERR_CAPACITY;
+  if (first) {
+    if (tid == 0) {
+      if (!bad_offsets) {
+        a.cu[hi + b] = (int32_t)carry.real;
+        a.cup[hi + b] = a.stretch ? (int32_t)a.capacity : (int32_t)total_pad;
+      }
+      a.rec[b] = BinRec{status, (int)min(total_pad, (long long)INT32_MAX), s_longest, bad_offsets ? 0 : hi - lo};
+      s_last = inc_acq_rel(&a.hdr->finished, (unsigned)a.num_bins - 1u) == (unsigned)a.num_bins - 1u;
+    }
+    __syncthreads();
+    if (s_last) fold_records(a);
   }
+  if (status != PSEQ_OK || !a.out) return;
+  // every slot of the window, once: loads first, then stores.  A thread's
+  // slots ascend, so its member index only moves forward through the table.
+  using T = typename Elem<EB>::T;
+  const T* src = reinterpret_cast<const T*>(a.src);
+  T* row = reinterpret_cast<T*>(a.out) + (int64_t)b * a.width;
+  uint8_t* mrow = a.mask ? a.mask + (int64_t)b * a.width : nullptr;
+  const int32_t lim = (int32_t)min((long long)c1, total_pad);  // slots below are in members
+  const int32_t end = (int32_t)c1;
+  const T pv = (T)(uint64_t)a.pad_value;
+  int j = 0;
+  if constexpr (VEC) {
+    // 16-byte vectors of V slots.  The host takes this path only when row
+    // pitches, width and multiple keep every member start on a vector
+    // boundary, so a vector never spans two members; only the real/padding
+    // boundary inside a member can fall inside one.
+    constexpr int V = 16 / EB;
+    constexpr int NV = SLOTS / V;
+    static_assert(NV * V == SLOTS, "window must hold whole vectors");
+    T pad_elems[V];
 #pragma unroll
-  for (int q = 0; q < kSlotsPerThread; ++q) {
-    const int64_t t = c0 + tid + (int64_t)q * kFusedThreads;
-    pad[q] = true;
-    v[q] = pv;
-    if (t < c1 && t < total_pad) {
-      const int j = seq_of(s_dst, n, t);
-      const int64_t off = t - s_dst[j];
-      if (off < s_real[j]) {
-        pad[q] = false;
-        v[q] = load_row(a.src + ((int64_t)s_src[j] * a.W + off) * eb, eb);
+    for (int k = 0; k < V; ++k) pad_elems[k] = pv;
+    int4 pad4;
+    memcpy(&pad4, pad_elems, 16);
+    int4 v[NV];
+    int nreal[NV];
+    const int32_t base = (int32_t)c0 + tid * V;
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+      const int32_t t = base + q * kThreads * V;
+      v[q] = pad4;
+      nreal[q] = 0;
+      if (t < lim) {
+        while (j + 1 < held && s_dst[j + 1] <= t) ++j;
+        const int32_t off = t - s_dst[j];
+        const int32_t r = s_real[j];
+        const T* p = src + (int64_t)s_src[j] * a.W + off;
+        if (off + V <= r) {
+          v[q] = ld_stream(reinterpret_cast<const int4*>(p));
+          nreal[q] = V;
+        } else if (off < r) {
+          T e[V];
+#pragma unroll
+          for (int k = 0; k < V; ++k) e[k] = off + k < r ? __ldg(p + k) : pv;
+          memcpy(&v[q], e, 16);
+          nreal[q] = r - off;
+        }
       }
     }
-  }
 #pragma unroll
-  for (int q = 0; q < kSlotsPerThread; ++q) {
-    const int64_t t = c0 + tid + (int64_t)q * kFusedThreads;
-    if (t < c1) {
-      store_row(row + t * eb, v[q], eb);
-      if (mrow) mrow[t] = pad[q] ? 1 : 0;
+    for (int q = 0; q < NV; ++q) {
+      const int32_t t = base + q * kThreads * V;
+      if (t < end) {
+        st_stream(reinterpret_cast<int4*>(row + t), v[q]);
+        if (mrow) {
+          // byte k is 1 for padding: slots nreal[q] .. V-1
+          uint8_t m[V];
+#pragma unroll
+          for (int k = 0; k < V; ++k) m[k] = k >= nreal[q] ? 1 : 0;
+          if constexpr (V == 16) {
+            int4 w;
+            memcpy(&w, m, 16);
+            *reinterpret_cast<int4*>(mrow + t) = w;
+          } else if constexpr (V == 8) {
+            unsigned long long w;
+            memcpy(&w, m, 8);
+            *reinterpret_cast<unsigned long long*>(mrow + t) = w;
+          } else if constexpr (V == 4) {
+            unsigned int w;
+            memcpy(&w, m, 4);
+            *reinterpret_cast<unsigned int*>(mrow + t) = w;
+          } else {
+            unsigned short w;
+            memcpy(&w, m, 2);
+            *reinterpret_cast<unsigned short*>(mrow + t) = w;
+          }
+        }
+      }
+    }
+  } else {
+    T v[SLOTS];
+    unsigned padmask = 0;
+    const int32_t base = (int32_t)c0 + tid;
+#pragma unroll
+    for (int q = 0; q < SLOTS; ++q) {
+      const int32_t t = base + q * kThreads;
+      v[q] = pv;
+      bool pad = true;
+      if (t < lim) {
+        while (j + 1 < held && s_dst[j + 1] <= t) ++j;
+        const int32_t off = t - s_dst[j];
+        if (off < s_real[j]) {
+          pad = false;
+          v[q] = __ldg(src + (int64_t)s_src[j] * a.W + off);
+        }
+      }
+      padmask |= (pad ? 1u : 0u) << q;
+    }
+#pragma unroll
+    for (int q = 0; q < SLOTS; ++q) {
+      const int32_t t = base + q * kThreads;
+      if (t < end) {
+        __stcs(row + t, v[q]);
+        if (mrow) mrow[t] = (uint8_t)((padmask >> q) & 1u);
+      }
     }
   }
 }
@@ -385,6 +332,38 @@ __global__ void empty_squeeze_kernel(pseq_info* info) {
   *info = {PSEQ_OK, 0, 0, 0};
 }
 
+template <int SLOTS, int EB, bool VEC>
+cudaError_t launch_squeeze(const Args& a, unsigned gy, cudaStream_t st) {
+  static bool configured = false;  // per process; the attribute is per function
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(squeeze_kernel<SLOTS, EB, VEC>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)table_bytes<SLOTS>());
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  constexpr int64_t w = window<SLOTS>();
+  const unsigned gx = a.out && a.width > 0 ? (unsigned)((a.width + w - 1) / w) : 1u;
+  return launch_pdl(squeeze_kernel<SLOTS, EB, VEC>, dim3(gx, gy), dim3(kThreads), table_bytes<SLOTS>(), st, a);
+}
+
+template <int SLOTS, int EB>
+cudaError_t launch_squeeze(const Args& a, bool vec, unsigned gy, cudaStream_t st) {
+  if constexpr (SLOTS % (16 / EB) == 0) {
+    if (vec) return launch_squeeze<SLOTS, EB, true>(a, gy, st);
+  }
+  return launch_squeeze<SLOTS, EB, false>(a, gy, st);
+}
+
+template <int SLOTS>
+cudaError_t launch_squeeze(const Args& a, bool vec, unsigned gy, cudaStream_t st) {
+  switch (a.elem_bytes) {
+    case 8: return launch_squeeze<SLOTS, 8>(a, vec, gy, st);
+    case 4: return launch_squeeze<SLOTS, 4>(a, vec, gy, st);
+    case 2: return launch_squeeze<SLOTS, 2>(a, vec, gy, st);
+    default: return launch_squeeze<SLOTS, 1>(a, vec, gy, st);
+  }
+}
+
 }  // namespace
 }  // namespace pseq
 
@@ -392,7 +371,7 @@ using namespace pseq;
 
 extern "C" size_t pack_squeeze_workspace_size(int64_t num_members, int64_t num_bins) {
   if (num_members < 0 || num_bins < 0) return 0;
-  return workspace_bytes(num_members, num_bins);
+  return workspace_bytes(num_bins);
 }
 
 extern "C" pseq_status pack_squeeze(const void* src, int64_t N, int64_t W, int32_t elem_bytes,
@@ -412,6 +391,7 @@ extern "C" pseq_status pack_squeeze(const void* src, int64_t N, int64_t W, int32
   if (N > INT32_MAX || W > INT32_MAX || capacity > INT32_MAX || width > INT32_MAX || num_bins > INT32_MAX / 2 ||
       num_members > INT32_MAX / 2)
     return fail(PSEQ_ERR_OVERFLOW, "%s: a size exceeds the int32 range", fn);
+  if (width > INT32_MAX - 65536) return fail(PSEQ_ERR_OVERFLOW, "%s: width exceeds 2^31 - 2^16", fn);
   if (num_bins > 65535) return fail(PSEQ_ERR_ARG, "%s: at most 65535 bins per call", fn);
   if ((out == nullptr) != (padding_mask == nullptr) && out == nullptr)
     return fail(PSEQ_ERR_ARG, "%s: padding_mask needs out", fn);
@@ -433,89 +413,42 @@ extern "C" pseq_status pack_squeeze(const void* src, int64_t N, int64_t W, int32
     if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
     return check_launch(fn);
   }
-  const size_t need = workspace_bytes(num_members, num_bins);
+  const size_t need = workspace_bytes(num_bins);
   if (!workspace || workspace_bytes_ < need || !aligned(workspace, 16))
     return fail(PSEQ_ERR_ARG, "%s: workspace needs %zu bytes, 16-byte aligned (got %zu)", fn, need, workspace_bytes_);
-  if (num_members <= kFusedMaxMembers && num_bins <= kFusedMaxMembers) {
-    FusedArgs a = {};
-    a.src = static_cast<const unsigned char*>(src);
-    a.real = real_lens;
-    a.off = bin_offsets;
-    a.mem = bin_members;
-    a.num_bins = (int)num_bins;
-    a.M = (int)num_members;
-    a.N = N;
-    a.W = W;
-    a.multiple = multiple;
-    a.capacity = capacity;
-    a.width = width;
-    a.pad_value = pad_value;
-    a.stretch = stretch_to_capacity ? 1 : 0;
-    a.elem_bytes = elem_bytes;
-    a.out = static_cast<unsigned char*>(out);
-    a.mask = padding_mask;
-    a.cu = cu_seqlens;
-    a.cup = cu_seqlens_padded;
-    a.info = info;
-    const int64_t chunk = (int64_t)kFusedThreads * kSlotsPerThread;
-    const unsigned gx = out && width > 0 ? (unsigned)((width + chunk - 1) / chunk) : 1u;
-    const cudaError_t e = launch_pdl(squeeze_fused_kernel, dim3(gx, (unsigned)num_bins), dim3(kFusedThreads), 0, st, a);
-    count_launches(1);
-    if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
-    return check_launch(fn);
-  }
-  Workspace ws = carve(workspace, num_members, num_bins);
-
-  MetaArgs m = {};
-  m.real = real_lens;
-  m.off = bin_offsets;
-  m.mem = bin_members;
-  m.num_bins = (int)num_bins;
-  m.M = (int)num_members;
-  m.N = N;
-  m.W = W;
-  m.multiple = multiple;
-  m.capacity = capacity;
-  m.width = width;
-  m.stretch = stretch_to_capacity ? 1 : 0;
-  m.check_width = out ? 1 : 0;
-  m.cu = cu_seqlens;
-  m.cup = cu_seqlens_padded;
-  cudaError_t e = launch_pdl(squeeze_meta_kernel, dim3((unsigned)((num_bins + kMetaWarps - 1) / kMetaWarps)),
-                             dim3(kMetaThreads), 0, st, m, ws);
-  count_launches(1);
-  if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
-  pseq_status s = check_launch(fn);
-  if (s != PSEQ_OK) return s;
-
-  CopyArgs c = {};
-  c.src = static_cast<const unsigned char*>(src);
-  c.W = W;
-  c.elem_bytes = elem_bytes;
-  c.off = bin_offsets;
-  c.num_bins = (int)num_bins;
-  c.M = (int)num_members;
-  c.width = width;
-  c.pad_value = pad_value;
-  c.out = static_cast<unsigned char*>(out);
-  c.mask = padding_mask;
-  c.info = info;
-  dim3 grid(1, 1);
-  if (out && width > 0) {
-    // chunks of whole 16-byte groups, about four CTAs per SM over the output
-    const int64_t slots = num_bins * width;
-    const int64_t target = (int64_t)sm_count() * 4;
-    int64_t chunk = (slots + target - 1) / target;
-    const int64_t per16 = 16 / elem_bytes;
-    const int64_t min_chunk = 4096 / elem_bytes;
-    if (chunk < min_chunk) chunk = min_chunk;
-    chunk = (chunk + per16 - 1) / per16 * per16;
-    c.chunk = chunk;
-    grid = dim3((unsigned)((width + chunk - 1) / chunk), (unsigned)num_bins);
-  } else {
-    c.chunk = 1;
-  }
-  e = launch_pdl(squeeze_copy_kernel, grid, dim3(kCopyThreads), 0, st, c, ws);
+  Args a = {};
+  a.src = static_cast<const unsigned char*>(src);
+  a.real = real_lens;
+  a.off = bin_offsets;
+  a.mem = bin_members;
+  a.num_bins = (int)num_bins;
+  a.M = (int)num_members;
+  a.N = N;
+  a.W = W;
+  a.multiple = multiple;
+  a.capacity = capacity;
+  a.width = width;
+  a.pad_value = pad_value;
+  a.stretch = stretch_to_capacity ? 1 : 0;
+  a.elem_bytes = elem_bytes;
+  a.out = static_cast<unsigned char*>(out);
+  a.mask = padding_mask;
+  a.cu = cu_seqlens;
+  a.cup = cu_seqlens_padded;
+  a.info = info;
+  a.hdr = static_cast<Header*>(workspace);
+  a.rec = reinterpret_cast<BinRec*>(static_cast<unsigned char*>(workspace) + sizeof(Header));
+  // wide windows when they still give every SM two CTAs, else narrow ones
+  const int64_t wide_ctas = (out && width > 0 ? (width + window<kSlotsWide>() - 1) / window<kSlotsWide>() : 1) *
+                            num_bins;
+  // 16-byte vectors when every member start, row start and window start
+  // falls on a 16-byte boundary of both src and out
+  const int64_t eb = elem_bytes;
+  const bool vec = out && aligned(src, 16) && aligned(out, 16) && aligned(padding_mask, 16) && (W * eb) % 16 == 0 &&
+                   (width * eb) % 16 == 0 && (multiple * eb) % 16 == 0;
+  const cudaError_t e = wide_ctas >= 2 * (int64_t)sm_count()
+                            ? launch_squeeze<kSlotsWide>(a, vec, (unsigned)num_bins, st)
+                            : launch_squeeze<kSlotsNarrow>(a, vec, (unsigned)num_bins, st);
   count_launches(1);
   if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
   return check_launch(fn);

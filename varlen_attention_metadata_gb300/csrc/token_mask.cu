@@ -34,12 +34,6 @@ struct Part {
 
 size_t workspace_bytes(int64_t ctas) { return sizeof(Header) + sizeof(Part) * (size_t)ctas; }
 
-__device__ __forceinline__ unsigned inc_acq_rel(unsigned* p, unsigned limit) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(limit) : "memory");
-  return old;
-}
-
 template <typename Id, bool kVector>
 __global__ void __launch_bounds__(kThreads)
     token_mask_kernel(const Id* __restrict__ ids, int64_t n, Id pad, uint8_t* __restrict__ mask,
