@@ -16,8 +16,9 @@
 //
 // Every published summary is two 64-bit words, each carrying a valid bit, so
 // a single poll returns the summary itself: no flag-then-value round trip and
-// no release fence on the publishing side.  A look-back round polls 128
-// predecessors at once.  A map that fits one tile skips all of this.  Waits are bounded by a time limit
+// no release fence on the publishing side.  A look-back round polls 32
+// predecessors at once (one per lane), all loads in flight together, and
+// joins them with a shuffle tree.  A map that fits one tile skips all of this.  Waits are bounded by a time limit
 // and report PSEQ_ERR_TIMEOUT.  Boundaries are compacted through shared
 // memory (tile-relative 16-bit positions) and stored coalesced.  The CTA that
 // finishes its look-back last writes cu_seqlens[num_segments] and the info
@@ -39,7 +40,7 @@ namespace {
 constexpr int kThreads = PSEQ_SCAN_THREADS;
 constexpr int kWarps = kThreads / 32;
 constexpr int kItems = PSEQ_SCAN_ITEMS;
-constexpr int kPerLane = 4;  // look-back windows of 32 tiles polled together
+constexpr int kPerLane = 1;  // look-back windows of 32 tiles polled together (more unrolled code costs more on a cold instruction cache than extra rounds)
 constexpr int kTile = kThreads * kItems;  // tokens per tile
 static_assert(kTile <= 65536, "tile-relative positions are 16-bit");
 
@@ -242,18 +243,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         int polls = 0;
         uint64_t start = 0;
         while (true) {
+          // issue every window's loads before looking at any of them, so a
+          // round costs one L2 round trip however many windows are open
+          unsigned long long ia[kPerLane], ib[kPerLane], aa[kPerLane], ab[kPerLane];
+#pragma unroll
+          for (int w = 0; w < kPerLane; ++w) {
+            ia[w] = ib[w] = aa[w] = ab[w] = 0ull;
+            if (!done[w]) {
+              const Slot* sl = ws.slots + (j - 32 * w - lane);
+              ia[w] = ld_word(&sl->inc_a);
+              ib[w] = ld_word(&sl->inc_b);
+              aa[w] = ld_word(&sl->agg_a);
+              ab[w] = ld_word(&sl->agg_b);
+            }
+          }
           bool all_done = true;
 #pragma unroll
           for (int w = 0; w < kPerLane; ++w) {
             if (done[w]) continue;
-            const Slot* sl = ws.slots + (j - 32 * w - lane);
-            const unsigned long long ia = ld_word(&sl->inc_a), ib = ld_word(&sl->inc_b);
-            const unsigned long long aa = ld_word(&sl->agg_a), ab = ld_word(&sl->agg_b);
-            if (ia & ib & kValid) {
-              b[w] = from_words(ia, ib);
+            if (ia[w] & ib[w] & kValid) {
+              b[w] = from_words(ia[w], ib[w]);
               done[w] = true;
-            } else if (aa & ab & kValid) {
-              b[w] = from_words(aa, ab);
+            } else if (aa[w] & ab[w] & kValid) {
+              b[w] = from_words(aa[w], ab[w]);
               incl[w] = false;
               done[w] = true;
             } else {
@@ -261,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (all_done) break;
-          if (polls == 0) {
+          if (polls++ == 0) {
             start = global_ns();
           } else if ((int64_t)(global_ns() - start) >= wait_ns) {
             gave_up = true;  // treat what is missing as an empty inclusive prefix and finish
@@ -274,7 +286,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             break;
           }
-          if (++polls > 64) __nanosleep(64);
         }
         // nearest inclusive summary: lowest window, then lowest lane
         int stop_w = kPerLane, stop_l = 32;
@@ -286,12 +297,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             stop_l = __ffs(m) - 1;
           }
         }
-        // join from the farthest counted tile to the nearest one
-        Bounds span = none();
-        for (int w = (stop_w < kPerLane ? stop_w : kPerLane - 1); w >= 0; --w) {
-          const int top = w == stop_w ? stop_l : 31;
-          for (int L = top; L >= 0; --L) span = join(span, shfl(b[w], L));
+        // Join the counted tiles, farthest first.  Within a window a higher
+        // lane holds an earlier tile, so a shuffle-down tree leaves
+        // x_31 . x_30 . ... . x_0 in lane 0; tiles past the inclusive one
+        // count as empty.
+#pragma unroll
+        for (int w = 0; w < kPerLane; ++w) {
+          if (w > stop_w || (w == stop_w && lane > stop_l)) b[w] = none();
+#pragma unroll
+          for (int d = 1; d < 32; d <<= 1) {
+            const Bounds o = {__shfl_down_sync(~0u, b[w].count, d), __shfl_down_sync(~0u, b[w].first, d),
+                              __shfl_down_sync(~0u, b[w].last, d), __shfl_down_sync(~0u, b[w].gap, d)};
+            if (lane + d < 32) b[w] = join(o, b[w]);
+          }
         }
+        Bounds span = none();
+#pragma unroll
+        for (int w = kPerLane - 1; w >= 0; --w) span = join(span, shfl(b[w], 0));
         run = join(span, run);
         if (stop_w < kPerLane) break;
         j -= 32 * kPerLane;
@@ -306,9 +328,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_word(&mine_slot->inc_b, word_b(all));
       }
       s_prefix = prefix;
-      // this CTA reads no more summary words: count it finished (release
-      // orders the words above; the last one to arrive acquires them all)
-      s_last_cta = inc_acq_rel(&ws.hdr->finished, (unsigned)(tiles - 1)) == (unsigned)(tiles - 1);
     }
   }
 
@@ -324,6 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (tid == 0) {
     atomicOr(&ws.hdr->gave_up, 2u);  // only reachable from a workspace that was not zero-filled
   }
+  // This CTA reads no more summary words: count it finished once its stores
+  // are issued (release orders its words; the last arrival acquires them all).
+  if (tid == 0) s_last_cta = inc_acq_rel(&ws.hdr->finished, (unsigned)(tiles - 1)) == (unsigned)(tiles - 1);
+  __syncthreads();
   if (!s_last_cta) return;
 
   // ---- last CTA: close the array, report, and clear the summary words
