@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--profile-calls", action="store_true",
+                    help="issue every configuration's call (and the scaled squeeze and next-row calls) a few "
+                         "times, untimed, for a profiler to capture; prints no JSON line")
     return ap.parse_args()
 
 
@@ -452,6 +455,41 @@ def time_next_rows(dev, stream, seed: int, flush_l2, reps: int = 60) -> dict:
     return out
 
 
+def link_ceiling(dev, nbytes: int = 256 << 20) -> dict:
+    """Host<->device copy bandwidth of this machine from pinned memory: one
+    direction at a time, and both at once on two streams (best of 3)."""
+    import torch
+
+    h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    out = {}
+    for mode in ("h2d", "d2h", "both"):
+        times = []
+        for _ in range(4):
+            torch.cuda.synchronize(dev)
+            a, b, j = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                       torch.cuda.Event())
+            a.record(s1)
+            s2.wait_event(a)
+            if mode in ("h2d", "both"):
+                with torch.cuda.stream(s1):
+                    d_in.copy_(h_in, non_blocking=True)
+            if mode in ("d2h", "both"):
+                with torch.cuda.stream(s2):
+                    h_out.copy_(d_out, non_blocking=True)
+            j.record(s2)
+            s1.wait_event(j)
+            b.record(s1)
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b))
+        t = min(times[1:])
+        out[f"{mode}_gbs"] = round(nbytes * (2 if mode == "both" else 1) / (t / 1e3) / 1e9, 1)
+    return out
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "varlen_attention_metadata_gb300", "csrc")
@@ -474,7 +512,7 @@ def measured_peak():
 def profiled_traffic():
     """DRAM bytes per launch of the embedding conversion from the committed
     ncu summary, or None when the kernels changed since that capture."""
-    path = os.path.join(ROOT, "profiles", "thd_fused_bulk_embeddings.md")
+    path = os.path.join(ROOT, "profiles", "per_kernel_dram.md")
     try:
         with open(path) as f:
             text = f.read()
@@ -708,6 +746,7 @@ def run_native(args, dist: Dist):
     torch.cuda.synchronize(dev)
     pipe_ms = dist.max(p_ev[0].elapsed_time(p_ev[1]), dev) / Ke
 
+    link = link_ceiling(dev)
     next_rows = time_next_rows(dev, stream, args.seed + dist.rank, flush_l2) if dist.rank == 0 else None
 
     peak, peak_kind = measured_peak()
@@ -770,7 +809,11 @@ def run_native(args, dist: Dist):
                     "how": "every step copies all inputs in from pinned host memory and all outputs back; "
                            "steps pipelined over two buffer sets (copy-in, compute, copy-out streams)",
                     "serial": {"value": round(all_tokens / (serial_ms / 1e3), 1), "ms_per_step": round(serial_ms, 4),
-                               "how": "copy-in, compute, copy-out back to back on one stream"}},
+                               "how": "copy-in, compute, copy-out back to back on one stream"},
+                    "link": dict(link, frac_of_both=round((step.h2d_bytes + step.d2h_bytes) / (pipe_ms / 1e3) / 1e9
+                                                          / link["both_gbs"], 4),
+                                 how="pinned 256 MiB copies through torch (copy engines), best of 3; the pipelined "
+                                     "step's host bytes per second over the both-directions figure")},
             "next_rows": next_rows,
             "per_config": per_config,
             "gpu_launches": int(launches),
@@ -1106,8 +1149,41 @@ def run_reference(args, dist: Dist):
         dist.close()
 
 
+def profile_calls(args):
+    """The workload for a per-kernel profiler capture: two rounds of every
+    configuration's ABI call and the scaled squeeze, then six of each
+    next-row call.  Nothing is timed."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from varlen_attention_metadata_gb300 import build
+
+    build.build()
+    host = make_inputs(args.seed)
+    host["squeeze_scaled"] = synth.squeeze(args.seed, N=16384)
+    stream = torch.cuda.Stream(dev)
+    step = NativeStep(host, dev, stream)
+    scaled = NativeStep(host, dev, stream, host_pinned=step.pinned, only=("squeeze_scaled",))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for s in (step, scaled):
+                for name, fn, a in s.calls:
+                    st = fn(*a)
+                    if st != 0:
+                        raise RuntimeError(f"{name}: status {st}")
+    torch.cuda.synchronize(dev)
+    step.resolve()
+    scaled.resolve()
+    time_next_rows(dev, stream, args.seed, lambda: None, reps=1)
+    torch.cuda.synchronize(dev)
+
+
 def main():
     args = parse_args()
+    if args.profile_calls:
+        profile_calls(args)
+        return
     dist = Dist()
     if args.gpus > 1 and dist.world == 1:
         sys.exit("bench.py --gpus N > 1 must be launched with torchrun (one process per GPU)")
