@@ -371,6 +371,8 @@ def time_next_rows(dev, stream, seed: int, flush_l2, reps: int = 60) -> dict:
         keep.append(t)
         return t
 
+    graph_us = {}
+
     def timed(fn, args):
         ts = []
         with torch.cuda.stream(stream):
@@ -382,7 +384,13 @@ def time_next_rows(dev, stream, seed: int, flush_l2, reps: int = 60) -> dict:
                 b.record(stream)
                 ts.append((a, b))
         torch.cuda.synchronize(dev)
+        # back-to-back calls replayed from one CUDA graph: launch gaps removed
+        graph_us[id(fn)] = _graph_us([(fn, args)] * 20, dev, stream, flush_l2) / 20 if reps > 1 else None
         return statistics.median(x.elapsed_time(y) * 1e3 for x, y in ts[5:])
+
+    def g(fn):
+        v = graph_us.get(id(fn))
+        return round(v, 2) if v is not None else None
 
     out = {}
     # split_batch_into_thd_chunks: the B=8 S=8192 batch as 4 chunks of 2 rows
@@ -411,7 +419,8 @@ def time_next_rows(dev, stream, seed: int, flush_l2, reps: int = 60) -> dict:
     T = int(infos.view(nc, 4)[:, 3].sum().item())
     nbytes = 2 * T * 5 * 8 + T + 16 * B * Pk
     out["split_batch_into_thd_chunks"] = {"workload": "B=8 S=8192 ids/labels/mRoPE, 4 chunks", "us": round(us, 2),
-                                          "bytes": nbytes, "gbs": round(nbytes / us / 1e3, 1)}
+                                          "graph_us": g(lib.thd_chunks_from_batch), "bytes": nbytes,
+                                          "gbs": round(nbytes / us / 1e3, 1)}
     # thd_padding_mask_from_token_ids: a 2M-token id stream with a padded tail
     rng = np.random.default_rng(seed)
     n = 1 << 21
@@ -425,7 +434,8 @@ def time_next_rows(dev, stream, seed: int, flush_l2, reps: int = 60) -> dict:
     us = timed(lib.thd_mask_from_token_ids, (P(ids), 8, n, 0, P(tmask), P(tinfo), P(tws), tws.numel(), sh))
     nbytes = 9 * n
     out["thd_padding_mask_from_token_ids"] = {"workload": "int64 ids [2097152], 4096-token pad tail",
-                                              "us": round(us, 2), "bytes": nbytes, "gbs": round(nbytes / us / 1e3, 1)}
+                                              "us": round(us, 2), "graph_us": g(lib.thd_mask_from_token_ids),
+                                              "bytes": nbytes, "gbs": round(nbytes / us / 1e3, 1)}
     # first-fit-decreasing: the squeeze workload's 256 lengths at capacity 32768
     c3 = synth.squeeze(seed)
     lens = dev_t(c3["real_lens"])
@@ -436,7 +446,8 @@ def time_next_rows(dev, stream, seed: int, flush_l2, reps: int = 60) -> dict:
     us = timed(lib.pack_ffd, (P(lens), len(c3["real_lens"]), c3["multiple"], c3["capacity"], P(offs), P(mem),
                               P(finfo), sh))
     out["first_fit_decreasing"] = {"workload": "256 lengths, multiple 64, capacity 32768", "us": round(us, 2),
-                                   "bytes": 8 * 256 + 4 * 513, "bound": "latency (sequential first fit)"}
+                                   "graph_us": g(lib.pack_ffd), "bytes": 8 * 256 + 4 * 513,
+                                   "bound": "latency (sequential first fit)"}
     # doc_ids -> seq_lens bridge: the stress map [64, 32768]
     d4 = dev_t(synth.doc_map_stress(seed))
     Bm, Sm = d4.shape
@@ -451,7 +462,8 @@ def time_next_rows(dev, stream, seed: int, flush_l2, reps: int = 60) -> dict:
                                              bws.numel(), sh))
     nbytes = 4 * Bm * Sm + 8 * Bm * Sm + 2 * 8 * Bm * np_
     out["doc_ids_to_seq_lens"] = {"workload": "doc_ids [64,32768] -> seq_lens [64,8192] x2 + positions [64,32768]",
-                                  "us": round(us, 2), "bytes": nbytes, "gbs": round(nbytes / us / 1e3, 1)}
+                                  "us": round(us, 2), "graph_us": g(lib.pseq_doc_ids_to_lengths), "bytes": nbytes,
+                                  "gbs": round(nbytes / us / 1e3, 1)}
     return out
 
 

@@ -476,6 +476,25 @@ def test_squeeze_random(dtype):
         check_squeeze(prob, m, cap, stretch, width, pad_value=int(rng.integers(-5, 5)))
 
 
+@pytest.mark.parametrize("dtype", [np.int8, np.int16, np.int32, np.int64])
+@pytest.mark.parametrize("wide", [False, True])
+def test_squeeze_aligned_shapes(dtype, wide):
+    # row pitch, width and multiple on 16-byte boundaries: the 16-byte vector
+    # path (where the window holds whole vectors), with lengths that end
+    # inside a vector and zero-length members
+    eb = np.dtype(dtype).itemsize
+    V = 16 // eb
+    rng = np.random.default_rng(100 + eb + 10 * wide)
+    W = 16 * int(rng.integers(8, 40))
+    nb, N = (80, 640) if wide else (5, 60)
+    prob = synth.random_squeeze(rng, N, W, nb, elem_dtype=dtype)
+    for m in (V, 4 * V):
+        need = max(sum(-(-int(prob["real_lens"][i]) // m) * m for i in b) for b in prob["bins"])
+        width = -(-max(need, 13000 if wide else need + 1) // 16) * 16
+        check_squeeze(prob, m, width, True, width, pad_value=-2)
+        check_squeeze(prob, m, width + 16, False, width, pad_value=3)
+
+
 def test_squeeze_many_members():
     rng = np.random.default_rng(8)
     prob = synth.random_squeeze(rng, 1500, 40, 30)
