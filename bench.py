@@ -503,13 +503,14 @@ def link_ceiling(dev, nbytes: int = 256 << 20) -> dict:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources the roofline kernel (thd_fused_bulk_kernel) is
+    built from: its translation unit, the shared device header, the C ABI."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "varlen_attention_metadata_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
+    for path in (os.path.join(csrc, "thd.cu"), os.path.join(csrc, "common.cuh"),
+                 os.path.join(ROOT, "include", "pseq.h")):
+        with open(path, "rb") as fh:
             h.update(fh.read())
-    with open(os.path.join(ROOT, "include", "pseq.h"), "rb") as fh:
-        h.update(fh.read())
     return h.hexdigest()[:16]
 
 

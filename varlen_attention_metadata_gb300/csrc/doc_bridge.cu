@@ -67,8 +67,17 @@ struct BridgeArgs {
 template <typename Id>
 __device__ __forceinline__ Marks chunk_flags(const Id* d, int S, int s0, Id (&v)[kItems], Id& left, unsigned& runs,
                                              unsigned& seqs) {
+  if (s0 + kItems <= S && (reinterpret_cast<uintptr_t>(d + s0) & 15) == 0) {
+    // whole group in the row and 16-byte aligned: vector loads
+    constexpr int kVec = kItems * (int)sizeof(Id) / 16;
+    int4 q[kVec];
 #pragma unroll
-  for (int k = 0; k < kItems; ++k) v[k] = s0 + k < S ? __ldg(d + s0 + k) : Id(0);
+    for (int k = 0; k < kVec; ++k) q[k] = ld_stream(reinterpret_cast<const int4*>(d + s0) + k);
+    memcpy(v, q, sizeof(v));
+  } else {
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) v[k] = s0 + k < S ? __ldg(d + s0 + k) : Id(0);
+  }
   left = (s0 > 0 && s0 < S) ? __ldg(d + s0 - 1) : Id(0);
   runs = 0;
   seqs = 0;
@@ -170,16 +179,19 @@ __global__ void __launch_bounds__(kThreads) bridge_walk_kernel(const Id* __restr
   const Marks row_so_far = join(prefix, s_warp[kThreads / 32 - 1]);
   // walk this thread's tokens
   int last_run = before.last_run, last_seq = before.last_seq, count = before.seqs;
+  int longest = 0;
+  long long pos[kItems];
 #pragma unroll
   for (int k = 0; k < kItems; ++k) {
     const int s = s0 + k;
+    pos[k] = 0;
     if (s >= S) break;
     const Id prev = k ? v[k - 1] : left;
     if (runs & (1u << k)) {
       if (s > 0 && prev != 0) {  // the document run [last_run, s) ends here
         const int len = s - last_run;
         if (count - 1 < P) real_out[count - 1] = len;
-        atomicMax(&s_longest, len);
+        longest = max(longest, len);
       }
       last_run = s;
     }
@@ -193,8 +205,24 @@ __global__ void __launch_bounds__(kThreads) bridge_walk_kernel(const Id* __restr
       last_seq = s;
       count += 1;
     }
-    if (a.positions) a.positions[(int64_t)row * S + s] = v[k] != 0 ? s - last_run : 0;
+    pos[k] = v[k] != 0 ? s - last_run : 0;
   }
+  if (a.positions) {
+    int64_t* prow = a.positions + (int64_t)row * S;
+    if (s0 + kItems <= S && (reinterpret_cast<uintptr_t>(prow + s0) & 15) == 0) {
+#pragma unroll
+      for (int k = 0; k < kItems; k += 2)
+        st_stream(reinterpret_cast<int4*>(prow + s0 + k),
+                  make_int4((int)(uint32_t)pos[k], (int)(pos[k] >> 32), (int)(uint32_t)pos[k + 1],
+                            (int)(pos[k + 1] >> 32)));
+    } else {
+      for (int k = 0; k < kItems && s0 + k < S; ++k) prow[s0 + k] = pos[k];
+    }
+  }
+  // one shared atomic per warp for the longest document run
+#pragma unroll
+  for (int dd = 16; dd > 0; dd >>= 1) longest = max(longest, __shfl_xor_sync(~0u, longest, dd));
+  if (lane == 0 && longest) atomicMax(&s_longest, longest);
   const bool row_end = ch == a.chunks - 1;
   // the row's last chunk closes the last run and the last sequence
   if (row_end && tid == 0 && S > 0) {
