@@ -130,7 +130,7 @@ def test_ffd_examples():
     check_ffd(np.array([5, -1, 2]), 10)   # a negative length
 
 
-@pytest.mark.parametrize("n", [1, 33, 256, 1000, 4097, 8192])
+@pytest.mark.parametrize("n", [1, 2, 17, 31, 32, 33, 64, 256, 1000, 1024, 1025, 4097, 8192])
 def test_ffd_random(n):
     rng = np.random.default_rng(n)
     for multiple in (1, 64):

@@ -9,7 +9,7 @@
 // ascending bitonic sort in shared memory yields the visiting order.  First
 // fit is inherently sequential over items, so one warp walks them in order
 // with the open bins' remaining room held in registers across its lanes: one
-// ballot per 32 bins picks the first that fits.  Bins are numbered in the order
+// ballot per item picks the first that fits.  Bins are numbered in the order
 // they open, members keep their placement order, and a block scan of the bin
 // counts turns the placements into CSR arrays.
 #include "common.cuh"
@@ -66,20 +66,64 @@ __global__ void __launch_bounds__(kThreads)
   for (int d = 16; d > 0; d >>= 1) my_total += __shfl_xor_sync(~0u, my_total, d);
   if ((tid & 31) == 0 && my_total) atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), (unsigned long long)my_total);
   __syncthreads();
-  for (int width = 2; width <= pow2; width <<= 1) {
-    for (int stride = width >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < pow2; i += kThreads) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool up = (i & width) == 0;
-          const unsigned long long a = key[i], b = key[j];
-          if ((a > b) == up) {
-            key[i] = b;
-            key[j] = a;
-          }
+  if (n <= 256) {
+    // Rank sort: keys are distinct (the index is in the low word), so each
+    // key's rank is the number of smaller keys; one pass over the table per
+    // thread, reading broadcast from shared memory.
+    unsigned long long mine = tid < n ? key[tid] : 0ull;
+    int rank = 0;
+    if (tid < n) {
+#pragma unroll 4
+      for (int j = 0; j < n; ++j) rank += key[j] < mine ? 1 : 0;
+    }
+    __syncthreads();
+    if (tid < n) key[rank] = mine;
+    __syncthreads();
+  } else if (pow2 <= kThreads) {
+    // One key per thread, in registers: exchanges within a warp by shuffle,
+    // across warps through shared memory.  Whole warps take part (padding
+    // keys sort last), so every shuffle has its full warp.
+    const int span = pow2 < 32 ? 32 : pow2;
+    const bool in = tid < span;
+    unsigned long long k = tid < pow2 ? key[tid] : ~0ull;
+    for (int width = 2; width <= pow2; width <<= 1) {
+      for (int stride = width >> 1; stride > 0; stride >>= 1) {
+        unsigned long long other = 0;
+        if (stride >= 32) {
+          __syncthreads();  // the previous exchange has been read
+          if (in) key[tid] = k;
+          __syncthreads();
+          if (in) other = key[tid ^ stride];
+        } else if (in) {
+          other = __shfl_xor_sync(~0u, k, stride);
+        }
+        if (in) {
+          // ascending runs where (tid & width) == 0; the lower index of a
+          // pair keeps the smaller key of an ascending run
+          const bool take_min = ((tid & stride) == 0) == ((tid & width) == 0);
+          k = take_min ? (k < other ? k : other) : (k < other ? other : k);
         }
       }
-      __syncthreads();
+    }
+    __syncthreads();
+    if (tid < pow2) key[tid] = k;
+    __syncthreads();
+  } else {
+    for (int width = 2; width <= pow2; width <<= 1) {
+      for (int stride = width >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < pow2; i += kThreads) {
+          const int j = i ^ stride;
+          if (j > i) {
+            const bool up = (i & width) == 0;
+            const unsigned long long a = key[i], b = key[j];
+            if ((a > b) == up) {
+              key[i] = b;
+              key[j] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
     }
   }
   if (s_bad || s_big) {
@@ -89,123 +133,122 @@ __global__ void __launch_bounds__(kThreads)
   // sizes in visiting order, as int32 (room and count arrays are free yet)
   for (int k = tid; k < n; k += kThreads) bin_of[k] = INT32_MAX - (int)(key[k] >> 32);
   __syncthreads();
-  // first fit, one warp, items in visiting order.  The remaining room and
-  // member count of bin b live in register b / 32 of lane b % 32 for the first
-  // kRegBins * 32 bins (one ballot per 32 bins finds the first that fits), in
-  // shared memory beyond that.
+  // first fit, one warp, items in visiting order.  While at most 32 bins are
+  // open, bin b's remaining room and member count sit in lane b's registers
+  // and one ballot per item finds the first bin with room.  Beyond that, lane
+  // L holds bins [L*kRegBins, (L+1)*kRegBins): each lane tests its own bins,
+  // one ballot picks the first lane with a fit and that lane picks its first
+  // register; bins past 32*kRegBins live in shared memory.  The lane that owns
+  // the chosen bin records the placement itself, so no value crosses lanes
+  // after the ballot; sizes are read two items ahead.
   if (tid < 32) {
     constexpr int kRegBins = 8;
+    constexpr int kRegTotal = 32 * kRegBins;
     const int lane = tid;
+    int bins = 0;
+    int cur = n > 0 ? bin_of[0] : 0;
+    int nxt = n > 1 ? bin_of[1] : 0;
+    int k = 0;
+    int my_room = 0, my_cnt = 0;
+    for (; k < n; ++k) {
+      const int size = cur;
+      const unsigned fits = __ballot_sync(~0u, lane < bins && my_room >= size);
+      int chosen = __ffs(fits) - 1;
+      if (!fits) {
+        if (bins == 32) break;  // a 33rd bin: continue on the general path below
+        chosen = bins++;
+        if (lane == chosen) {
+          my_room = (int)capacity;
+          my_cnt = 0;
+        }
+      }
+      cur = nxt;
+      if (k + 2 < n) nxt = bin_of[k + 2];  // sizes still staged two items ahead
+      if (lane == chosen) {
+        my_room -= size;
+        slot_of[k] = my_cnt++;
+        bin_of[k] = chosen;  // its size was read already
+      }
+    }
+    // general layout: bin b in lane b / kRegBins, register b % kRegBins
     int room_r[kRegBins], count_r[kRegBins];
 #pragma unroll
     for (int r = 0; r < kRegBins; ++r) {
-      room_r[r] = 0;
-      count_r[r] = 0;
-    }
-    int bins = 0;
-    int next = n > 0 ? bin_of[0] : 0;
-    int k = 0;
-    // while at most 32 bins are open: one register per lane, one ballot per item
-    {
-      int room = 0, cnt = 0;
-      for (; k < n; ++k) {
-        const int size = next;
-        const unsigned fits = __ballot_sync(~0u, lane < bins && room >= size);
-        int chosen;
-        if (fits) {
-          chosen = __ffs(fits) - 1;
-        } else {
-          if (bins == 32) break;  // a 33rd bin: continue on the general path below
-          chosen = bins++;
-          if (lane == chosen) {
-            room = (int)capacity;
-            cnt = 0;
-          }
-        }
-        if (k + 1 < n) next = bin_of[k + 1];
-        int mine = 0;
-        if (lane == chosen) {
-          room -= size;
-          mine = cnt++;
-        }
-        const int slot = __shfl_sync(~0u, mine, chosen);
-        if (lane == 0) {
-          slot_of[k] = slot;
-          bin_of[k] = chosen;  // its size was read already; the look-ahead reads k + 1
-        }
-      }
-      room_r[0] = room;
-      count_r[0] = cnt;
+      const int b = lane * kRegBins + r;
+      const int from_room = __shfl_sync(~0u, my_room, b & 31), from_cnt = __shfl_sync(~0u, my_cnt, b & 31);
+      room_r[r] = b < bins ? from_room : 0;
+      count_r[r] = b < bins ? from_cnt : 0;
     }
     for (; k < n; ++k) {
-      const int size = next;
-      if (k + 1 < n) next = bin_of[k + 1];
-      const int groups = (min(bins, kRegBins * 32) + 31) >> 5;
-      int chosen = -1;
+      const int size = cur;
+      cur = nxt;
+      if (k + 2 < n) nxt = bin_of[k + 2];
+      bool any = false;
 #pragma unroll
-      for (int r = 0; r < kRegBins; ++r) {
-        if (r < groups && chosen < 0) {
-          const unsigned fits = __ballot_sync(~0u, r * 32 + lane < bins && room_r[r] >= size);
-          if (fits) chosen = r * 32 + __ffs(fits) - 1;
-        }
+      for (int r = 0; r < kRegBins; ++r) any |= lane * kRegBins + r < bins && room_r[r] >= size;
+      const unsigned lanes = __ballot_sync(~0u, any);
+      if (lanes) {
+        const bool owner = lane == __ffs(lanes) - 1;
+        int pick = kRegBins;
+#pragma unroll
+        for (int r = kRegBins - 1; r >= 0; --r)
+          if (lane * kRegBins + r < bins && room_r[r] >= size) pick = r;
+#pragma unroll
+        for (int r = 0; r < kRegBins; ++r)
+          if (owner && pick == r) {
+            room_r[r] -= size;
+            slot_of[k] = count_r[r]++;
+            bin_of[k] = lane * kRegBins + r;
+          }
+        continue;
       }
-      int slot = 0;
-      if (chosen < 0 && bins > kRegBins * 32) {  // bins that live in shared memory
-        for (int base = kRegBins * 32; chosen < 0 && base < bins; base += 32) {
-          const unsigned fits = __ballot_sync(~0u, base + lane < bins && room[base + lane] >= size);
-          if (fits) chosen = base + __ffs(fits) - 1;
+      int chosen = -1;
+      if (bins > kRegTotal) {  // bins that live in shared memory
+        for (int base = kRegTotal; chosen < 0 && base < bins; base += 32) {
+          const unsigned f = __ballot_sync(~0u, base + lane < bins && room[base + lane] >= size);
+          if (f) chosen = base + __ffs(f) - 1;
         }
         if (chosen >= 0) {
           __syncwarp();
           if (lane == 0) {
             room[chosen] -= size;
-            slot = count[chosen];
+            slot_of[k] = count[chosen];
             count[chosen] += 1;
-          }
-          slot = __shfl_sync(~0u, slot, 0);
-          __syncwarp();
-        }
-      }
-      if (chosen < 0) {  // open a new bin
-        chosen = bins;
-        bins += 1;
-        if (chosen >= kRegBins * 32) {
-          if (lane == 0) {
-            room[chosen] = (int32_t)capacity - size;
-            count[chosen] = 1;
+            bin_of[k] = chosen;
           }
           __syncwarp();
-        } else {
-#pragma unroll
-          for (int r = 0; r < kRegBins; ++r)
-            if (chosen == r * 32 + lane) {
-              room_r[r] = (int)capacity;
-              count_r[r] = 0;
-            }
+          continue;
         }
       }
-      if (chosen < kRegBins * 32) {
-        int mine = 0;
+      // open a new bin
+      chosen = bins;
+      bins += 1;
+      if (chosen >= kRegTotal) {
+        __syncwarp();
+        if (lane == 0) {
+          room[chosen] = (int32_t)capacity - size;
+          count[chosen] = 1;
+          slot_of[k] = 0;
+          bin_of[k] = chosen;
+        }
+        __syncwarp();
+      } else {
 #pragma unroll
         for (int r = 0; r < kRegBins; ++r)
-          if (chosen == r * 32 + lane) {
-            room_r[r] -= size;
-            mine = count_r[r];
-            count_r[r] += 1;
+          if (lane * kRegBins + r == chosen) {
+            room_r[r] = (int)capacity - size;
+            count_r[r] = 1;
+            slot_of[k] = 0;
+            bin_of[k] = chosen;
           }
-        slot = __shfl_sync(~0u, mine, chosen & 31);
-      }
-      if (lane == 0) {
-        slot_of[k] = slot;
-        bin_of[k] = chosen;  // its size was read already; the look-ahead reads k + 1
       }
     }
     __syncwarp();
 #pragma unroll
     for (int r = 0; r < kRegBins; ++r)
-      if (r * 32 + lane < bins) {
-        room[r * 32 + lane] = room_r[r];
-        count[r * 32 + lane] = count_r[r];
+      if (lane * kRegBins + r < bins && lane * kRegBins + r < kRegTotal) {
+        room[lane * kRegBins + r] = room_r[r];
+        count[lane * kRegBins + r] = count_r[r];
       }
     if (lane == 0) s_bins = bins;
   }
