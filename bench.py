@@ -299,15 +299,20 @@ class NativeStep:
                 continue
             if emb_events is not None:
                 emb_events[0].record(emb)
-            fn(*(self.emb_side_args if two else args))
+            self._ok(name, fn(*(self.emb_side_args if two else args)))
             if emb_events is not None:
                 emb_events[1].record(emb)
         for name, fn, args in self.calls:
             if name != "thd_emb":
-                fn(*args)
+                self._ok(name, fn(*args))
         if two:
             self._join.record(self.side)
             self.stream.wait_event(self._join)
+
+    def _ok(self, name, status):
+        # a call that enqueued nothing must not pass for a fast one
+        if status != 0:
+            raise RuntimeError(f"{name}: status {status}: {self.v.load_library().pseq_last_error().decode()}")
 
     def resolve(self):
         """After one untimed step: exact token counts, output sizes, checks."""
@@ -380,8 +385,10 @@ def time_next_rows(dev, stream, seed: int, flush_l2, reps: int = 60) -> dict:
                 flush_l2()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                fn(*args)
+                st = fn(*args)
                 b.record(stream)
+                if st != 0:
+                    raise RuntimeError(f"next-row call: status {st}")
                 ts.append((a, b))
         torch.cuda.synchronize(dev)
         # back-to-back calls replayed from one CUDA graph: launch gaps removed
@@ -913,8 +920,10 @@ def time_per_config(step, host, dev, stream, flush_l2, peak, warm=20, reps=200) 
                 flush_l2()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                fn(*args)
+                st = fn(*args)
                 b.record(stream)
+                if st != 0:
+                    raise RuntimeError(f"{name}: status {st}")
                 if i >= warm:
                     ts.append((a, b))
         torch.cuda.synchronize(dev)
