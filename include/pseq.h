@@ -65,10 +65,11 @@ const char* pseq_last_error(void);
 int64_t pseq_launch_count(void);
 
 /* Bounded-wait controls, for failure-detection tests.  spin_limit_ns caps
- * every device-side wait of pseq_from_doc_ids (default 1e9 ns); when
- * withhold_tile >= 0 that tile never publishes its partial result, so the
- * tiles after it run into the cap and report PSEQ_ERR_TIMEOUT.  Process-wide;
- * pass (-1, -1) to restore the defaults. */
+ * every device-side wait of pseq_from_doc_ids and pseq_doc_ids_to_lengths
+ * (default 1e9 ns); when withhold_tile >= 0 that scan tile (or bridge chunk,
+ * counted row-major over rows and 4096-token chunks) never publishes its
+ * partial result, so the ones after it run into the cap and report
+ * PSEQ_ERR_TIMEOUT.  Process-wide; pass (-1, -1) to restore the defaults. */
 void pseq_debug_set_wait(int64_t spin_limit_ns, int64_t withhold_tile);
 
 /* ------------------------------------------------------------------------
@@ -292,8 +293,10 @@ pseq_status pack_ffd(const int64_t* lens, int64_t n, int64_t multiple,
  * Device errors: PSEQ_ERR_CAPACITY when a row holds more than num_packs
  *   sequences (the slots that fit are written).
  * workspace: pseq_doc_ids_to_lengths_workspace_size(B, S) bytes, 16-byte
- *   aligned (per-chunk scratch; no initial contents needed).  At most 65535
- *   rows per call.
+ *   aligned, ZERO-FILLED before its first use; every call leaves it zero
+ *   again (calls sharing one must be ordered).  At most 65535 rows per call.
+ * Device errors also include PSEQ_ERR_TIMEOUT (a chunk's wait for the chunks
+ *   before it in its row hit the cap set by pseq_debug_set_wait).
  * ---------------------------------------------------------------------- */
 size_t pseq_doc_ids_to_lengths_workspace_size(int64_t B, int64_t S);
 pseq_status pseq_doc_ids_to_lengths(const void* doc_ids, int32_t id_bytes,

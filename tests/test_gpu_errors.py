@@ -49,6 +49,29 @@ def test_lookback_wait_gives_up_and_reports():
     assert p.max_seqlen == ref_mx
 
 
+def test_bridge_wait_gives_up_and_reports():
+    import varlen_attention_metadata_gb300 as v
+
+    lib = v.load_library()
+    rng = np.random.default_rng(1)
+    d = synth.random_doc_ids(rng, 2, 4 * 4096, "runs", np.int32)  # 2 rows of 4 chunks
+    dt = torch.from_numpy(d).to(DEV)
+    try:
+        lib.pseq_debug_set_wait(1_000_000, 5)  # row 1, chunk 1 never publishes
+        _, _, _, info = v.pseq_doc_ids_to_lengths(dt, 4 * 4096)
+        assert info[:16].view(torch.int32).tolist()[0] == v._lib.PSEQ_ERR_TIMEOUT
+    finally:
+        lib.pseq_debug_set_wait(-1, -1)
+    torch.cuda.synchronize()
+    # the workspace is clean again: the next call is exact
+    real, padded, pos, info = v.pseq_doc_ids_to_lengths(dt, 4 * 4096)
+    ref = oracle.doc_ids_to_lengths(d, 4 * 4096)
+    assert info[:16].view(torch.int32).tolist()[0] == 0
+    np.testing.assert_array_equal(real.cpu().numpy(), ref["seq_lens"])
+    np.testing.assert_array_equal(padded.cpu().numpy(), ref["seq_lens_padded"])
+    np.testing.assert_array_equal(pos.cpu().numpy(), ref["position_ids"])
+
+
 def test_host_side_errors_launch_nothing():
     import varlen_attention_metadata_gb300 as v
 

@@ -185,6 +185,14 @@ def test_bridge_random(kind):
     check_bridge(d, 4)  # rows hold more sequences than slots
 
 
+def test_bridge_long_rows():
+    # rows of 35 and 49 chunks: the look-back takes more than one round of 32
+    rng = np.random.default_rng(41)
+    for S, kind in ((140_001, "runs"), (200_000, "long"), (200_000, "runs")):
+        d = synth.random_doc_ids(rng, 2, S, kind, np.int32)
+        check_bridge(d, S)
+
+
 def test_bridge_workloads():
     check_bridge(synth.doc_map_small(0)["doc_ids"], 64)
     check_bridge(synth.doc_map_stress(0), 8192)

@@ -90,7 +90,7 @@ class _WorkspaceCache:
     per-call scratch.
     """
 
-    ZEROED = ("scan", "token_mask", "squeeze")
+    ZEROED = ("scan", "token_mask", "squeeze", "bridge")
 
     def __init__(self):
         self._bufs: dict = {}

@@ -63,6 +63,17 @@ __device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Relaxed 64-bit accesses at GPU scope, for self-validating summary words
+// that other CTAs poll.
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // Wrapping counter of finished CTAs (acq_rel): returns the old value; the
 // value after `limit` is 0, so the last of limit+1 arrivals leaves it zero.
 __device__ __forceinline__ unsigned inc_acq_rel(unsigned* p, unsigned limit) {

@@ -12,29 +12,54 @@
 // row is a sequence of real length 0.  Positions count 0, 1, ... inside each
 // document run and are 0 on padding.
 //
-// Every row is cut into chunks of 4096 tokens, one CTA each, in two
-// launches.  The first summarises every chunk: how many sequences start in
-// it, its last run start and its last sequence start (a commutative join:
-// sum, max, max).  The second gives each chunk its row prefix by joining the
-// summaries of the chunks before it -- no waiting, they are all done -- and
-// walks its tokens with a block scan: every run end writes its sequence's
-// real length, every sequence start closes the padded length of the one
-// before it, and the row's last chunk closes the row and fills unused slots.
-// Row statistics reach the info block through atomics (the first launch
-// initialises it).
+// One pass.  Every row is cut into chunks of 4096 tokens, one CTA each.  A
+// chunk summarises its tokens -- how many sequences start in it, its last run
+// start, its last sequence start (a commutative join: sum, max, max) -- with
+// a block scan, publishes that summary, and looks back over the chunks
+// before it in its row for the row prefix (self-validating words, 32
+// predecessors per poll round, stopping at the nearest inclusive prefix,
+// bounded waits).  It then walks its tokens: every run end writes its
+// sequence's real length, every sequence start closes the padded length of
+// the one before it, and the row's last chunk closes the row and fills unused
+// slots.  Each chunk writes its own statistics record; the CTA that finishes
+// last (a wrapping acq_rel counter) folds the records into the info block
+// and clears the summary words, so the workspace is zero again for the next
+// call.
 #include "common.cuh"
 
 namespace pseq {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kItems = 8;
+constexpr int kThreads = 256;
+constexpr int kItems = 16;  // 4096-token chunks; four CTAs per SM, so one wave covers a [64, 32768] map
 constexpr int kTile = kThreads * kItems;
+
+struct Header {
+  unsigned finished;  // CTAs done with their look-back; wraps back to 0 after each call
+  unsigned gave_up;   // a wait hit its time limit
+  unsigned pad[30];
+};
+
+// Per chunk, written by its own CTA every call and folded by the last one:
+// longest document run ending in the chunk, whether the row overflowed its
+// slots there, and (for a row's last chunk) the row's sequence count.
+struct Stat {
+  int longest, overflow, row_seqs, row_end;
+};
+static_assert(sizeof(Header) == 128, "header is 128 bytes");
+
+// Per chunk: its own summary and the inclusive one (the row up to it), each
+// as two words carrying a valid bit.
+struct Slot {
+  unsigned long long agg_a, agg_b, inc_a, inc_b;
+};
 
 size_t workspace_bytes(int64_t B, int64_t S) {
   const int64_t chunks = S > 0 ? (S + kTile - 1) / kTile : 1;
-  return 16 * (size_t)(B > 0 ? B : 1) * (size_t)chunks;
+  return sizeof(Header) + (sizeof(Slot) + sizeof(Stat)) * (size_t)(B > 0 ? B : 1) * (size_t)chunks;
 }
+
+constexpr unsigned long long kValid = 1ull << 63;
 
 // Scan element: sequence starts counted, last run start, last sequence start.
 struct Marks {
@@ -53,6 +78,16 @@ __device__ __forceinline__ Marks shfl_xor(const Marks& v, int d) {
   return {__shfl_xor_sync(~0u, v.seqs, d), __shfl_xor_sync(~0u, v.last_run, d), __shfl_xor_sync(~0u, v.last_seq, d)};
 }
 
+// {valid, seqs, last_run} and {valid, last_seq}; positions -1 ("none") round-
+// trip through the unsigned low word.
+__device__ __forceinline__ unsigned long long word_a(const Marks& m) {
+  return kValid | ((unsigned long long)(unsigned)m.seqs << 32) | (unsigned)m.last_run;
+}
+__device__ __forceinline__ unsigned long long word_b(const Marks& m) { return kValid | (unsigned)m.last_seq; }
+__device__ __forceinline__ Marks from_words(unsigned long long a, unsigned long long b) {
+  return {(int)((a >> 32) & 0x7fffffffu), (int)(unsigned)a, (int)(unsigned)b};
+}
+
 struct BridgeArgs {
   int B, S, P, chunks;
   int64_t pad_value;
@@ -60,33 +95,50 @@ struct BridgeArgs {
   int64_t* seq_lens_padded;
   int64_t* positions;  // may be NULL
   pseq_info* info;
-  int4* marks;         // [B * chunks]
+  Header* hdr;
+  Slot* slots;         // [B * chunks]
+  Stat* stats;         // [B * chunks]
+  int64_t wait_ns;
+  int64_t withhold;    // chunk (row-major) that never publishes: failure tests only
 };
 
 // This thread's eight tokens of a row chunk: run starts, sequence starts.
 template <typename Id>
-__device__ __forceinline__ Marks chunk_flags(const Id* d, int S, int s0, Id (&v)[kItems], Id& left, unsigned& runs,
-                                             unsigned& seqs) {
+__device__ __forceinline__ Marks chunk_flags(const Id* d, int S, int s0, unsigned& runs, unsigned& seqs,
+                                             unsigned& nz, unsigned& pnz) {
+  Id v[kItems];
   if (s0 + kItems <= S && (reinterpret_cast<uintptr_t>(d + s0) & 15) == 0) {
     // whole group in the row and 16-byte aligned: vector loads
     constexpr int kVec = kItems * (int)sizeof(Id) / 16;
-    int4 q[kVec];
+    constexpr int kPer = 16 / (int)sizeof(Id);
 #pragma unroll
-    for (int k = 0; k < kVec; ++k) q[k] = ld_stream(reinterpret_cast<const int4*>(d + s0) + k);
-    memcpy(v, q, sizeof(v));
+    for (int k = 0; k < kVec; ++k) {
+      const int4 q = ld_stream(reinterpret_cast<const int4*>(d + s0) + k);
+      if constexpr (kPer == 4) {
+        v[4 * k] = (Id)q.x;
+        v[4 * k + 1] = (Id)q.y;
+        v[4 * k + 2] = (Id)q.z;
+        v[4 * k + 3] = (Id)q.w;
+      } else {
+        v[2 * k] = (Id)(((unsigned long long)(unsigned)q.y << 32) | (unsigned)q.x);
+        v[2 * k + 1] = (Id)(((unsigned long long)(unsigned)q.w << 32) | (unsigned)q.z);
+      }
+    }
   } else {
 #pragma unroll
     for (int k = 0; k < kItems; ++k) v[k] = s0 + k < S ? __ldg(d + s0 + k) : Id(0);
   }
-  left = (s0 > 0 && s0 < S) ? __ldg(d + s0 - 1) : Id(0);
+  const Id left = (s0 > 0 && s0 < S) ? __ldg(d + s0 - 1) : Id(0);
   runs = 0;
   seqs = 0;
+  nz = 0;
   Marks mine = {0, -1, -1};
 #pragma unroll
   for (int k = 0; k < kItems; ++k) {
     const int s = s0 + k;
     if (s >= S) break;
     const Id prev = k ? v[k - 1] : left;
+    if (v[k] != 0) nz |= 1u << k;
     if (s == 0 || v[k] != prev) {
       runs |= 1u << k;
       mine.last_run = s;
@@ -97,35 +149,100 @@ __device__ __forceinline__ Marks chunk_flags(const Id* d, int S, int s0, Id (&v)
       mine.seqs += 1;
     }
   }
+  // bit k: the token before token k is a document token
+  pnz = (nz << 1) | (left != 0 ? 1u : 0u);
   return mine;
 }
 
-template <typename Id>
-__global__ void __launch_bounds__(kThreads) bridge_summary_kernel(const Id* __restrict__ doc, BridgeArgs a) {
-  __shared__ Marks s_warp[kThreads / 32];
-  pdl_enter();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = blockIdx.y, ch = blockIdx.x;
-  if (row == 0 && ch == 0 && tid == 0) *a.info = {PSEQ_OK, 0, 0, 0};
-  Id v[kItems], left;
-  unsigned runs, seqs;
-  Marks m = chunk_flags(doc + (int64_t)row * a.S, a.S, ch * kTile + tid * kItems, v, left, runs, seqs);
+// The row prefix of chunk `ch`: join of every earlier chunk of the row,
+// looking back in rounds of 32 (lane L polls chunk j - L) and stopping at the
+// nearest inclusive summary.  Warp 0 only.
+__device__ __forceinline__ Marks row_prefix(const BridgeArgs& a, const Slot* row_slots, int ch, bool& gave_up) {
+  const int lane = threadIdx.x & 31;
+  Marks run = {0, -1, -1};
+  int j = ch - 1;
+  while (j >= 0) {
+    const int t = j - lane;
+    bool done = t < 0, incl = true;
+    Marks m = {0, -1, -1};
+    // each lane polls its own chunk until it has a summary or its wait runs
+    // out; no warp-wide operation inside the loop
+    int polls = 0;
+    uint64_t start = 0;
+    while (!done) {
+      const Slot* sl = row_slots + t;
+      const unsigned long long ia = ld_relaxed_u64(&sl->inc_a), ib = ld_relaxed_u64(&sl->inc_b);
+      const unsigned long long aa = ld_relaxed_u64(&sl->agg_a), ab = ld_relaxed_u64(&sl->agg_b);
+      if (ia & ib & kValid) {
+        m = from_words(ia, ib);
+        done = true;
+      } else if (aa & ab & kValid) {
+        m = from_words(aa, ab);
+        incl = false;
+        done = true;
+      } else if (polls++ == 0) {
+        start = global_ns();
+      } else if ((int64_t)(global_ns() - start) >= a.wait_ns) {
+        gave_up = true;  // count what is missing as an empty inclusive prefix and finish
+        break;
+      }
+    }
+    gave_up = __any_sync(~0u, gave_up);
+    // nearest inclusive summary: the lowest lane that has one
+    const unsigned inc_lanes = __ballot_sync(~0u, incl && t >= 0);
+    const int stop = inc_lanes ? __ffs(inc_lanes) - 1 : 32;
+    if (lane > stop || t < 0) m = {0, -1, -1};
 #pragma unroll
-  for (int d = 16; d > 0; d >>= 1) m = join(m, shfl_xor(m, d));
-  if (lane == 0) s_warp[warp] = m;
+    for (int d = 16; d > 0; d >>= 1) m = join(m, shfl_xor(m, d));
+    run = join(run, m);
+    if (inc_lanes || gave_up) break;
+    j -= 32;
+  }
+  return run;
+}
+
+// The last CTA: fold every chunk's record into the info block.
+__device__ __noinline__ void fold_stats(const BridgeArgs& a) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  __shared__ int f_longest, f_overflow, f_most, f_total;
+  if (tid == 0) f_longest = f_overflow = f_most = f_total = 0;
+  __syncthreads();
+  int lng = 0, over = 0, most = 0, total = 0;
+  const int64_t n = (int64_t)a.B * a.chunks;
+  for (int64_t i = tid; i < n; i += kThreads) {
+    // L2 loads: the records were released by the counter that thread 0 acquired
+    const int4 r = __ldcg(reinterpret_cast<const int4*>(a.stats + i));
+    lng = max(lng, r.x);
+    over |= r.y;
+    most = max(most, r.z);
+    total += r.z;
+  }
+#pragma unroll
+  for (int dd = 16; dd > 0; dd >>= 1) {
+    lng = max(lng, __shfl_xor_sync(~0u, lng, dd));
+    over |= __shfl_xor_sync(~0u, over, dd);
+    most = max(most, __shfl_xor_sync(~0u, most, dd));
+    total += __shfl_xor_sync(~0u, total, dd);
+  }
+  if (lane == 0) {
+    atomicMax(&f_longest, lng);
+    atomicOr(&f_overflow, over);
+    atomicMax(&f_most, most);
+    atomicAdd(&f_total, total);
+  }
   __syncthreads();
   if (tid == 0) {
-    Marks t = s_warp[0];
-    for (int w = 1; w < kThreads / 32; ++w) t = join(t, s_warp[w]);
-    a.marks[(int64_t)row * a.chunks + ch] = make_int4(t.seqs, t.last_run, t.last_seq, 0);
+    const unsigned failed = atomicExch(&a.hdr->gave_up, 0u);
+    const int status = failed ? PSEQ_ERR_TIMEOUT : (f_overflow ? PSEQ_ERR_CAPACITY : PSEQ_OK);
+    *a.info = pseq_info{status, f_most, f_longest, f_total};
   }
 }
 
 template <typename Id>
-__global__ void __launch_bounds__(kThreads) bridge_walk_kernel(const Id* __restrict__ doc, BridgeArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restrict__ doc, const __grid_constant__ BridgeArgs a) {
   __shared__ Marks s_warp[kThreads / 32];
   __shared__ Marks s_prefix;
-  __shared__ int s_longest, s_overflow;
+  __shared__ int s_longest, s_overflow, s_last;
   pdl_enter();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.y, ch = blockIdx.x;
@@ -133,25 +250,13 @@ __global__ void __launch_bounds__(kThreads) bridge_walk_kernel(const Id* __restr
   const Id* d = doc + (int64_t)row * S;
   int64_t* real_out = a.seq_lens + (int64_t)row * P;
   int64_t* pad_out = a.seq_lens_padded + (int64_t)row * P;
-  // the row prefix: every earlier chunk's summary (all written by the first launch)
-  if (warp == 0) {
-    Marks pre = {0, -1, -1};
-    for (int c = lane; c < ch; c += 32) {
-      const int4 q = __ldcg(a.marks + (int64_t)row * a.chunks + c);
-      pre = join(pre, Marks{q.x, q.y, q.z});
-    }
-#pragma unroll
-    for (int dd = 16; dd > 0; dd >>= 1) pre = join(pre, shfl_xor(pre, dd));
-    if (lane == 0) {
-      s_prefix = pre;
-      s_longest = 0;
-      s_overflow = 0;
-    }
+  if (tid == 0) {
+    s_longest = 0;
+    s_overflow = 0;
   }
-  Id v[kItems], left;
-  unsigned runs, seqs;
+  unsigned runs, seqs, nz, pnz;
   const int s0 = ch * kTile + tid * kItems;
-  const Marks mine = chunk_flags(d, S, s0, v, left, runs, seqs);
+  const Marks mine = chunk_flags(d, S, s0, runs, seqs, nz, pnz);
   // exclusive block scan of the marks, in token order
   Marks inc = mine;
 #pragma unroll
@@ -171,52 +276,84 @@ __global__ void __launch_bounds__(kThreads) bridge_walk_kernel(const Id* __restr
     if (lane < kThreads / 32) s_warp[lane] = w;
   }
   __syncthreads();
+  const Marks chunk_sum = s_warp[kThreads / 32 - 1];
+  // publish this chunk's summary, then the row prefix from the chunks before it
+  if (warp == 0) {
+    Slot* row_slots = a.slots + (int64_t)row * a.chunks;
+    const int64_t linear = (int64_t)row * a.chunks + ch;
+    const bool publish = a.chunks > 1 && linear != a.withhold;
+    Marks prefix = {0, -1, -1};
+    if (ch > 0) {
+      if (lane == 0 && publish) {
+        st_relaxed_u64(&row_slots[ch].agg_a, word_a(chunk_sum));
+        st_relaxed_u64(&row_slots[ch].agg_b, word_b(chunk_sum));
+      }
+      bool gave_up = false;
+      prefix = row_prefix(a, row_slots, ch, gave_up);
+      if (gave_up && lane == 0) atomicOr(&a.hdr->gave_up, 1u);
+    }
+    if (lane == 0) {
+      if (publish) {
+        const Marks all = join(prefix, chunk_sum);
+        st_relaxed_u64(&row_slots[ch].inc_a, word_a(all));
+        st_relaxed_u64(&row_slots[ch].inc_b, word_b(all));
+      }
+      s_prefix = prefix;
+    }
+  }
   Marks before = shfl_up(inc, 1);
   if (lane == 0) before = {0, -1, -1};
   if (warp > 0) before = join(s_warp[warp - 1], before);
+  __syncthreads();
   const Marks prefix = s_prefix;
   before = join(prefix, before);
-  const Marks row_so_far = join(prefix, s_warp[kThreads / 32 - 1]);
-  // walk this thread's tokens
+  const Marks row_so_far = join(prefix, chunk_sum);
+  // walk this thread's run and sequence starts, in token order
   int last_run = before.last_run, last_seq = before.last_seq, count = before.seqs;
   int longest = 0;
-  long long pos[kItems];
-#pragma unroll
-  for (int k = 0; k < kItems; ++k) {
+  for (unsigned ev = runs | seqs; ev; ev &= ev - 1) {
+    const int k = __ffs(ev) - 1;
+    const unsigned bit = 1u << k;
     const int s = s0 + k;
-    pos[k] = 0;
-    if (s >= S) break;
-    const Id prev = k ? v[k - 1] : left;
-    if (runs & (1u << k)) {
-      if (s > 0 && prev != 0) {  // the document run [last_run, s) ends here
+    if (runs & bit) {
+      if (s > 0 && (pnz & bit)) {  // the document run [last_run, s) ends here
         const int len = s - last_run;
         if (count - 1 < P) real_out[count - 1] = len;
         longest = max(longest, len);
       }
       last_run = s;
     }
-    if (seqs & (1u << k)) {
+    if (seqs & bit) {
       if (count > 0 && count - 1 < P) pad_out[count - 1] = s - last_seq;
       if (count < P) {
-        if (v[k] == 0) real_out[count] = 0;  // padding before any document
+        if (!(nz & bit)) real_out[count] = 0;  // padding before any document
       } else {
         s_overflow = 1;
       }
       last_seq = s;
       count += 1;
     }
-    pos[k] = v[k] != 0 ? s - last_run : 0;
   }
+  // positions: count from the latest run start, two per 16-byte store
   if (a.positions) {
     int64_t* prow = a.positions + (int64_t)row * S;
+    int lr = before.last_run;
     if (s0 + kItems <= S && (reinterpret_cast<uintptr_t>(prow + s0) & 15) == 0) {
 #pragma unroll
-      for (int k = 0; k < kItems; k += 2)
-        st_stream(reinterpret_cast<int4*>(prow + s0 + k),
-                  make_int4((int)(uint32_t)pos[k], (int)(pos[k] >> 32), (int)(uint32_t)pos[k + 1],
-                            (int)(pos[k + 1] >> 32)));
+      for (int k = 0; k < kItems; k += 2) {
+        if (runs & (1u << k)) lr = s0 + k;
+        const int p0 = (nz >> k) & 1u ? s0 + k - lr : 0;
+        if (runs & (2u << k)) lr = s0 + k + 1;
+        const int p1 = (nz >> (k + 1)) & 1u ? s0 + k + 1 - lr : 0;
+        st_stream(reinterpret_cast<int4*>(prow + s0 + k), make_int4(p0, 0, p1, 0));
+      }
     } else {
-      for (int k = 0; k < kItems && s0 + k < S; ++k) prow[s0 + k] = pos[k];
+#pragma unroll
+      for (int k = 0; k < kItems; ++k) {
+        if (s0 + k >= S) break;
+        if (runs & (1u << k)) lr = s0 + k;
+        prow[s0 + k] = (nz >> k) & 1u ? s0 + k - lr : 0;
+      }
     }
   }
   // one shared atomic per warp for the longest document run
@@ -234,19 +371,27 @@ __global__ void __launch_bounds__(kThreads) bridge_walk_kernel(const Id* __restr
     if (total - 1 < P) pad_out[total - 1] = S - row_so_far.last_seq;
   }
   if (row_end) {
-    for (int k = min(row_so_far.seqs, P) + tid; k < P; k += kThreads) {
-      real_out[k] = a.pad_value;
-      pad_out[k] = a.pad_value;
-    }
+    const int used = min(row_so_far.seqs, P);
+    block_fill(real_out + used, P - used, 8, a.pad_value);
+    block_fill(pad_out + used, P - used, 8, a.pad_value);
   }
   __syncthreads();
+  const int64_t linear = (int64_t)row * a.chunks + ch;
   if (tid == 0) {
-    if (s_longest) atomicMax(&a.info->max_seqlen, s_longest);
-    if (s_overflow) atomicMax(&a.info->status, (int)PSEQ_ERR_CAPACITY);
-    if (row_end) {
-      atomicMax(&a.info->count, row_so_far.seqs);
-      atomicAdd(&a.info->total, row_so_far.seqs);
-    }
+    a.stats[linear] = Stat{s_longest, s_overflow, row_end ? row_so_far.seqs : 0, row_end ? 1 : 0};
+    // this CTA reads no more summary words and has written its record
+    // (release); the last one to arrive acquires them all
+    const unsigned ctas = gridDim.x * gridDim.y;
+    s_last = inc_acq_rel(&a.hdr->finished, ctas - 1u) == ctas - 1u;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // ---- last CTA: fold the records, report, leave the workspace zero
+  fold_stats(a);
+  if (a.chunks > 1) {
+    unsigned long long* words = reinterpret_cast<unsigned long long*>(a.slots);
+    const int64_t n = 4 * (int64_t)a.B * a.chunks;
+    for (int64_t i = tid; i < n; i += kThreads) words[i] = 0ull;
   }
 }
 
@@ -314,18 +459,16 @@ extern "C" pseq_status pseq_doc_ids_to_lengths(const void* doc_ids, int32_t id_b
     if (!workspace || workspace_bytes_ < need || !aligned(workspace, 16))
       return fail(PSEQ_ERR_ARG, "%s: workspace needs %zu bytes, 16-byte aligned (got %zu)", fn, need,
                   workspace_bytes_);
-    a.marks = static_cast<int4*>(workspace);
+    a.hdr = static_cast<Header*>(workspace);
+    a.slots = reinterpret_cast<Slot*>(static_cast<unsigned char*>(workspace) + sizeof(Header));
+    a.stats = reinterpret_cast<Stat*>(a.slots + (int64_t)B * a.chunks);
+    a.wait_ns = wait_limit_ns();
+    a.withhold = withhold_tile();
     const dim3 grid((unsigned)a.chunks, (unsigned)B);
-    if (id_bytes == 4) {
-      const int32_t* d = static_cast<const int32_t*>(doc_ids);
-      e = launch_pdl(bridge_summary_kernel<int32_t>, grid, dim3(kThreads), 0, st, d, a);
-      if (e == cudaSuccess) e = launch_pdl(bridge_walk_kernel<int32_t>, grid, dim3(kThreads), 0, st, d, a);
-    } else {
-      const int64_t* d = static_cast<const int64_t*>(doc_ids);
-      e = launch_pdl(bridge_summary_kernel<int64_t>, grid, dim3(kThreads), 0, st, d, a);
-      if (e == cudaSuccess) e = launch_pdl(bridge_walk_kernel<int64_t>, grid, dim3(kThreads), 0, st, d, a);
-    }
-    launches = 2;
+    e = id_bytes == 4 ? launch_pdl(bridge_kernel<int32_t>, grid, dim3(kThreads), 0, st,
+                                   static_cast<const int32_t*>(doc_ids), a)
+                      : launch_pdl(bridge_kernel<int64_t>, grid, dim3(kThreads), 0, st,
+                                   static_cast<const int64_t*>(doc_ids), a);
   }
   count_launches(launches);
   if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));

@@ -88,15 +88,6 @@ __device__ __forceinline__ Bounds from_words(unsigned long long a, unsigned long
   return {(int)((a >> 32) & 0x7fffffffu), (int)(unsigned)b, (int)(unsigned)a, (int)((b >> 32) & 0x7fffffffu)};
 }
 
-__device__ __forceinline__ unsigned long long ld_word(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_word(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-// Increment that wraps back to 0 after `limit`, with acquire-release order.
 struct Header {
   unsigned int finished;  // tiles done with their look-back; wraps back to 0 after each call
   unsigned int gave_up;   // nonzero when some wait hit its time limit
@@ -222,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bounds prefix = none();
     if (tile > 0) {
       if (lane == 0 && withhold != tile) {
-        st_word(&mine_slot->agg_a, word_a(tile_sum));
-        st_word(&mine_slot->agg_b, word_b(tile_sum));
+        st_relaxed_u64(&mine_slot->agg_a, word_a(tile_sum));
+        st_relaxed_u64(&mine_slot->agg_b, word_b(tile_sum));
       }
       // Each round polls kPerLane windows of 32 predecessors at once (lane L
       // of window w looks at tile j - 32w - L), waits until every one has
@@ -251,10 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ia[w] = ib[w] = aa[w] = ab[w] = 0ull;
             if (!done[w]) {
               const Slot* sl = ws.slots + (j - 32 * w - lane);
-              ia[w] = ld_word(&sl->inc_a);
-              ib[w] = ld_word(&sl->inc_b);
-              aa[w] = ld_word(&sl->agg_a);
-              ab[w] = ld_word(&sl->agg_b);
+              ia[w] = ld_relaxed_u64(&sl->inc_a);
+              ib[w] = ld_relaxed_u64(&sl->inc_b);
+              aa[w] = ld_relaxed_u64(&sl->agg_a);
+              ab[w] = ld_relaxed_u64(&sl->agg_b);
             }
           }
           bool all_done = true;
@@ -324,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       if (withhold != tile) {
         const Bounds all = join(prefix, tile_sum);
-        st_word(&mine_slot->inc_a, word_a(all));
-        st_word(&mine_slot->inc_b, word_b(all));
+        st_relaxed_u64(&mine_slot->inc_a, word_a(all));
+        st_relaxed_u64(&mine_slot->inc_b, word_b(all));
       }
       s_prefix = prefix;
     }
@@ -352,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- last CTA: close the array, report, and clear the summary words
   if (tid == 0) {
     const Slot* sl = ws.slots + (tiles - 1);
-    const unsigned long long ia = ld_word(&sl->inc_a), ib = ld_word(&sl->inc_b);
+    const unsigned long long ia = ld_relaxed_u64(&sl->inc_a), ib = ld_relaxed_u64(&sl->inc_b);
     const unsigned failed = atomicExch(&ws.hdr->gave_up, 0u);
     const Bounds all = from_words(ia, ib);
     pseq_info out;
