@@ -120,20 +120,20 @@ union Items {
   Id v[kItems];
 };
 
-template <typename Id, bool kVector>
-__global__ void __launch_bounds__(kThreads, 1)
+template <typename Id, bool kVector, int THREADS>
+__global__ void __launch_bounds__(THREADS, THREADS <= 512 ? 2 : 1)
     doc_ids_scan_kernel(const Id* __restrict__ doc, int N, int S, int32_t* __restrict__ cu,
                         pseq_info* __restrict__ info, Workspace ws, int tiles, int64_t wait_ns,
                         int withhold) {
-  __shared__ Bounds s_warp[kWarps];
+  __shared__ Bounds s_warp[(THREADS / 32)];
   __shared__ Bounds s_prefix;
   __shared__ int s_last_cta;
-  __shared__ unsigned short s_pos[kTile];
+  __shared__ unsigned short s_pos[(THREADS * kItems)];
 
   pdl_enter();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tile = blockIdx.x;
-  const int64_t tile_base = (int64_t)tile * kTile;
+  const int64_t tile_base = (int64_t)tile * (THREADS * kItems);
   const int64_t t0 = tile_base + (int64_t)tid * kItems;
 
   // ---- this thread's 16 tokens and the token to their left
@@ -178,19 +178,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (lane == 31) s_warp[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    Bounds w = lane < kWarps ? s_warp[lane] : none();
+    Bounds w = lane < (THREADS / 32) ? s_warp[lane] : none();
 #pragma unroll
-    for (int d = 1; d < kWarps; d <<= 1) {
+    for (int d = 1; d < (THREADS / 32); d <<= 1) {
       const Bounds o = shfl_up(w, d);
       if (lane >= d) w = join(o, w);
     }
-    if (lane < kWarps) s_warp[lane] = w;
+    if (lane < (THREADS / 32)) s_warp[lane] = w;
   }
   __syncthreads();
   Bounds before_me = shfl_up(inc, 1);
   if (lane == 0) before_me = none();
   if (warp > 0) before_me = join(s_warp[warp - 1], before_me);
-  const Bounds tile_sum = s_warp[kWarps - 1];
+  const Bounds tile_sum = s_warp[(THREADS / 32) - 1];
 
   // ---- one tile: no neighbours, no workspace
   if (tiles == 1) {
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = 0; k < kItems; ++k)
       if (flags & (1ull << k)) s_pos[li++] = (unsigned short)(t0 + k - tile_base);
     __syncthreads();
-    for (int i = tid; i < tile_sum.count; i += kThreads) cu[i] = (int32_t)s_pos[i];
+    for (int i = tid; i < tile_sum.count; i += THREADS) cu[i] = (int32_t)s_pos[i];
     if (tid == 0) {
       cu[tile_sum.count] = N;
       *info = {PSEQ_OK, tile_sum.count, max(tile_sum.gap, N - tile_sum.last), N};
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   const int base = s_prefix.count;
   if (base >= 0 && base <= N - tile_sum.count) {
-    for (int i = tid; i < tile_sum.count; i += kThreads) cu[base + i] = (int32_t)(tile_base + s_pos[i]);
+    for (int i = tid; i < tile_sum.count; i += THREADS) cu[base + i] = (int32_t)(tile_base + s_pos[i]);
   } else if (tid == 0) {
     atomicOr(&ws.hdr->gave_up, 2u);  // only reachable from a workspace that was not zero-filled
   }
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *info = out;
   }
   unsigned long long* words = reinterpret_cast<unsigned long long*>(ws.slots);
-  for (int i = tid; i < 4 * tiles; i += kThreads) words[i] = 0ull;
+  for (int i = tid; i < 4 * tiles; i += THREADS) words[i] = 0ull;
 }
 
 __global__ void empty_map_kernel(int32_t* cu, pseq_info* info) {
@@ -371,11 +371,19 @@ cudaError_t launch_scan(const void* doc, int N, int S, int32_t* cu, pseq_info* i
   const Id* d = static_cast<const Id*>(doc);
   const int64_t wait = wait_limit_ns();
   const int withhold = (int)(withhold_tile() < 0 ? -1 : (withhold_tile() > INT32_MAX ? -1 : withhold_tile()));
+  // a map that fits half a tile runs as one 512-thread CTA (a 1024-thread
+  // CTA would leave half its threads idle)
+  constexpr int kSmall = 512;
+  const bool small = tiles == 1 && N <= kSmall * kItems;
   if (aligned(doc, 16))
-    return launch_pdl(doc_ids_scan_kernel<Id, true>, dim3(tiles), dim3(kThreads), 0, st, d, N, S, cu, info, ws,
-                      tiles, wait, withhold);
-  return launch_pdl(doc_ids_scan_kernel<Id, false>, dim3(tiles), dim3(kThreads), 0, st, d, N, S, cu, info, ws, tiles,
-                    wait, withhold);
+    return small ? launch_pdl(doc_ids_scan_kernel<Id, true, kSmall>, dim3(1), dim3(kSmall), 0, st, d, N, S, cu, info,
+                              ws, tiles, wait, withhold)
+                 : launch_pdl(doc_ids_scan_kernel<Id, true, kThreads>, dim3(tiles), dim3(kThreads), 0, st, d, N, S, cu,
+                              info, ws, tiles, wait, withhold);
+  return small ? launch_pdl(doc_ids_scan_kernel<Id, false, kSmall>, dim3(1), dim3(kSmall), 0, st, d, N, S, cu, info,
+                            ws, tiles, wait, withhold)
+               : launch_pdl(doc_ids_scan_kernel<Id, false, kThreads>, dim3(tiles), dim3(kThreads), 0, st, d, N, S, cu,
+                            info, ws, tiles, wait, withhold);
 }
 
 cudaError_t launch_empty_map(int32_t* cu, pseq_info* info, cudaStream_t st) {
