@@ -15,6 +15,9 @@ pseq_status fail(pseq_status st, const char* fmt, ...);
 pseq_status check_launch(const char* what);
 void clear_error();
 void count_launches(int n);
+// Resident CTAs per SM of `kernel` at `threads` and `smem` bytes of dynamic
+// shared memory (cached per device).
+int occupancy(const void* kernel, int threads, size_t smem);
 int sm_count();
 int64_t wait_limit_ns();
 int64_t withhold_tile();

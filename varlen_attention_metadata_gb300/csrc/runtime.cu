@@ -3,7 +3,9 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "common.cuh"
 
@@ -36,6 +38,21 @@ pseq_status check_launch(const char* what) {
 }
 
 void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int occupancy(const void* kernel, int threads, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, size_t>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto key = std::make_tuple(dev, kernel, smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
+  cache[key] = n;
+  return n;
+}
 
 int sm_count() {
   int dev = 0;

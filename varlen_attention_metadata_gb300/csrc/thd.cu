@@ -591,21 +591,6 @@ __global__ void __launch_bounds__(kRowThreads, 2)
 // ----------------------------------------------------------------------------
 // host side
 // ----------------------------------------------------------------------------
-int occupancy(const void* kernel, int threads, size_t smem) {
-  static std::mutex mu;
-  static std::map<std::tuple<int, const void*, size_t>, int> cache;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  std::lock_guard<std::mutex> lock(mu);
-  auto key = std::make_tuple(dev, kernel, smem);
-  auto it = cache.find(key);
-  if (it != cache.end()) return it->second;
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
-  cache[key] = n;
-  return n;
-}
-
 // One wave of CTAs: about one row per thread on the row-by-row path, every
 // resident slot for wide rows.
 int row_grid(const void* kernel, size_t smem, int64_t rows, const Fields& f) {

@@ -133,12 +133,19 @@ __global__ void __launch_bounds__(kThreads)
   *info = ok ? pseq_info{PSEQ_OK, (int32_t)total, 0, (int32_t)n} : pseq_info{PSEQ_ERR_VALUE, 0, 0, (int32_t)n};
 }
 
-int grid_for(int64_t n) {
+// One wave: at most `per_sm` resident CTAs per SM (the workspace is sized for
+// the largest any variant can have, 2048 threads' worth).
+int grid_for(int64_t n, int per_sm = 2048 / kThreads) {
   const int64_t groups = (n + kGroup - 1) / kGroup;
   const int64_t want = (groups + kThreads - 1) / kThreads;
-  const int64_t full = (int64_t)sm_count() * (2048 / kThreads);
+  const int64_t full = (int64_t)sm_count() * per_sm;
   const int64_t g = want < full ? want : full;
   return (int)(g < 1 ? 1 : g);
+}
+
+template <typename Id, bool kVector>
+int launch_grid(int64_t n) {
+  return grid_for(n, occupancy(reinterpret_cast<const void*>(token_mask_kernel<Id, kVector>), kThreads, 0));
 }
 
 }  // namespace
@@ -163,13 +170,14 @@ extern "C" pseq_status thd_mask_from_token_ids(const void* input_ids, int32_t id
   if (!aligned(input_ids, (uintptr_t)id_bytes) || !aligned(info, 4)) return fail(PSEQ_ERR_ARG, "%s: misaligned pointer", fn);
   if (id_bytes == 4 && (padding_token_id < INT32_MIN || padding_token_id > INT32_MAX))
     return fail(PSEQ_ERR_ARG, "%s: padding_token_id does not fit 32-bit ids", fn);
-  const int grid = grid_for(n);
-  const size_t need = workspace_bytes(grid);
+  const size_t need = workspace_bytes(grid_for(n));
   if (!workspace || workspace_bytes_ < need || !aligned(workspace, 16))
     return fail(PSEQ_ERR_ARG, "%s: workspace needs %zu bytes, 16-byte aligned (got %zu)", fn, need, workspace_bytes_);
   Header* hdr = static_cast<Header*>(workspace);
   Part* parts = reinterpret_cast<Part*>(static_cast<unsigned char*>(workspace) + sizeof(Header));
   const bool vec = aligned(input_ids, 16) && aligned(mask, 8);
+  const int grid = id_bytes == 4 ? (vec ? launch_grid<int32_t, true>(n) : launch_grid<int32_t, false>(n))
+                                 : (vec ? launch_grid<int64_t, true>(n) : launch_grid<int64_t, false>(n));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (id_bytes == 4) {
