@@ -770,10 +770,11 @@ def run_native(args, dist: Dist):
     next_rows = time_next_rows(dev, stream, args.seed + dist.rank, flush_l2) if dist.rank == 0 else None
 
     peak, peak_kind = measured_peak()
-    per_config = None
+    per_config = torch_gpu = None
     if dist.rank == 0:
         host["squeeze_scaled"] = synth.squeeze(args.seed, N=16384)
         per_config = time_per_config(step, host, dev, stream, flush_l2, peak)
+        torch_gpu = time_torch_restatement(host, dev, stream, flush_l2, per_config)
     emb_avg_ms = statistics.mean(emb_ms)
     achieved = step.emb_bytes / (emb_avg_ms / 1e3) / 1e9
     traffic = profiled_traffic()
@@ -836,6 +837,11 @@ def run_native(args, dist: Dist):
                                      "step's host bytes per second over the both-directions figure")},
             "next_rows": next_rows,
             "per_config": per_config,
+            "torch_gpu_restatement": {
+                "what": "each call restated as plain PyTorch ops on the same GPU (boolean filtering, cumsum, "
+                        "nonzero, index gathers; bench-only, not the product path), cold: L2 flushed first, "
+                        "host synchronisations inside the timed span",
+                "per_config": torch_gpu},
             "gpu_launches": int(launches),
             "gpu_launches_per_step": per_step_launches,
             "clocks": clocks.summary(),
@@ -952,6 +958,152 @@ def time_per_config(step, host, dev, stream, flush_l2, peak, warm=20, reps=200) 
         if base is not step:
             del base
             torch.cuda.empty_cache()
+    return out
+
+
+# ----------------------------------------------------------------------------
+# A comparison line: each call restated as plain PyTorch ops on the same GPU
+# (boolean filtering, cumsum, nonzero, index gathers), written from what the
+# calls compute.  Bench-only and labelled as such; never the product path.
+# ----------------------------------------------------------------------------
+def torch_doc_ids(d):
+    """cu_seqlens (int32) and max_seqlen of a [B, S] document map."""
+    import torch
+
+    B, S = d.shape
+    starts = torch.ones_like(d, dtype=torch.bool)
+    starts[:, 1:] = d[:, 1:] != d[:, :-1]
+    idx = starts.reshape(-1).nonzero().squeeze(1)
+    cu = torch.cat([idx, idx.new_tensor([B * S])]).to(torch.int32)
+    return cu, int((cu[1:] - cu[:-1]).max()) if B * S else 0
+
+
+def torch_thd(real, padded, S, fields, pad_value=-1000):
+    """BSHD -> THD: cu arrays, gathered fields ([planes, B, S, row] tensors
+    given as (tensor, planes)), padding mask (True = padding), max_seqlen."""
+    import torch
+
+    dev = real.device
+    keep = real != pad_value
+    r, p = real[keep], padded[keep]
+    n = r.numel()
+    pz = torch.where(keep, padded, torch.zeros_like(padded))
+    off = (pz.cumsum(1) - pz)[keep]
+    rows = keep.nonzero()[:, 0]
+    cu = torch.zeros(n + 1, dtype=torch.int64, device=dev)
+    cup = torch.zeros(n + 1, dtype=torch.int64, device=dev)
+    cu[1:] = r.cumsum(0)
+    cup[1:] = p.cumsum(0)
+    T = int(cup[-1])
+    seq = torch.repeat_interleave(torch.arange(n, device=dev), p, output_size=T)
+    within = torch.arange(T, device=dev) - cup[:-1][seq]
+    src = rows[seq] * S + off[seq] + within
+    outs = []
+    for x, planes in fields:
+        flat = x.reshape(planes, -1, *x.shape[3 if planes > 1 else 2:])
+        outs.append(flat[:, src])
+    mask = within >= r[seq]
+    if n >= 1 and bool((r[:-1] == p[:-1]).all()):
+        cu[-1] = T
+    max_seqlen = int((cu[1:] - cu[:-1]).max()) if n else 0
+    return cu.to(torch.int32), cup.to(torch.int32), outs, mask, max_seqlen
+
+
+def torch_squeeze(src, real, offsets, members, multiple, capacity, stretch, width, pad_value):
+    """The trainer-side squeeze: packed [bins, width], mask (True = padding),
+    flat per-bin cu arrays (bin b at offsets[b] + b)."""
+    import torch
+
+    dev = src.device
+    nb = offsets.numel() - 1
+    M = members.numel()
+    mem = members.long()
+    counts = (offsets[1:] - offsets[:-1]).long()
+    bin_of = torch.repeat_interleave(torch.arange(nb, device=dev), counts, output_size=M)
+    r = real[mem]
+    p = (r + multiple - 1) // multiple * multiple
+    ex_p = p.cumsum(0) - p
+    ex_r = r.cumsum(0) - r
+    first = offsets[:-1].long()
+    dst = ex_p - ex_p[first][bin_of]
+    totals = torch.zeros(nb, dtype=torch.int64, device=dev).index_add_(0, bin_of, p)
+    if bool((totals > capacity).any()) or bool((totals > width).any()):
+        raise ValueError("a bin exceeds capacity")
+    R = int(r.sum())
+    mi = torch.repeat_interleave(torch.arange(M, device=dev), r, output_size=R)
+    within = torch.arange(R, device=dev) - ex_r[mi]
+    slot = bin_of[mi] * width + dst[mi] + within
+    out = torch.full((nb * width,), pad_value, dtype=src.dtype, device=dev)
+    out[slot] = src[mem[mi], within]
+    mask = torch.ones(nb * width, dtype=torch.bool, device=dev)
+    mask[slot] = False
+    pos = torch.arange(M, device=dev) + bin_of + 1
+    cu = torch.zeros(M + nb, dtype=torch.int64, device=dev)
+    cup = torch.zeros(M + nb, dtype=torch.int64, device=dev)
+    cu[pos] = r.cumsum(0) - ex_r[first][bin_of]
+    cup[pos] = p.cumsum(0) - ex_p[first][bin_of]
+    if stretch:
+        cup[offsets[1:].long() + torch.arange(nb, device=dev)] = capacity
+    return out.view(nb, width), mask.view(nb, width), cu.to(torch.int32), cup.to(torch.int32)
+
+
+def torch_calls(host: dict, dev) -> dict:
+    """One closure per configuration, inputs already on the device."""
+    import torch
+
+    def d(a):
+        return (a if isinstance(a, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(a))).to(dev)
+
+    calls = {}
+    for name in ("map_small", "map_stress"):
+        m = d(host[name])
+        calls[name] = (lambda m=m: torch_doc_ids(m))
+    for name, planes in (("thd_small", 1), ("thd_ids", 3)):
+        bt = host[name]
+        S = bt["input_ids"].shape[1]
+        fields = [(d(bt["input_ids"]), 1), (d(bt["labels"]), 1), (d(bt["position_ids"]), planes)]
+        real, pad = d(bt["seq_lens"]), d(bt["seq_lens_padded"])
+        calls[name] = (lambda real=real, pad=pad, S=S, fields=fields: torch_thd(real, pad, S, fields))
+    emb = host["thd_emb"]
+    hid = d(emb["hidden"])
+    er, ep = d(emb["seq_lens"]), d(emb["seq_lens_padded"])
+    calls["thd_emb"] = lambda: torch_thd(er, ep, hid.shape[1], [(hid, 1)])
+    for name in ("squeeze", "squeeze_scaled"):
+        if name not in host:
+            continue
+        c = host[name]
+        args = (d(c["src"]), d(c["real_lens"]), d(c["bin_offsets"]), d(c["bin_members"]), c["multiple"],
+                c["capacity"], c["stretch"], c["width"], c["pad_value"])
+        calls[name] = (lambda args=args: torch_squeeze(*args))
+    return calls
+
+
+def time_torch_restatement(host, dev, stream, flush_l2, per_config, warm=5, reps=30) -> dict:
+    """Cold per-call time of the torch restatement (L2 flushed first; the
+    host synchronisations its ops need are inside the timed span), beside
+    this library's cold time from per_config."""
+    import torch
+
+    out = {}
+    with torch.cuda.stream(stream):
+        calls = torch_calls(host, dev)
+        for name, fn in calls.items():
+            ts = []
+            for i in range(warm + reps):
+                flush_l2()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize(dev)
+                if i >= warm:
+                    ts.append(a.elapsed_time(b) * 1e3)
+            us = statistics.median(ts)
+            mine = per_config.get(name, {}).get("cold_us") if per_config else None
+            out[name] = {"us": round(us, 2), "pseq_cold_us": mine,
+                         "speedup": round(us / mine, 1) if mine else None}
+    del calls
+    torch.cuda.empty_cache()
     return out
 
 

@@ -126,3 +126,35 @@ def test_one_stream_step_matches_the_oracle(step):
     with torch.cuda.stream(step.stream):
         step.run()
     check_outputs(step)
+
+
+def test_torch_restatement_matches_the_oracle():
+    """The bench's torch-on-GPU comparison line computes the same results."""
+    import bench
+
+    host = bench.make_inputs(1)
+    calls = bench.torch_calls(host, DEV)
+    for name in ("map_small", "map_stress"):
+        cu, mx = calls[name]()
+        ref_cu, ref_mx = oracle.from_doc_ids(host[name])
+        np.testing.assert_array_equal(cu.cpu().numpy(), ref_cu)
+        assert mx == ref_mx
+    for name in ("thd_small", "thd_ids"):
+        bt = host[name]
+        cu, cup, outs, mask, mx = calls[name]()
+        ref = oracle.process_input_for_thd(
+            {k: bt[k] for k in ("input_ids", "labels", "position_ids", "seq_lens", "seq_lens_padded")})
+        np.testing.assert_array_equal(cu.cpu().numpy(), ref["cu_seqlens"])
+        np.testing.assert_array_equal(cup.cpu().numpy(), ref["cu_seqlens_padded"])
+        np.testing.assert_array_equal(mask.cpu().numpy(), ref["padding_mask"])
+        assert mx == ref["max_seqlen"]
+        for got, key in zip(outs, ("input_ids", "labels", "position_ids")):
+            np.testing.assert_array_equal(got.cpu().numpy().reshape(-1), ref[key].reshape(-1))
+    c = host["squeeze"]
+    out, mask, cu, cup = calls["squeeze"]()
+    ref = oracle.pack_squeeze(c["src"], c["real_lens"], c["bin_offsets"], c["bin_members"], c["multiple"],
+                              c["capacity"], c["stretch"], c["width"], c["pad_value"])
+    np.testing.assert_array_equal(out.cpu().numpy(), ref["packed"])
+    np.testing.assert_array_equal(mask.cpu().numpy(), ref["padding_mask"])
+    np.testing.assert_array_equal(cu.cpu().numpy(), ref["cu_flat"])
+    np.testing.assert_array_equal(cup.cpu().numpy(), ref["cu_padded_flat"])
