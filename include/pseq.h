@@ -101,14 +101,14 @@ pseq_status pseq_from_doc_ids(const void* doc_ids, int32_t id_bytes, int64_t B,
 
 /* ------------------------------------------------------------------------
  * pseq_from_doc_ids_static -- pseq_from_doc_ids without a workspace
- * The paper has no counterpart to this entry point; it is an integration
+ * The pages have no counterpart to this entry point; it is an integration
  * variant of the call above.
  * Some callers cannot allocate device memory when they call in: code running
  * under a memory-pool policy that forbids new allocations, a plugin or
  * callback that is handed only input and output pointers, or a process that
  * has reserved all of HBM up front.  This entry point takes the same inputs
  * and outputs as pseq_from_doc_ids and no workspace.  Its scratch is a
- * static device array of about 144 KiB inside libpseq.so, which every GPU
+ * static device array of about 32 KiB inside libpseq.so, which every GPU
  * that loads the library holds until the process exits.
  *  - B*S must not exceed PSEQ_STATIC_MAX_TOKENS; larger maps get
  *    PSEQ_ERR_ARG before anything is enqueued (use pseq_from_doc_ids).
@@ -243,9 +243,9 @@ pseq_status thd_chunks_from_batch(const int64_t* seq_lens,
 /* ------------------------------------------------------------------------
  * thd_mask_from_token_ids -- thd_padding_mask_from_token_ids
  * [thd_utils] "thd_padding_mask_from_token_ids": mask[t] = 1 where
- *   input_ids[t] == padding_token_id.  A value comparison is only correct
- *   when the pad id fills a right-padded tail and appears nowhere else, so a
- *   pad token followed by any other token is PSEQ_ERR_VALUE (the page raises
+ *   input_ids[t] == padding_token_id.  That comparison marks padding
+ *   correctly only if the pad positions form a suffix of the stream, so a pad
+ *   token followed by any other token is PSEQ_ERR_VALUE (the page raises
  *   ValueError).
  * input_ids: n integers of id_bytes (4 or 8).  mask: n bytes.
  * info: count = number of pad tokens, total = n.
@@ -262,8 +262,8 @@ pseq_status thd_mask_from_token_ids(const void* input_ids, int32_t id_bytes,
 
 /* ------------------------------------------------------------------------
  * pack_ffd -- first-fit-decreasing bins for pack_squeeze
- * [who_packs] get_packer "picks which rows share a bin, by token budget";
- *   First Fit Decreasing is one of the packers the page names.  Item i has
+ * [who_packs] get_packer: the step that groups rows into bins under a token
+ *   budget; First Fit Decreasing is one of the packers the page names.  Item i has
  *   size lens[i] rounded up to `multiple`; items are visited largest first
  *   (ties: smaller index first) and each goes into the first open bin with
  *   room; a new bin opens when none has room.
@@ -328,9 +328,8 @@ pseq_status thd_padding_mask(int64_t total_tokens,
 
 /* ------------------------------------------------------------------------
  * pack_squeeze -- the trainer-side squeeze
- * [who_packs] "Trainer packs: a padded rectangle squeezed inside the
- * worker", "Loader packs", and the note that cu_seqlens_padded ends at the
- * pack capacity.
+ * [who_packs] sections "Trainer packs" and "Loader packs", and the note
+ * that cu_seqlens_padded ends at the pack capacity.
  *
  * src: [N, W] rectangle of elem_bytes (1, 2, 4 or 8) elements; source i
  *   holds real_lens[i] (int64 [N]) tokens at the start of its row.

@@ -213,13 +213,12 @@ int oracle_thd_padding_mask(int64_t total_tokens, const int64_t* valid_seq_lens,
 
 /* ------------------------------------------------------------------------
  * O5  trainer-side squeeze
- * [who_packs] "Trainer packs: a padded rectangle squeezed inside the
- *   worker" and "Loader packs": each source is padded to a multiple of m;
- *   the sources of one bin are concatenated end to end in the given order;
- *   cu_seqlens = [0] + cumsum(real) ("where the real tokens end"),
- *   cu_seqlens_padded = [0] + cumsum(padded) ("where each padded source
- *   ends"); with stretch set, the last padded boundary is set to the pack
- *   capacity (36 instead of 20 in the page's example).
+ * [who_packs] sections "Trainer packs" and "Loader packs": each source is
+ *   padded to a multiple of m; the sources of one bin are concatenated end to
+ *   end in the given order; cu_seqlens = [0] + cumsum(real) marks the end of
+ *   each source's real tokens, cu_seqlens_padded = [0] + cumsum(padded) the
+ *   end of each padded source; with stretch set, the last padded boundary is
+ *   set to the pack capacity (36 instead of 20 in the page's example).
  * Readings: only the first real_i tokens of a source row are copied; every
  *   other slot of the [num_bins, width] output holds pad_value and is marked
  *   1 in padding_mask.  A bin whose padded total exceeds capacity or width
@@ -294,10 +293,10 @@ int oracle_pack_squeeze(const void* src, int64_t N, int64_t W, int elem_bytes,
 
 /* ------------------------------------------------------------------------
  * O6  thd_padding_mask_from_token_ids
- * [thd_utils] "thd_padding_mask_from_token_ids": padding is marked by
- *   comparing token ids with padding_token_id, which is only correct when the
- *   pad id fills a right-padded tail and appears nowhere else; anything else
- *   is rejected (the page raises ValueError).
+ * [thd_utils] thd_padding_mask_from_token_ids: padding is marked by
+ *   comparing token ids with padding_token_id.  That comparison is sound only
+ *   if the pad positions form a suffix of the stream; any other placement is
+ *   rejected (the page raises ValueError).
  * Returns ORC_VALUE when a pad token is followed by a non-pad token.
  * ---------------------------------------------------------------------- */
 int oracle_mask_from_token_ids(const void* ids, int elem_bytes, int64_t n,
@@ -314,8 +313,8 @@ int oracle_mask_from_token_ids(const void* ids, int elem_bytes, int64_t n,
 
 /* ------------------------------------------------------------------------
  * O7  first-fit-decreasing bin assignment
- * [who_packs] "get_packer picks which rows share a bin, by token budget"; the
- *   page names First Fit Decreasing among the packers.  The textbook
+ * [who_packs] get_packer: the packer decides which rows go into one bin under
+ *   a token budget; the page names First Fit Decreasing among the packers.  The textbook
  *   algorithm: visit the items largest first (ties: smaller index first) and
  *   put each into the first open bin with room; open a new bin when none has
  *   room.  bin_members lists each bin's items in placement order, bin b

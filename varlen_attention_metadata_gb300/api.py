@@ -588,7 +588,7 @@ def split_batch_into_thd_chunks(batch: dict, num_chunks: int, seq_lens_padding_v
 def thd_padding_mask_from_token_ids(input_ids: torch.Tensor, padding_token_id: int) -> torch.Tensor:
     """NeMo AutoModel v0.5 thd_utils, ``thd_padding_mask_from_token_ids``:
     bool mask (True = padding) by value; ValueError when the pad id also
-    occurs as content (anywhere before the right-padded tail)."""
+    occurs as content (anywhere before the suffix of pad tokens)."""
     mask, info = thd_mask_from_token_ids(input_ids, padding_token_id)
     st = _info_view(info).tolist()[0]
     if st != _lib.PSEQ_OK:

@@ -1,8 +1,8 @@
 // pack_ffd: first-fit-decreasing bin assignment for the trainer-side squeeze.
 //
-// "Who packs the sequences: the loader, or the trainer?" has get_packer pick
-// which rows share a bin by token budget and names First Fit Decreasing among
-// the packers.  The textbook algorithm: visit the items largest first (ties:
+// In "Who packs the sequences: the loader, or the trainer?", get_packer is the
+// step that groups rows into bins under a token budget, and First Fit
+// Decreasing is one of the packers the page names.  The textbook algorithm: visit the items largest first (ties:
 // smaller index first) and put each into the first open bin with room.
 //
 // One CTA.  Each item becomes a 64-bit key (inverted size, index) so an

@@ -2,9 +2,9 @@
 // also occurs as content.
 //
 // Follows NeMo AutoModel v0.5 "nemo_automodel.components.distributed.thd_utils",
-// thd_padding_mask_from_token_ids: a value comparison is only correct when the
-// pad id fills a right-padded tail and appears nowhere else, so exactly that
-// is validated and a colliding id is an error.
+// thd_padding_mask_from_token_ids: comparing ids with the pad id marks padding
+// correctly only if the pad positions form a suffix of the stream, so the
+// kernel checks that and reports a pad id that also occurs as content.
 //
 // One pass.  Each thread compares eight consecutive ids (16-byte loads) and
 // stores their eight mask bytes at once; each CTA reduces the first pad
