@@ -512,13 +512,20 @@ def link_ceiling(dev, nbytes: int = 256 << 20) -> dict:
 
 def kernel_source_hash() -> str:
     """Hash of the sources the roofline kernel (thd_fused_bulk_kernel) is
-    built from: its translation unit, the shared device header, the C ABI."""
+    built from -- its translation unit, the shared device header, the C ABI --
+    with comments and blank lines removed, so only code changes count."""
+    import re
+
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "varlen_attention_metadata_gb300", "csrc")
     for path in (os.path.join(csrc, "thd.cu"), os.path.join(csrc, "common.cuh"),
                  os.path.join(ROOT, "include", "pseq.h")):
-        with open(path, "rb") as fh:
-            h.update(fh.read())
+        with open(path) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(code.encode())
     return h.hexdigest()[:16]
 
 
