@@ -504,6 +504,19 @@ def test_squeeze_many_members():
     check_squeeze(prob, m, need, False, need)
 
 
+@pytest.mark.parametrize("members", [1, 31, 32, 33, 127, 128, 129, 300])
+def test_squeeze_bin_member_counts(members):
+    # bins of up to 128 members are scanned by one warp, larger ones by the block
+    rng = np.random.default_rng(members)
+    prob = synth.random_squeeze(rng, members * 3, 50, 3)
+    m = 8
+    need = max(sum(-(-int(prob["real_lens"][i]) // m) * m for i in b) for b in prob["bins"])
+    check_squeeze(prob, m, need, True, need, pad_value=5)
+    one = synth.random_squeeze(rng, members, 50, 1)
+    need = sum(-(-int(one["real_lens"][i]) // m) * m for i in one["bins"][0])
+    check_squeeze(one, m, need + 64, False, need + 64)
+
+
 def test_squeeze_bins_denser_than_a_window():
     # multiple 1 and lengths 0..3: a window of output slots meets up to one
     # member per slot, and zero-length members own no slot at all
