@@ -668,6 +668,15 @@ pseq_status build_fields(const char* fn, const pseq_field* fields, int num_field
 }
 
 
+// Bulk-copy CTAs: one per SM on four fifths of the SMs.  About 120 copy
+// engines already saturate HBM (each moves ~55 GB/s here; 88 fall short),
+// and the SMs left free let calls that run beside this one -- on another
+// stream -- start at once instead of waiting for SMs to drain.
+int bulk_ctas() {
+  const int n = sm_count() - sm_count() / 5;
+  return n > 0 ? n : 1;
+}
+
 pseq_status launch_fused(const char* fn, const MetaArgs& a, const Fields& f, uint8_t* mask, int64_t mask_cap,
                          cudaStream_t st) {
   const int64_t rows = a.fixed_total >= 0 ? a.fixed_total : (int64_t)a.B * a.S;
@@ -684,7 +693,7 @@ pseq_status launch_fused(const char* fn, const MetaArgs& a, const Fields& f, uin
       if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
       attr_set[dev] = true;
     }
-    e = launch_pdl(thd_fused_bulk_kernel, dim3((unsigned)sm_count(), (unsigned)a.chunks), dim3(kRowThreads), smem, st,
+    e = launch_pdl(thd_fused_bulk_kernel, dim3((unsigned)bulk_ctas(), (unsigned)a.chunks), dim3(kRowThreads), smem, st,
                    a, f, mask, mask_cap, wait_limit_ns());
   } else {
     const size_t smem = table_bytes(a.B, a.P);
