@@ -682,6 +682,7 @@ def run_native(args, dist: Dist):
             ev1[i][1].record(stream)
     torch.cuda.synchronize(dev)
     one_stream_ms = statistics.mean(a.elapsed_time(b) for a, b in ev1)
+    graph_ms = step_graph_ms(step, dev, stream, flush_l2, K1)
 
     gpu_id = None
     try:
@@ -818,6 +819,9 @@ def run_native(args, dist: Dist):
                           "second stream forked from and joined into the step's stream, the other five calls on "
                           "the step's stream",
                 "ms_per_step_one_stream": round(one_stream_ms, 6),
+                "ms_per_step_graph": round(graph_ms, 6) if graph_ms else None,
+                "graph": "the same two-stream step captured once in a CUDA graph and replayed (fork and join "
+                         "become graph edges); not the headline, which issues the calls directly",
             },
             "roofline": {
                 "kernel": "thd_fused_bulk_kernel via thd_from_batch (bf16 hidden [4,8192,4096] -> [T,4096], cu arrays, mask)",
@@ -875,6 +879,42 @@ PER_CONFIG = (
     ("squeeze_scaled", "scaled squeeze (labelled extra, not a config): int64 [16384,4096] -> FFD bins x 32768"),
 )
 ROTATE_MAX_SETS = 4096
+
+
+def capture_step(step, stream):
+    """The two-stream step captured in a CUDA graph (the side stream joins
+    the capture through the step's fork event)."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step.run(two_streams=True)
+    return g
+
+
+def step_graph_ms(step, dev, stream, flush_l2, reps) -> float | None:
+    """Mean device time of one replay of the captured step, L2 flushed
+    between replays outside the events."""
+    import torch
+
+    try:
+        g = capture_step(step, stream)
+    except RuntimeError:
+        return None
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush_l2()
+            g.replay()
+        for i in range(reps):
+            flush_l2()
+            ev[i][0].record(stream)
+            g.replay()
+            ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    del g
+    return ms
 
 
 def _graph_us(calls, dev, stream, flush_l2, replays=10):

@@ -158,3 +158,15 @@ def test_torch_restatement_matches_the_oracle():
     np.testing.assert_array_equal(mask.cpu().numpy(), ref["padding_mask"])
     np.testing.assert_array_equal(cu.cpu().numpy(), ref["cu_flat"])
     np.testing.assert_array_equal(cup.cpu().numpy(), ref["cu_padded_flat"])
+
+
+def test_step_replayed_from_a_cuda_graph_matches_the_oracle(step):
+    """The two-stream step captured once in a CUDA graph and replayed."""
+    import bench
+
+    g = bench.capture_step(step, step.stream)
+    for _ in range(2):
+        clear_outputs(step)
+        with torch.cuda.stream(step.stream):
+            g.replay()
+        check_outputs(step)
