@@ -429,6 +429,20 @@ def time_next_rows(dev, stream, seed: int, flush_l2, reps: int = 60) -> dict:
     out["split_batch_into_thd_chunks"] = {"workload": "B=8 S=8192 ids/labels/mRoPE, 4 chunks", "us": round(us, 2),
                                           "graph_us": g(lib.thd_chunks_from_batch), "bytes": nbytes,
                                           "gbs": round(nbytes / us / 1e3, 1)}
+    # thd_padding_mask (the standalone a8 call): the B=8 S=8192 batch's kept lengths
+    kept = c1["seq_lens"] != -1000
+    vr, vp = dev_t(c1["seq_lens"][kept]), dev_t(c1["seq_lens_padded"][kept])
+    nk = int(kept.sum())
+    Tk = int(c1["seq_lens_padded"][kept].sum())
+    pmask = torch.empty(Tk, dtype=torch.uint8, device=dev)
+    pinfo = torch.empty(4, dtype=torch.int32, device=dev)
+    pws = torch.empty(lib.thd_workspace_size(1, nk), dtype=torch.uint8, device=dev)
+    keep += [pmask, pinfo, pws]
+    us = timed(lib.thd_padding_mask, (Tk, P(vr), P(vp), nk, P(pmask), P(pinfo), P(pws), pws.numel(), sh))
+    nbytes = Tk + 16 * nk
+    out["thd_padding_mask"] = {"workload": f"{nk} kept sequences of the B=8 S=8192 batch -> mask [{Tk}]",
+                               "us": round(us, 2), "graph_us": g(lib.thd_padding_mask), "bytes": nbytes,
+                               "gbs": round(nbytes / us / 1e3, 1)}
     # thd_padding_mask_from_token_ids: a 2M-token id stream with a padded tail
     rng = np.random.default_rng(seed)
     n = 1 << 21
