@@ -1,0 +1,119 @@
+"""Calls at the largest sizes the C ABI accepts, checked where the oracle can
+follow (sampled rows) and by properties that hold at any size.
+
+The inputs are built on the device (a few GB each); the oracle runs on the
+sampled rows only.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+INT32_MAX = 2**31 - 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from varlen_attention_metadata_gb300 import build
+
+    build.build()
+    yield
+    torch.cuda.empty_cache()
+
+
+def info_of(t):
+    return t[:16].view(torch.int32).tolist()[:4] if t.dtype == torch.uint8 else t[:4].tolist()
+
+
+def test_doc_ids_scan_at_two_billion_tokens():
+    import varlen_attention_metadata_gb300 as v
+
+    B, S = 32768, 65535  # B*S = 2^31 - 2^15: 131070 tiles, far more than one wave
+    N = B * S
+    assert N <= INT32_MAX
+    g = torch.Generator(device=DEV).manual_seed(5)
+    # runs of about 64 tokens: a new document wherever a 1-in-64 draw hits
+    starts = torch.randint(0, 64, (B, S), device=DEV, dtype=torch.int32, generator=g) == 0
+    d = starts.to(torch.int32).cumsum(1, dtype=torch.int32)
+    del starts
+    cu, info = v.pseq_from_doc_ids(d)
+    st, count, mx, total = info_of(info)
+    assert st == 0 and total == N
+    c = cu[: count + 1]
+    assert int(c[0]) == 0 and int(c[-1]) == N
+    assert bool((c[1:] > c[:-1]).all())
+    # every row start is a boundary; boundaries per row equal the run count of the row
+    row_first = torch.arange(B, device=DEV, dtype=torch.int64) * S
+    pos = torch.searchsorted(c.to(torch.int64), row_first)
+    assert bool((c.to(torch.int64)[pos] == row_first).all())
+    assert mx == int((c[1:] - c[:-1]).max())
+    # sampled rows against the oracle
+    rng = np.random.default_rng(0)
+    for b in sorted(rng.choice(B, size=16, replace=False).tolist()) + [0, B - 1]:
+        row = d[b:b + 1].cpu().numpy()
+        ref_cu, _ = oracle.from_doc_ids(row)
+        lo = int(pos[b])
+        hi = int(pos[b + 1]) if b + 1 < B else count
+        got = c[lo:hi + 1].to(torch.int64).cpu().numpy() - b * S
+        np.testing.assert_array_equal(got, ref_cu)
+    del d, cu, c
+
+
+def test_squeeze_with_the_most_bins():
+    import varlen_attention_metadata_gb300 as v
+
+    nb = 65535  # the grid's second dimension
+    rng = np.random.default_rng(6)
+    W = 64
+    real = rng.integers(0, W + 1, size=nb).astype(np.int64)
+    src = rng.integers(-1000, 1000, size=(nb, W)).astype(np.int64)
+    offs = np.arange(nb + 1, dtype=np.int32)
+    mem = rng.permutation(nb).astype(np.int32)
+    width = 64
+    r = v.pack_squeeze(torch.from_numpy(src).to(DEV), torch.from_numpy(real).to(DEV),
+                       (torch.from_numpy(offs).to(DEV), torch.from_numpy(mem).to(DEV)), 8, width, True, width, 7)
+    st, count, mx, total = info_of(r["info"])
+    ref = oracle.pack_squeeze(src, real, offs, mem, 8, width, True, width, 7)
+    assert st == 0 and count == nb and total == ref["max_total"]
+    np.testing.assert_array_equal(r["packed"].cpu().numpy(), ref["packed"])
+    np.testing.assert_array_equal(r["padding_mask"].cpu().numpy(), ref["padding_mask"])
+    np.testing.assert_array_equal(r["cu_seqlens"][: 2 * nb].cpu().numpy(), ref["cu_flat"])
+    np.testing.assert_array_equal(r["cu_seqlens_padded"][: 2 * nb].cpu().numpy(), ref["cu_padded_flat"])
+    # one bin more than the grid holds is refused before anything is enqueued
+    offs2 = np.arange(nb + 2, dtype=np.int32)
+    mem2 = np.arange(nb + 1, dtype=np.int32)
+    real2 = np.ones(nb + 1, np.int64)
+    src2 = np.zeros((nb + 1, 1), np.int64)
+    with pytest.raises(Exception):
+        v.pack_squeeze(torch.from_numpy(src2).to(DEV), torch.from_numpy(real2).to(DEV),
+                       (torch.from_numpy(offs2).to(DEV), torch.from_numpy(mem2).to(DEV)), 1, 1, False, 1, 0)
+
+
+def test_token_mask_at_the_int32_limit():
+    import varlen_attention_metadata_gb300 as v
+
+    n = INT32_MAX
+    tail = 1 << 20
+    g = torch.Generator(device=DEV).manual_seed(7)
+    ids = torch.randint(1, 32000, (n,), device=DEV, dtype=torch.int32, generator=g)
+    ids[n - tail:] = 0
+    mask, info = v.thd_mask_from_token_ids(ids, 0)
+    st, count, _, total = info_of(info)
+    assert st == 0 and count == tail and total == n
+    assert int(mask[: n - tail].sum(dtype=torch.int64)) == 0 and bool(mask[n - tail:].all())
+    # a pad id inside the content is refused
+    ids[12345] = 0
+    _, info = v.thd_mask_from_token_ids(ids, 0)
+    assert info_of(info)[0] == 3
+    # sampled windows against the oracle
+    ids[12345] = 7
+    rng = np.random.default_rng(1)
+    for start in [0, n - tail - 100, n - 4096] + rng.integers(0, n - tail - 4096, size=6).tolist():
+        win = ids[start:start + 4096].cpu().numpy()  # content, then possibly the pad tail: a valid stream
+        got = mask[start:start + 4096].cpu().numpy().astype(bool)
+        np.testing.assert_array_equal(got, oracle.mask_from_token_ids(win, 0))
+    del ids, mask
