@@ -117,3 +117,42 @@ def test_token_mask_at_the_int32_limit():
         got = mask[start:start + 4096].cpu().numpy().astype(bool)
         np.testing.assert_array_equal(got, oracle.mask_from_token_ids(win, 0))
     del ids, mask
+
+
+def test_thd_conversion_at_two_billion_tokens():
+    import varlen_attention_metadata_gb300 as v
+
+    B, S, P = 32768, 65535, 8  # 2^31 - 2^15 source slots, 262144 table entries: the two-kernel path
+    rng = np.random.default_rng(8)
+    real = np.full((B, P), -1000, np.int64)
+    padded = np.full((B, P), -1000, np.int64)
+    for b in range(B):
+        k = int(rng.integers(1, P + 1))
+        used = int(rng.integers(k, S + 1))  # rows may end short of S
+        cuts = np.sort(rng.choice(np.arange(1, used), size=k - 1, replace=False)) if k > 1 else np.array([], int)
+        pl = np.diff(np.concatenate([[0], cuts, [used]]))
+        rl = pl - rng.integers(0, np.minimum(pl, 4))
+        slots = np.sort(rng.choice(P, size=k, replace=False))  # filler between kept entries too
+        padded[b, slots] = pl
+        real[b, slots] = rl
+    g = torch.Generator(device=DEV).manual_seed(9)
+    ids = torch.randint(-2**31, 2**31 - 1, (B, S), device=DEV, dtype=torch.int32, generator=g)
+    r = v.thd_from_batch(torch.from_numpy(real).to(DEV), torch.from_numpy(padded).to(DEV), S, [(ids, 1)])
+    st, n, mx, T = info_of(r["info"])
+    meta = oracle.thd_meta(real, padded, S)
+    assert st == 0 and n == meta["num_sequences"] and T == meta["total_tokens"] and mx == meta["max_seqlen"]
+    np.testing.assert_array_equal(r["cu_seqlens"][: n + 1].cpu().numpy(), meta["cu_seqlens"])
+    np.testing.assert_array_equal(r["cu_seqlens_padded"][: n + 1].cpu().numpy(), meta["cu_seqlens_padded"])
+    mask = r["padding_mask"][:T]
+    assert int(mask.sum(dtype=torch.int64)) == T - int(meta["seq_real"].sum())
+    out = r["dst"][0][0]
+    # sampled rows: the row's stream slice against the oracle on that row alone
+    first_seq = np.concatenate([[0], np.cumsum((real != -1000).sum(axis=1))])
+    cup = meta["cu_seqlens_padded"]
+    for b in sorted(rng.choice(B, size=12, replace=False).tolist()) + [0, B - 1]:
+        ref = oracle.process_input_for_thd({"input_ids": ids[b:b + 1].cpu().numpy(), "seq_lens": real[b:b + 1],
+                                            "seq_lens_padded": padded[b:b + 1]}, absorb=False)
+        lo, hi = int(cup[first_seq[b]]), int(cup[first_seq[b + 1]])
+        np.testing.assert_array_equal(out[lo:hi].cpu().numpy(), ref["input_ids"])
+        np.testing.assert_array_equal(mask[lo:hi].cpu().numpy(), ref["padding_mask"])
+    del ids, r, out, mask
