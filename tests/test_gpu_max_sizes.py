@@ -156,3 +156,30 @@ def test_thd_conversion_at_two_billion_tokens():
         np.testing.assert_array_equal(out[lo:hi].cpu().numpy(), ref["input_ids"])
         np.testing.assert_array_equal(mask[lo:hi].cpu().numpy(), ref["padding_mask"])
     del ids, r, out, mask
+
+
+def test_bridge_with_the_most_rows():
+    import varlen_attention_metadata_gb300 as v
+
+    B, S, P = 65535, 32768, 1024  # 65535 rows is the grid's limit; B*S = 2^31 - 2^15
+    g = torch.Generator(device=DEV).manual_seed(10)
+    draw = torch.randint(0, 64, (B, S), device=DEV, dtype=torch.int32, generator=g)
+    # documents of about 64 tokens, a padding run wherever a 1-in-16 draw hits a run start
+    starts = draw == 0
+    d = starts.to(torch.int32).cumsum(1, dtype=torch.int32)
+    d = torch.where((d % 16) == 5, torch.zeros_like(d), d)
+    del draw, starts
+    real, padded, pos, info = v.pseq_doc_ids_to_lengths(d, P)
+    st, most, longest, total = info_of(info)
+    assert st == 0
+    kept = real != -1000
+    assert total == int(kept.sum()) and most == int(kept.sum(dim=1).max())
+    # padded lengths tile every row
+    assert bool((torch.where(kept, padded, torch.zeros_like(padded)).sum(dim=1) == S).all())
+    rng = np.random.default_rng(2)
+    for b in sorted(rng.choice(B, size=12, replace=False).tolist()) + [0, B - 1]:
+        ref = oracle.doc_ids_to_lengths(d[b:b + 1].cpu().numpy(), P)
+        np.testing.assert_array_equal(real[b:b + 1].cpu().numpy(), ref["seq_lens"])
+        np.testing.assert_array_equal(padded[b:b + 1].cpu().numpy(), ref["seq_lens_padded"])
+        np.testing.assert_array_equal(pos[b:b + 1].cpu().numpy(), ref["position_ids"])
+    del d, real, padded, pos
