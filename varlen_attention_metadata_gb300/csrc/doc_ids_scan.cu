@@ -38,7 +38,6 @@ namespace {
 #define PSEQ_SCAN_ITEMS 16
 #endif
 constexpr int kThreads = PSEQ_SCAN_THREADS;
-constexpr int kWarps = kThreads / 32;
 constexpr int kItems = PSEQ_SCAN_ITEMS;
 constexpr int kPerLane = 1;  // look-back windows of 32 tiles polled together (more unrolled code costs more on a cold instruction cache than extra rounds)
 constexpr int kTile = kThreads * kItems;  // tokens per tile
