@@ -295,6 +295,8 @@ pseq_status pack_ffd(const int64_t* lens, int64_t n, int64_t multiple,
  * workspace: pseq_doc_ids_to_lengths_workspace_size(B, S) bytes, 16-byte
  *   aligned, ZERO-FILLED before its first use; every call leaves it zero
  *   again (calls sharing one must be ordered).  At most 65535 rows per call.
+ * Host errors: PSEQ_ERR_OVERFLOW when B*S or B*num_packs exceeds INT32_MAX
+ *   or S exceeds 2^31 - 1 - 4096.
  * Device errors also include PSEQ_ERR_TIMEOUT (a chunk's wait for the chunks
  *   before it in its row hit the cap set by pseq_debug_set_wait).
  * ---------------------------------------------------------------------- */

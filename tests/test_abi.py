@@ -74,6 +74,15 @@ def test_host_argument_errors_without_gpu(lib):
                             fake, 1 << 20, None) == _lib.PSEQ_ERR_ARG
     assert lib.pack_squeeze(fake, 2, 2, 8, fake, fake, fake, 1, 2, 4, 16, 1, 8, 0, fake, fake, fake, fake, fake,
                             fake, 1 << 20, None) == _lib.PSEQ_ERR_ARG  # stretch needs width >= capacity
+    # size limits
+    assert lib.pack_squeeze(fake, 2, 2, 8, fake, fake, fake, 1, 2, 4, 8, 0, 2**31 - 65535, 0, fake, fake, fake, fake,
+                            fake, fake, 1 << 20, None) == _lib.PSEQ_ERR_OVERFLOW  # width past 2^31 - 2^16
+    assert lib.pack_squeeze(fake, 2, 2, 8, fake, fake, fake, 65536, 65536, 4, 8, 0, 8, 0, fake, fake, fake, fake,
+                            fake, fake, 1 << 20, None) == _lib.PSEQ_ERR_ARG  # more bins than the grid holds
+    assert lib.thd_mask_from_token_ids(fake, 4, 2**31, 0, fake, fake, fake, 1 << 20, None) == _lib.PSEQ_ERR_OVERFLOW
+    assert lib.pack_ffd(fake, 8193, 1, 100, fake, fake, fake, None) == _lib.PSEQ_ERR_ARG
+    assert lib.pseq_doc_ids_to_lengths(fake, 4, 1, 2**31 - 4000, 4, -1000, fake, fake, None, fake, fake, 1 << 20,
+                                       None) == _lib.PSEQ_ERR_OVERFLOW  # one row within a chunk of INT32_MAX
     assert lib.pseq_version() >= 100
 
 

@@ -430,6 +430,7 @@ extern "C" pseq_status pseq_doc_ids_to_lengths(const void* doc_ids, int32_t id_b
   if (B < 0 || S < 0 || num_packs < 0) return fail(PSEQ_ERR_ARG, "%s: negative size", fn);
   if (id_bytes != 4 && id_bytes != 8) return fail(PSEQ_ERR_ARG, "%s: id_bytes must be 4 or 8", fn);
   if (B > 0 && S > INT32_MAX / B) return fail(PSEQ_ERR_OVERFLOW, "%s: B*S exceeds INT32_MAX", fn);
+  if (S > INT32_MAX - kTile) return fail(PSEQ_ERR_OVERFLOW, "%s: S exceeds 2^31 - 1 - %d", fn, kTile);
   if (B > 0 && num_packs > INT32_MAX / B) return fail(PSEQ_ERR_OVERFLOW, "%s: B*num_packs exceeds INT32_MAX", fn);
   if (B > 65535) return fail(PSEQ_ERR_ARG, "%s: at most 65535 rows per call", fn);
   if (!info || (B * S > 0 && !doc_ids) || (B * num_packs > 0 && (!seq_lens || !seq_lens_padded)))
