@@ -18,6 +18,9 @@ void count_launches(int n);
 // Resident CTAs per SM of `kernel` at `threads` and `smem` bytes of dynamic
 // shared memory (cached per device).
 int occupancy(const void* kernel, int threads, size_t smem);
+// Raise `kernel`'s dynamic shared memory limit to `bytes` on the current
+// device, once per (device, kernel); safe to call from several host threads.
+cudaError_t allow_dynamic_smem(const void* kernel, size_t bytes);
 int sm_count();
 int64_t wait_limit_ns();
 int64_t withhold_tile();

@@ -322,14 +322,8 @@ extern "C" pseq_status pack_ffd(const int64_t* lens, int64_t n, int64_t multiple
   if (!aligned(lens, 8) || !aligned(bin_offsets, 4) || !aligned(bin_members, 4) || !aligned(info, 4))
     return fail(PSEQ_ERR_ARG, "%s: misaligned pointer", fn);
   const size_t smem = ffd_smem((int)n);
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(ffd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ffd_smem(kMaxItems));
-    if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
-    attr_set[dev] = true;
-  }
+  const cudaError_t ea = allow_dynamic_smem(reinterpret_cast<const void*>(ffd_kernel), ffd_smem(kMaxItems));
+  if (ea != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(ea));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = launch_pdl(ffd_kernel, dim3(1), dim3(kThreads), smem, st, lens, (int)n, multiple, capacity,
                                    bin_offsets, bin_members, info);

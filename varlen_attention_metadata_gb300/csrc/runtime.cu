@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <map>
 #include <mutex>
+#include <set>
 #include <tuple>
 
 #include "common.cuh"
@@ -52,6 +53,20 @@ int occupancy(const void* kernel, int threads, size_t smem) {
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1) n = 1;
   cache[key] = n;
   return n;
+}
+
+cudaError_t allow_dynamic_smem(const void* kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::set<std::tuple<int, const void*, size_t>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const auto key = std::make_tuple(dev, kernel, bytes);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) done.insert(key);
+  return e;
 }
 
 int sm_count() {

@@ -334,13 +334,9 @@ __global__ void empty_squeeze_kernel(pseq_info* info) {
 
 template <int SLOTS, int EB, bool VEC>
 cudaError_t launch_squeeze(const Args& a, unsigned gy, cudaStream_t st) {
-  static bool configured = false;  // per process; the attribute is per function
-  if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(squeeze_kernel<SLOTS, EB, VEC>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)table_bytes<SLOTS>());
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  const cudaError_t e =
+      allow_dynamic_smem(reinterpret_cast<const void*>(squeeze_kernel<SLOTS, EB, VEC>), table_bytes<SLOTS>());
+  if (e != cudaSuccess) return e;
   constexpr int64_t w = window<SLOTS>();
   const unsigned gx = a.out && a.width > 0 ? (unsigned)((a.width + w - 1) / w) : 1u;
   return launch_pdl(squeeze_kernel<SLOTS, EB, VEC>, dim3(gx, gy), dim3(kThreads), table_bytes<SLOTS>(), st, a);

@@ -684,15 +684,9 @@ pseq_status launch_fused(const char* fn, const MetaArgs& a, const Fields& f, uin
   if (f.bulk) {
     // one CTA per SM; the ring of bulk-copy buffers sits in front of the tables
     const size_t smem = (size_t)kStages * kStage + table_bytes(a.B, a.P);
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-      e = cudaFuncSetAttribute(thd_fused_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)((size_t)kStages * kStage + table_bytes(kFusedMaxEntries, 1)));
-      if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
-      attr_set[dev] = true;
-    }
+    e = allow_dynamic_smem(reinterpret_cast<const void*>(thd_fused_bulk_kernel),
+                           (size_t)kStages * kStage + table_bytes(kFusedMaxEntries, 1));
+    if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
     e = launch_pdl(thd_fused_bulk_kernel, dim3((unsigned)bulk_ctas(), (unsigned)a.chunks), dim3(kRowThreads), smem, st,
                    a, f, mask, mask_cap, wait_limit_ns());
   } else {
