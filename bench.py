@@ -231,8 +231,6 @@ class NativeStep:
         args = (self._p(dreal), self._p(dpad), B, S, P, -1000, 1, fields, k, self._p(cu), self._p(cup),
                 self._p(mask), self._p(info, 16), self._p(info), self._p(ws), ws.numel(), self.sh)
         self.calls.append((name, lib.thd_from_batch, args))
-        if name == "thd_emb":
-            self.emb_side_args = args[:-1] + (self.side_sh,)
         self._finish[name] = lambda: (info, cu, cup, mask, dsts)
 
     def _squeeze(self, name, c):
@@ -282,28 +280,32 @@ class NativeStep:
         # a larger squeeze, timed on its own only (never part of the step)
         if self.only is not None and self._want("squeeze_scaled"):
             self._squeeze("squeeze_scaled", h["squeeze_scaled"])
+        # the same calls with the side stream's handle (every ABI call takes its stream last)
+        self.side_calls = [(name, fn, args[:-1] + (self.side_sh,)) for name, fn, args in self.calls]
         self.torch.cuda.synchronize(self.dev)
 
     def run(self, emb_events=None, two_streams=False):
         """Issue one step; optionally bracket the embedding call with events.
 
-        With two_streams the embedding conversion is issued first on the side
-        stream (forked from and joined back into self.stream), so the other
-        calls run next to it while it streams its 537 MB."""
+        The embedding conversion goes first, on self.stream.  With two_streams
+        the other calls go to the side stream (forked from and joined back
+        into self.stream), so they run next to it while it streams its
+        537 MB: issued first, with no cross-stream wait in front of it, the
+        embedding call's CTAs take their SMs before the small calls' CTAs
+        arrive, and the small calls fill the SMs it leaves free."""
         two = two_streams and self.side is not None
         if two:
             self._fork.record(self.stream)
             self.side.wait_event(self._fork)
-        emb = self.side if two else self.stream
         for name, fn, args in self.calls:
             if name != "thd_emb":
                 continue
             if emb_events is not None:
-                emb_events[0].record(emb)
-            self._ok(name, fn(*(self.emb_side_args if two else args)))
+                emb_events[0].record(self.stream)
+            self._ok(name, fn(*args))
             if emb_events is not None:
-                emb_events[1].record(emb)
-        for name, fn, args in self.calls:
+                emb_events[1].record(self.stream)
+        for name, fn, args in (self.side_calls if two else self.calls):
             if name != "thd_emb":
                 self._ok(name, fn(*args))
         if two:
@@ -829,9 +831,9 @@ def run_native(args, dist: Dist):
                 "l2": "flushed between steps outside the timed events (256 MiB write, then 256 MiB read of another buffer)",
                 "parallelism": f"replicas x{dist.world} (independent batches per GPU)",
                 "algorithmic_bytes_per_step": sum(step.alg_bytes.values()),
-                "launch": "direct C ABI calls from prebuilt ctypes arguments; the embedding conversion on a "
-                          "second stream forked from and joined into the step's stream, the other five calls on "
-                          "the step's stream",
+                "launch": "direct C ABI calls from prebuilt ctypes arguments; the embedding conversion first "
+                          "on the step's stream, the other five calls on a second stream forked from and joined "
+                          "back into it",
                 "ms_per_step_one_stream": round(one_stream_ms, 6),
                 "ms_per_step_graph": round(graph_ms, 6) if graph_ms else None,
                 "graph": "the same two-stream step captured once in a CUDA graph and replayed (fork and join "
@@ -849,7 +851,7 @@ def run_native(args, dist: Dist):
                 "traffic": traffic,
                 "algorithmic_bytes_per_launch": step.emb_bytes,
                 "avg_launch_us": round(emb_avg_ms * 1e3, 3),
-                "timed_as": f"CUDA events on the side stream around the call, on every {EMB_SAMPLE}th timed step "
+                "timed_as": f"CUDA events on the step's stream around the call, on every {EMB_SAMPLE}th timed step "
                             f"({len(emb_ms)} launches; the event pair costs about 4 us of step time, so it is "
                             "not recorded on every step)",
             },

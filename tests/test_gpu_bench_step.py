@@ -1,8 +1,8 @@
 """The step exactly as bench.py times it, checked against the oracle.
 
 bench.py issues the five workloads' calls from prebuilt ctypes arguments, the
-embedding conversion on a second stream beside the other calls, step after
-step on the same buffers and workspaces.  These tests run that object
+embedding conversion first on the step's stream and the other calls beside it
+on a second stream, step after step on the same buffers and workspaces.  These tests run that object
 (``bench.NativeStep``) and compare every output of every call with the oracle
 element by element, after two-stream steps and after a one-stream step.
 """
