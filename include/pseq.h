@@ -108,7 +108,7 @@ pseq_status pseq_from_doc_ids(const void* doc_ids, int32_t id_bytes, int64_t B,
  * callback that is handed only input and output pointers, or a process that
  * has reserved all of HBM up front.  This entry point takes the same inputs
  * and outputs as pseq_from_doc_ids and no workspace.  Its scratch is a
- * static device array of about 32 KiB inside libpseq.so, which every GPU
+ * static device array of about 128 KiB inside libpseq.so, which every GPU
  * that loads the library holds until the process exits.
  *  - B*S must not exceed PSEQ_STATIC_MAX_TOKENS; larger maps get
  *    PSEQ_ERR_ARG before anything is enqueued (use pseq_from_doc_ids).
