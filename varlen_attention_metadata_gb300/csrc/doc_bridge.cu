@@ -201,6 +201,30 @@ __device__ __forceinline__ Marks row_prefix(const BridgeArgs& a, const Slot* row
   return run;
 }
 
+// Position ids of this thread's tokens [k_lo, k_hi): the distance to the
+// latest run start (lr: the one before the thread's first token), 0 on
+// padding.  Two per 16-byte store where the row allows it.
+__device__ __forceinline__ void write_positions(int64_t* prow, int S, int s0, unsigned runs, unsigned nz, int lr,
+                                                int k_lo, int k_hi) {
+  if (s0 + kItems <= S && (reinterpret_cast<uintptr_t>(prow + s0) & 15) == 0) {
+#pragma unroll
+    for (int k = 0; k < kItems; k += 2) {
+      if (runs & (1u << k)) lr = s0 + k;
+      const int p0 = (nz >> k) & 1u ? s0 + k - lr : 0;
+      if (runs & (2u << k)) lr = s0 + k + 1;
+      const int p1 = (nz >> (k + 1)) & 1u ? s0 + k + 1 - lr : 0;
+      if (k >= k_lo && k < k_hi) st_stream(reinterpret_cast<int4*>(prow + s0 + k), make_int4(p0, 0, p1, 0));
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+      if (s0 + k >= S) break;
+      if (runs & (1u << k)) lr = s0 + k;
+      if (k >= k_lo && k < k_hi) prow[s0 + k] = (nz >> k) & 1u ? s0 + k - lr : 0;
+    }
+  }
+}
+
 // The last CTA: fold every chunk's record into the info block.
 __device__ __noinline__ void fold_stats(const BridgeArgs& a) {
   const int tid = threadIdx.x, lane = tid & 31;
@@ -277,6 +301,16 @@ __global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restric
   }
   __syncthreads();
   const Marks chunk_sum = s_warp[kThreads / 32 - 1];
+  // marks of the chunk's tokens before this thread's (the row prefix joins later)
+  Marks before = shfl_up(inc, 1);
+  if (lane == 0) before = {0, -1, -1};
+  if (warp > 0) before = join(s_warp[warp - 1], before);
+  // Positions after the chunk's first run start do not depend on the row
+  // prefix: write them now, while warp 0 looks back.  Only the pairs before
+  // this thread's first known run start wait for the prefix.
+  int64_t* prow = a.positions ? a.positions + (int64_t)row * S : nullptr;
+  const int known = before.last_run >= 0 ? 0 : (runs ? (__ffs(runs) - 1 + 1) & ~1 : kItems);
+  if (prow) write_positions(prow, S, s0, runs, nz, before.last_run, known, kItems);
   // publish this chunk's summary, then the row prefix from the chunks before it
   if (warp == 0) {
     Slot* row_slots = a.slots + (int64_t)row * a.chunks;
@@ -301,9 +335,6 @@ __global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restric
       s_prefix = prefix;
     }
   }
-  Marks before = shfl_up(inc, 1);
-  if (lane == 0) before = {0, -1, -1};
-  if (warp > 0) before = join(s_warp[warp - 1], before);
   __syncthreads();
   const Marks prefix = s_prefix;
   before = join(prefix, before);
@@ -334,28 +365,8 @@ __global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restric
       count += 1;
     }
   }
-  // positions: count from the latest run start, two per 16-byte store
-  if (a.positions) {
-    int64_t* prow = a.positions + (int64_t)row * S;
-    int lr = before.last_run;
-    if (s0 + kItems <= S && (reinterpret_cast<uintptr_t>(prow + s0) & 15) == 0) {
-#pragma unroll
-      for (int k = 0; k < kItems; k += 2) {
-        if (runs & (1u << k)) lr = s0 + k;
-        const int p0 = (nz >> k) & 1u ? s0 + k - lr : 0;
-        if (runs & (2u << k)) lr = s0 + k + 1;
-        const int p1 = (nz >> (k + 1)) & 1u ? s0 + k + 1 - lr : 0;
-        st_stream(reinterpret_cast<int4*>(prow + s0 + k), make_int4(p0, 0, p1, 0));
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < kItems; ++k) {
-        if (s0 + k >= S) break;
-        if (runs & (1u << k)) lr = s0 + k;
-        prow[s0 + k] = (nz >> k) & 1u ? s0 + k - lr : 0;
-      }
-    }
-  }
+  // the positions that waited for the row prefix
+  if (prow && known > 0) write_positions(prow, S, s0, runs, nz, before.last_run, 0, known);
   // one shared atomic per warp for the longest document run
 #pragma unroll
   for (int dd = 16; dd > 0; dd >>= 1) longest = max(longest, __shfl_xor_sync(~0u, longest, dd));
