@@ -359,6 +359,11 @@ def test_thd_split_calls_match_whole():
     c = synth.thd_ids(3)
     S = c["input_ids"].shape[1]
     m = v.thd_meta(dev(c["seq_lens"]), dev(c["seq_lens_padded"]), S)
+    # another conversion of the same size on the same stream in between: the
+    # layout thd_gather reads must be the one thd_meta left
+    c2 = synth.thd_ids(4)
+    v.thd_from_batch(dev(c2["seq_lens"]), dev(c2["seq_lens_padded"]), S, [(dev(c2["input_ids"]), 1)])
+    v.thd_meta(dev(c2["seq_lens"]), dev(c2["seq_lens_padded"]), S)
     g = v.thd_gather(m, [(dev(c["input_ids"]), 1)])
     st, n, mx, T = info_of(m["info"])
     meta = oracle.thd_meta(c["seq_lens"], c["seq_lens_padded"], S)

@@ -237,7 +237,10 @@ def thd_meta(seq_lens, seq_lens_padded, S: int, pad_value: int = -1000, absorb_t
     cu = torch.empty(B * P + 1, dtype=torch.int32, device=dev)
     cup = torch.empty(B * P + 1, dtype=torch.int32, device=dev) if seq_lens_padded is not None else None
     info = _new_info(dev)
-    ws = _workspaces.get("thd", lib.thd_workspace_size(B, P), dev)
+    # the layout stays in this workspace until thd_gather reads it, so it is
+    # the caller's (held in the returned dict), not the per-stream cached one
+    # that the next conversion on the stream would overwrite
+    ws = torch.empty(lib.thd_workspace_size(B, P), dtype=torch.uint8, device=dev)
     _lib.check(lib.thd_meta(_p(seq_lens), _p(seq_lens_padded), B, S, P, pad_value, 1 if absorb_trailing_pad else 0,
                             _p(cu), _p(cup), ctypes.c_void_p(info.data_ptr() + 16), _p(info), _p(ws), ws.numel(),
                             _stream(dev)))
