@@ -796,10 +796,11 @@ def run_native(args, dist: Dist):
     next_rows = time_next_rows(dev, stream, args.seed + dist.rank, flush_l2) if dist.rank == 0 else None
 
     peak, peak_kind = measured_peak()
-    per_config = torch_gpu = None
+    per_config = torch_gpu = launch_floor = None
     if dist.rank == 0:
         host["squeeze_scaled"] = synth.squeeze(args.seed, N=16384)
         per_config = time_per_config(step, host, dev, stream, flush_l2, peak)
+        launch_floor = time_launch_floor(dev, stream, flush_l2)
         torch_gpu = time_torch_restatement(host, dev, stream, flush_l2, per_config)
     emb_avg_ms = statistics.mean(emb_ms)
     achieved = step.emb_bytes / (emb_avg_ms / 1e3) / 1e9
@@ -869,6 +870,7 @@ def run_native(args, dist: Dist):
                                      "step's host bytes per second over the both-directions figure")},
             "next_rows": next_rows,
             "per_config": per_config,
+            "launch_floor": launch_floor,
             "torch_gpu_restatement": {
                 "what": "each call restated as plain PyTorch ops on the same GPU (boolean filtering, cumsum, "
                         "nonzero, index gathers; bench-only, not the product path), cold: L2 flushed first, "
@@ -1027,6 +1029,43 @@ def time_per_config(step, host, dev, stream, flush_l2, peak, warm=20, reps=200) 
             del base
             torch.cuda.empty_cache()
     return out
+
+
+def time_launch_floor(dev, stream, flush_l2, warm=20, reps=200) -> dict:
+    """The library's smallest launch, timed like the configurations'
+    ``cold_us`` and ``graph_us``: ``pseq_from_doc_ids`` on an empty map
+    (B = 0), one single-thread kernel writing ``cu_seqlens[0]`` and the info
+    block.  What is left of a small call's cold time above this is its own."""
+    import torch
+
+    import varlen_attention_metadata_gb300 as v
+
+    lib = v.load_library()
+    cu = torch.zeros(16, dtype=torch.int32, device=dev)
+    info = torch.zeros(8, dtype=torch.int32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    d = torch.zeros(1, dtype=torch.int32, device=dev)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    args = (P(d), 4, 0, 1, P(cu), P(info), P(ws), ws.numel(), ctypes.c_void_p(stream.cuda_stream))
+    fn = lib.pseq_from_doc_ids
+    ts = []
+    with torch.cuda.stream(stream):
+        for i in range(warm + reps):
+            flush_l2()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            st = fn(*args)
+            b.record(stream)
+            if st != 0:
+                raise RuntimeError(f"empty map: status {st}")
+            if i >= warm:
+                ts.append((a, b))
+    torch.cuda.synchronize(dev)
+    cold = statistics.median(a.elapsed_time(b) * 1e3 for a, b in ts)
+    graph = _graph_us([(fn, args)] * 200, dev, stream, flush_l2) / 200
+    return {"what": "pseq_from_doc_ids on an empty map: one single-thread kernel, the library's smallest launch, "
+                    "timed as the configurations' cold_us and graph_us",
+            "cold_us": round(cold, 2), "graph_us": round(graph, 2)}
 
 
 # ----------------------------------------------------------------------------
