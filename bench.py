@@ -855,6 +855,11 @@ def run_native(args, dist: Dist):
                 "timed_as": f"CUDA events on the step's stream around the call, on every {EMB_SAMPLE}th timed step "
                             f"({len(emb_ms)} launches; the event pair costs about 4 us of step time, so it is "
                             "not recorded on every step)",
+                "whole_step": {"achieved": round(sum(step.alg_bytes.values()) / (ms_per_step / 1e3) / 1e9, 1),
+                               "frac": round(sum(step.alg_bytes.values()) / (ms_per_step / 1e3) / 1e9 / peak, 4),
+                               "what": "algorithmic bytes of all six calls per step over ms_per_step: the step "
+                                       "as one bandwidth-bound unit (the dominant kernel shares HBM with the "
+                                       "other five calls inside it)"},
             },
             "cpu_baseline": cpu,
             "e2e": {"value": round(all_tokens / (pipe_ms / 1e3), 1), "unit": UNIT,
