@@ -20,8 +20,8 @@
 // predecessors per poll round, stopping at the nearest inclusive prefix,
 // bounded waits).  It then walks its tokens: every run end writes its
 // sequence's real length, every sequence start closes the padded length of
-// the one before it, and the row's last chunk closes the row and fills unused
-// slots.  Each chunk writes its own statistics record; the CTA that finishes
+// the one before it, and the row's last chunk closes the row; the row's
+// other chunks then share the fill of its unused slots.  Each chunk writes its own statistics record; the CTA that finishes
 // last (a wrapping acq_rel counter) folds the records into the info block
 // and clears the summary words, so the workspace is zero again for the next
 // call.
@@ -266,7 +266,7 @@ template <typename Id>
 __global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restrict__ doc, const __grid_constant__ BridgeArgs a) {
   __shared__ Marks s_warp[kThreads / 32];
   __shared__ Marks s_prefix;
-  __shared__ int s_longest, s_overflow, s_last;
+  __shared__ int s_longest, s_overflow, s_last, s_used;
   pdl_enter();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.y, ch = blockIdx.x;
@@ -381,10 +381,45 @@ __global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restric
     }
     if (total - 1 < P) pad_out[total - 1] = S - row_so_far.last_seq;
   }
-  if (row_end) {
+  // The row's unused slots [used, P) take pad_value.  With one chunk per row
+  // that chunk fills them.  Otherwise the row's other chunks share the fill:
+  // each waits for the last chunk's inclusive summary (the row's sequence
+  // count, published right after that chunk's look-back; the last chunk is
+  // dispatched right after them and waits only on earlier chunks) and fills
+  // one share, so the last chunk is not left with the whole fill.  The walk
+  // writes only slots below `used`, so the fill never meets it.
+  if (a.chunks == 1) {
     const int used = min(row_so_far.seqs, P);
     block_fill(real_out + used, P - used, 8, a.pad_value);
     block_fill(pad_out + used, P - used, 8, a.pad_value);
+  } else if (!row_end) {
+    if (tid == 0) {
+      const Slot* last = a.slots + (int64_t)row * a.chunks + (a.chunks - 1);
+      int used = -1, polls = 0;
+      uint64_t start = 0;
+      while (true) {
+        const unsigned long long ia = ld_relaxed_u64(&last->inc_a), ib = ld_relaxed_u64(&last->inc_b);
+        if (ia & ib & kValid) {
+          used = min(from_words(ia, ib).seqs, P);
+          break;
+        }
+        if (polls++ == 0) {
+          start = global_ns();
+        } else if ((int64_t)(global_ns() - start) >= a.wait_ns) {
+          atomicOr(&a.hdr->gave_up, 1u);  // reported as PSEQ_ERR_TIMEOUT; the share is left unfilled
+          break;
+        }
+      }
+      s_used = used;
+    }
+    __syncthreads();
+    const int used = s_used;
+    if (used >= 0) {
+      const int64_t rest = P - used, shares = a.chunks - 1;
+      const int64_t lo = used + rest * ch / shares, hi = used + rest * (ch + 1) / shares;
+      block_fill(real_out + lo, hi - lo, 8, a.pad_value);
+      block_fill(pad_out + lo, hi - lo, 8, a.pad_value);
+    }
   }
   __syncthreads();
   const int64_t linear = (int64_t)row * a.chunks + ch;
