@@ -298,7 +298,8 @@ pseq_status pack_ffd(const int64_t* lens, int64_t n, int64_t multiple,
  * Host errors: PSEQ_ERR_OVERFLOW when B*S or B*num_packs exceeds INT32_MAX
  *   or S exceeds 2^31 - 1 - 4096.
  * Device errors also include PSEQ_ERR_TIMEOUT (a chunk's wait for the chunks
- *   before it in its row hit the cap set by pseq_debug_set_wait).
+ *   before it in its row, or for the row's last chunk before filling its
+ *   share of the unused slots, hit the cap set by pseq_debug_set_wait).
  * ---------------------------------------------------------------------- */
 size_t pseq_doc_ids_to_lengths_workspace_size(int64_t B, int64_t S);
 pseq_status pseq_doc_ids_to_lengths(const void* doc_ids, int32_t id_bytes,
