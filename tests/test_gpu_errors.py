@@ -49,7 +49,12 @@ def test_lookback_wait_gives_up_and_reports():
     assert p.max_seqlen == ref_mx
 
 
-def test_bridge_wait_gives_up_and_reports():
+@pytest.mark.parametrize("withheld", [5, 7])
+def test_bridge_wait_gives_up_and_reports(withheld):
+    """Chunk 5 (row 1, chunk 1): the row's later chunks run their look-back
+    waits out.  Chunk 7 (row 1's last chunk): the row's other chunks run out
+    their wait for its summary before filling their shares of the unused
+    slots."""
     import varlen_attention_metadata_gb300 as v
 
     lib = v.load_library()
@@ -57,7 +62,7 @@ def test_bridge_wait_gives_up_and_reports():
     d = synth.random_doc_ids(rng, 2, 4 * 4096, "runs", np.int32)  # 2 rows of 4 chunks
     dt = torch.from_numpy(d).to(DEV)
     try:
-        lib.pseq_debug_set_wait(1_000_000, 5)  # row 1, chunk 1 never publishes
+        lib.pseq_debug_set_wait(1_000_000, withheld)  # that chunk never publishes
         _, _, _, info = v.pseq_doc_ids_to_lengths(dt, 4 * 4096)
         assert info[:16].view(torch.int32).tolist()[0] == v._lib.PSEQ_ERR_TIMEOUT
     finally:
