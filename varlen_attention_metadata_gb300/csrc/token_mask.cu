@@ -6,8 +6,9 @@
 // correctly only if the pad positions form a suffix of the stream, so the
 // kernel checks that and reports a pad id that also occurs as content.
 //
-// One pass.  Each thread compares eight consecutive ids (16-byte loads) and
-// stores their eight mask bytes at once; each CTA reduces the first pad
+// One pass.  Each thread compares groups of eight consecutive ids (16-byte
+// loads), two groups per round with both loads in flight, and stores each
+// group's eight mask bytes at once; each CTA reduces the first pad
 // position, the last non-pad position and the pad count of its part and
 // writes them to its own workspace slot.  The CTA that finishes last (an
 // acq_rel counter that wraps back to zero) folds the slots: the input is
@@ -45,20 +46,25 @@ __global__ void __launch_bounds__(kThreads)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t groups = (n + kGroup - 1) / kGroup;
   long long first_pad = n, last_content = -1, pads = 0;
-  for (int64_t g = (int64_t)blockIdx.x * kThreads + tid; g < groups; g += (int64_t)gridDim.x * kThreads) {
+  // Two groups per round, both loads issued before either is examined, so a
+  // thread with a second group (the grid is one wave) pays one load latency.
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  auto load_group = [&](int64_t g, Id* v) {
     const int64_t t0 = g * kGroup;
-    Id v[kGroup];
     if (kVector && t0 + kGroup <= n) {
       constexpr int kVec = kGroup * sizeof(Id) / 16;
       const int4* p = reinterpret_cast<const int4*>(ids + t0);
       int4 q[kVec];
 #pragma unroll
       for (int k = 0; k < kVec; ++k) q[k] = ld_stream(p + k);
-      memcpy(v, q, sizeof(v));
+      memcpy(v, q, sizeof(Id) * kGroup);
     } else {
 #pragma unroll
       for (int k = 0; k < kGroup; ++k) v[k] = t0 + k < n ? ids[t0 + k] : pad;
     }
+  };
+  auto do_group = [&](int64_t g, const Id* v) {
+    const int64_t t0 = g * kGroup;
     // one bit per id: which are the pad id; the group's statistics from the bits
     const int live = t0 + kGroup <= n ? kGroup : (int)(n - t0);
     const unsigned valid = live >= 32 ? ~0u : ((1u << live) - 1u);
@@ -81,6 +87,14 @@ __global__ void __launch_bounds__(kThreads)
     } else {
       for (int k = 0; k < live; ++k) mask[t0 + k] = (uint8_t)((padbits >> k) & 1u);
     }
+  };
+  for (int64_t g0 = (int64_t)blockIdx.x * kThreads + tid; g0 < groups; g0 += 2 * stride) {
+    const int64_t g1 = g0 + stride;
+    Id v0[kGroup], v1[kGroup];
+    load_group(g0, v0);
+    if (g1 < groups) load_group(g1, v1);
+    do_group(g0, v0);
+    if (g1 < groups) do_group(g1, v1);
   }
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) {
