@@ -535,6 +535,27 @@ def test_squeeze_bins_denser_than_a_window():
     check_squeeze(one, 1, need, False, need)
 
 
+@pytest.mark.parametrize("dtype,m", [(np.int64, 2), (np.int64, 3), (np.int8, 16), (np.int16, 5)])
+@pytest.mark.parametrize("bins", [3, 64])
+def test_squeeze_window_meets_the_most_members(dtype, m, bins):
+    # every member padded to exactly `multiple` slots: a window meets
+    # ceil(window / multiple) + 1 members, the most its table is sized for
+    # (3 bins: narrow windows; 64 bins: enough CTAs for the wide ones)
+    rng = np.random.default_rng(1000 * m + bins)
+    per_bin = 16400 // m + 1
+    N = bins * per_bin
+    info = np.iinfo(dtype)
+    prob = {"src": rng.integers(max(info.min, -30000), min(info.max, 30000), size=(N, m)).astype(dtype),
+            "real_lens": rng.integers(1, m + 1, size=N).astype(np.int64)}
+    perm = rng.permutation(N).astype(np.int32)
+    prob["bin_members"] = perm
+    prob["bin_offsets"] = (np.arange(bins + 1) * per_bin).astype(np.int32)
+    need = per_bin * m
+    width = -(-need // 16) * 16
+    check_squeeze(prob, m, width, True, width, pad_value=-3)
+    check_squeeze(prob, m, need, False, need + 1)
+
+
 def test_squeeze_wide_windows():
     # enough (window, bin) CTAs that the 16-slot-per-thread kernel runs
     c = synth.squeeze(3, N=2048)

@@ -9,9 +9,11 @@
 // One launch over (slot window, bin) CTAs.  Every CTA scans its bin's members
 // (padded lengths, both cumulative sums) and keeps in shared memory only the
 // members whose padded range meets its window of output slots.  Those ranges
-// are disjoint and non-empty, so the table never holds more entries than the
-// window has slots, whatever the number of members.  Each thread then owns
-// kSlots slots of the window (interleaved across the CTA, so that a warp's
+// are disjoint and each at least `multiple` slots long, so the table never
+// holds more than min(window, window / multiple + 2) entries, whatever the
+// number of members; the launch sizes it so, which keeps shared memory from
+// limiting the CTAs resident on an SM.  Each thread then owns
+// a fixed number of slots of the window (interleaved across the CTA, so that a warp's
 // accesses are contiguous): it looks up the member of each slot, issues every
 // load before any store, and writes the token or pad_value with its mask
 // byte.  Every output slot is written exactly once.
@@ -26,8 +28,15 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kSlotsWide = 16;   // slots per thread on large outputs
 constexpr int kSlotsNarrow = 4;  // slots per thread when the grid would be small
+
+// Slots per thread on large outputs: 12 (six 16-byte vectors of 8-byte
+// elements) lets six CTAs share an SM; 1- and 2-byte elements keep 16 so that
+// a thread's slots still make whole 16-byte vectors.
+template <int EB>
+__host__ __device__ constexpr int slots_wide() {
+  return EB >= 4 ? 12 : 16;
+}
 
 struct Header {
   unsigned finished;
@@ -45,10 +54,11 @@ __host__ __device__ constexpr int window() {
   return kThreads * SLOTS;
 }
 
-template <int SLOTS>
-__host__ __device__ constexpr size_t table_bytes() {
-  return 3 * sizeof(int32_t) * (size_t)window<SLOTS>();
-}
+// A member table entry: output start, real length, source row (int32 each).
+constexpr size_t kEntryBytes = 3 * sizeof(int32_t);
+
+// Entries a window of w slots can meet: disjoint ranges, each >= multiple long.
+inline int table_entries(int64_t w, int64_t multiple) { return (int)min(w, w / multiple + 2); }
 
 struct Args {
   const unsigned char* src;
@@ -134,13 +144,17 @@ __device__ __noinline__ void fold_records(const Args& a) {
   }
 }
 
+// `cap` = table_entries(window, multiple): the table's length in entries.
+// Wide windows: five (16 slots) or six (12 slots) CTAs per SM, so that some
+// stream while others scan their tables; narrow grids fill less than a wave.
 template <int SLOTS, int EB, bool VEC>
-__global__ void __launch_bounds__(kThreads, SLOTS >= 16 ? 3 : 4) squeeze_kernel(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(kThreads, SLOTS >= 16 ? 5 : (SLOTS >= 12 ? 6 : 4))
+    squeeze_kernel(const __grid_constant__ Args a, int cap) {
   extern __shared__ __align__(16) int32_t s_table[];
   constexpr int kWindow = window<SLOTS>();
   int32_t* s_dst = s_table;
-  int32_t* s_real = s_table + kWindow;
-  int32_t* s_src = s_table + 2 * kWindow;
+  int32_t* s_real = s_table + cap;
+  int32_t* s_src = s_table + 2 * cap;
   __shared__ Triple scratch[kWarps];
   __shared__ int s_count[kWarps];
   __shared__ int s_bad, s_longest, s_last;
@@ -150,8 +164,9 @@ __global__ void __launch_bounds__(kThreads, SLOTS >= 16 ? 3 : 4) squeeze_kernel(
   const bool first = blockIdx.x == 0;
   const int lo = __ldg(a.off + b), hi = __ldg(a.off + b + 1);
   const bool bad_offsets = offsets_bad(a, b, lo, hi);
-  const int64_t c0 = (int64_t)blockIdx.x * kWindow;
-  const int64_t c1 = min(c0 + (int64_t)kWindow, a.width);
+  // the window [c0, c1): width < 2^31 - 2^16 (host check), so int32 holds both
+  const int32_t c0 = (int32_t)(blockIdx.x * (unsigned)kWindow);
+  const int32_t c1 = (int32_t)min((int64_t)c0 + kWindow, a.width);
   if (tid == 0) {
     s_bad = 0;
     s_longest = 0;
@@ -225,10 +240,10 @@ __global__ void __launch_bounds__(kThreads, SLOTS >= 16 ? 3 : 4) squeeze_kernel(
   const T* src = reinterpret_cast<const T*>(a.src);
   T* row = reinterpret_cast<T*>(a.out) + (int64_t)b * a.width;
   uint8_t* mrow = a.mask ? a.mask + (int64_t)b * a.width : nullptr;
-  const int32_t lim = (int32_t)min((long long)c1, total_pad);  // slots below are in members
-  const int32_t end = (int32_t)c1;
   const T pv = (T)(uint64_t)a.pad_value;
   int j = 0;
+  const int32_t lim = (int32_t)min((long long)c1, total_pad);  // slots below are in members
+  const int32_t end = c1;
   if constexpr (VEC) {
     // 16-byte vectors of V slots.  The host takes this path only when row
     // pitches, width and multiple keep every member start on a vector
@@ -243,13 +258,14 @@ __global__ void __launch_bounds__(kThreads, SLOTS >= 16 ? 3 : 4) squeeze_kernel(
     int4 pad4;
     memcpy(&pad4, pad_elems, 16);
     int4 v[NV];
-    int nreal[NV];
-    const int32_t base = (int32_t)c0 + tid * V;
+    uint32_t nreal[(NV + 3) / 4];  // real slots of vector q in byte q (fewer registers)
+#pragma unroll
+    for (int k = 0; k < (NV + 3) / 4; ++k) nreal[k] = 0;
+    const int32_t base = c0 + tid * V;
 #pragma unroll
     for (int q = 0; q < NV; ++q) {
       const int32_t t = base + q * kThreads * V;
       v[q] = pad4;
-      nreal[q] = 0;
       if (t < lim) {
         while (j + 1 < held && s_dst[j + 1] <= t) ++j;
         const int32_t off = t - s_dst[j];
@@ -257,13 +273,13 @@ __global__ void __launch_bounds__(kThreads, SLOTS >= 16 ? 3 : 4) squeeze_kernel(
         const T* p = src + (int64_t)s_src[j] * a.W + off;
         if (off + V <= r) {
           v[q] = ld_stream(reinterpret_cast<const int4*>(p));
-          nreal[q] = V;
+          nreal[q / 4] |= (uint32_t)V << (8 * (q % 4));
         } else if (off < r) {
           T e[V];
 #pragma unroll
           for (int k = 0; k < V; ++k) e[k] = off + k < r ? __ldg(p + k) : pv;
           memcpy(&v[q], e, 16);
-          nreal[q] = r - off;
+          nreal[q / 4] |= (uint32_t)(r - off) << (8 * (q % 4));
         }
       }
     }
@@ -273,10 +289,11 @@ __global__ void __launch_bounds__(kThreads, SLOTS >= 16 ? 3 : 4) squeeze_kernel(
       if (t < end) {
         st_stream(reinterpret_cast<int4*>(row + t), v[q]);
         if (mrow) {
-          // byte k is 1 for padding: slots nreal[q] .. V-1
+          // byte k is 1 for padding: the slots from the vector's real count on
+          const int nr = (int)((nreal[q / 4] >> (8 * (q % 4))) & 0xffu);
           uint8_t m[V];
 #pragma unroll
-          for (int k = 0; k < V; ++k) m[k] = k >= nreal[q] ? 1 : 0;
+          for (int k = 0; k < V; ++k) m[k] = k >= nr ? 1 : 0;
           if constexpr (V == 16) {
             int4 w;
             memcpy(&w, m, 16);
@@ -300,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, SLOTS >= 16 ? 3 : 4) squeeze_kernel(
   } else {
     T v[SLOTS];
     unsigned padmask = 0;
-    const int32_t base = (int32_t)c0 + tid;
+    const int32_t base = c0 + tid;
 #pragma unroll
     for (int q = 0; q < SLOTS; ++q) {
       const int32_t t = base + q * kThreads;
@@ -334,12 +351,16 @@ __global__ void empty_squeeze_kernel(pseq_info* info) {
 
 template <int SLOTS, int EB, bool VEC>
 cudaError_t launch_squeeze(const Args& a, unsigned gy, cudaStream_t st) {
-  const cudaError_t e =
-      allow_dynamic_smem(reinterpret_cast<const void*>(squeeze_kernel<SLOTS, EB, VEC>), table_bytes<SLOTS>());
-  if (e != cudaSuccess) return e;
   constexpr int64_t w = window<SLOTS>();
+  // the attribute allows the largest table (multiple 1), so that concurrent
+  // callers with other multiples never lower it under one another
+  const cudaError_t e =
+      allow_dynamic_smem(reinterpret_cast<const void*>(squeeze_kernel<SLOTS, EB, VEC>), kEntryBytes * (size_t)w);
+  if (e != cudaSuccess) return e;
+  const int cap = table_entries(w, a.multiple);
   const unsigned gx = a.out && a.width > 0 ? (unsigned)((a.width + w - 1) / w) : 1u;
-  return launch_pdl(squeeze_kernel<SLOTS, EB, VEC>, dim3(gx, gy), dim3(kThreads), table_bytes<SLOTS>(), st, a);
+  return launch_pdl(squeeze_kernel<SLOTS, EB, VEC>, dim3(gx, gy), dim3(kThreads), kEntryBytes * (size_t)cap, st, a,
+                    cap);
 }
 
 template <int SLOTS, int EB>
@@ -350,13 +371,22 @@ cudaError_t launch_squeeze(const Args& a, bool vec, unsigned gy, cudaStream_t st
   return launch_squeeze<SLOTS, EB, false>(a, gy, st);
 }
 
-template <int SLOTS>
+// Wide windows when they still give every SM two CTAs, else narrow ones.
+template <int EB>
+cudaError_t launch_squeeze(const Args& a, bool vec, unsigned gy, cudaStream_t st) {
+  constexpr int kWide = slots_wide<EB>();
+  constexpr int64_t w = window<kWide>();
+  const int64_t wide_ctas = (a.out && a.width > 0 ? (a.width + w - 1) / w : 1) * (int64_t)gy;
+  return wide_ctas >= 2 * (int64_t)sm_count() ? launch_squeeze<kWide, EB>(a, vec, gy, st)
+                                               : launch_squeeze<kSlotsNarrow, EB>(a, vec, gy, st);
+}
+
 cudaError_t launch_squeeze(const Args& a, bool vec, unsigned gy, cudaStream_t st) {
   switch (a.elem_bytes) {
-    case 8: return launch_squeeze<SLOTS, 8>(a, vec, gy, st);
-    case 4: return launch_squeeze<SLOTS, 4>(a, vec, gy, st);
-    case 2: return launch_squeeze<SLOTS, 2>(a, vec, gy, st);
-    default: return launch_squeeze<SLOTS, 1>(a, vec, gy, st);
+    case 8: return launch_squeeze<8>(a, vec, gy, st);
+    case 4: return launch_squeeze<4>(a, vec, gy, st);
+    case 2: return launch_squeeze<2>(a, vec, gy, st);
+    default: return launch_squeeze<1>(a, vec, gy, st);
   }
 }
 
@@ -434,17 +464,12 @@ extern "C" pseq_status pack_squeeze(const void* src, int64_t N, int64_t W, int32
   a.info = info;
   a.hdr = static_cast<Header*>(workspace);
   a.rec = reinterpret_cast<BinRec*>(static_cast<unsigned char*>(workspace) + sizeof(Header));
-  // wide windows when they still give every SM two CTAs, else narrow ones
-  const int64_t wide_ctas = (out && width > 0 ? (width + window<kSlotsWide>() - 1) / window<kSlotsWide>() : 1) *
-                            num_bins;
   // 16-byte vectors when every member start, row start and window start
   // falls on a 16-byte boundary of both src and out
   const int64_t eb = elem_bytes;
   const bool vec = out && aligned(src, 16) && aligned(out, 16) && aligned(padding_mask, 16) && (W * eb) % 16 == 0 &&
                    (width * eb) % 16 == 0 && (multiple * eb) % 16 == 0;
-  const cudaError_t e = wide_ctas >= 2 * (int64_t)sm_count()
-                            ? launch_squeeze<kSlotsWide>(a, vec, (unsigned)num_bins, st)
-                            : launch_squeeze<kSlotsNarrow>(a, vec, (unsigned)num_bins, st);
+  const cudaError_t e = launch_squeeze(a, vec, (unsigned)num_bins, st);
   count_launches(1);
   if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
   return check_launch(fn);
