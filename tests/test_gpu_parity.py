@@ -511,7 +511,8 @@ def test_squeeze_many_members():
 
 @pytest.mark.parametrize("members", [1, 31, 32, 33, 127, 128, 129, 300])
 def test_squeeze_bin_member_counts(members):
-    # bins of up to 128 members are scanned by one warp, larger ones by the block
+    # member counts around a warp and around a round of the block's member
+    # scan (256 members per round)
     rng = np.random.default_rng(members)
     prob = synth.random_squeeze(rng, members * 3, 50, 3)
     m = 8
