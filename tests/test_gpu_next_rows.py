@@ -81,6 +81,27 @@ def test_token_mask_random(dtype):
         check_token_mask(content, 7)  # a pad id that may not occur at all
 
 
+def test_token_mask_extreme_values():
+    # a pad id that shares its low 32 bits with content ids, and negative
+    # or limit pad ids: the comparison is on the whole value
+    rng = np.random.default_rng(21)
+    cases = [(np.int64, 1 << 32, np.array([0, 1 << 33, (1 << 32) + 1, -1, np.iinfo(np.int64).min], np.int64)),
+             (np.int64, -1, np.array([np.iinfo(np.int64).max, 1, 0, (1 << 32) - 1], np.int64)),
+             (np.int32, np.iinfo(np.int32).min, np.array([0, 1, -1, np.iinfo(np.int32).max], np.int32))]
+    for dtype, pad, content_pool in cases:
+        for n in (9, 4096 + 3, 100_001):
+            ids = content_pool[rng.integers(0, len(content_pool), size=n)].astype(dtype)
+            tail = int(rng.integers(0, n + 1))
+            if tail:
+                ids[n - tail:] = pad
+            check_token_mask(ids, pad)
+            check_token_mask(ids, pad, offset=1)
+            if tail > 1 and n - tail > 1:
+                bad = ids.copy()
+                bad[int(rng.integers(0, n - tail))] = pad  # the pad id inside the content
+                check_token_mask(bad, pad)
+
+
 def test_token_mask_page_rule_and_api():
     v = V()
     m = v.thd_padding_mask_from_token_ids(dev(np.array([5, 6, 0, 0])), 0)
@@ -183,6 +204,24 @@ def test_bridge_random(kind):
             check_bridge(d, S)
     d = synth.random_doc_ids(rng, 3, 500, "runs", np.int32)
     check_bridge(d, 4)  # rows hold more sequences than slots
+
+
+def test_bridge_extreme_values():
+    # non-zero ids whose low 32 bits are zero are documents, not padding;
+    # negative ids and the type's limits are documents too
+    rng = np.random.default_rng(43)
+    pool64 = np.array([0, 1, -1, 1 << 32, 1 << 33, (1 << 32) + 1, np.iinfo(np.int64).max,
+                       np.iinfo(np.int64).min], np.int64)
+    pool32 = np.array([0, 1, -1, 1 << 16, np.iinfo(np.int32).max, np.iinfo(np.int32).min], np.int32)
+    for pool in (pool64, pool32):
+        for B, S in ((3, 40), (2, 9000), (1, 40000)):
+            flat = np.empty(B * S, pool.dtype)
+            pos = 0
+            while pos < B * S:
+                L = int(rng.geometric(0.2))
+                flat[pos:pos + L] = pool[rng.integers(0, len(pool))]
+                pos += L
+            check_bridge(flat.reshape(B, S), S)
 
 
 def test_bridge_long_rows():

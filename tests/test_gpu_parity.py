@@ -95,6 +95,34 @@ def test_doc_ids_random(kind, dtype):
         check_doc_ids(d, offset_elems=1)  # unaligned pointer: scalar load path
 
 
+def extreme_runs(rng, pool, B, S):
+    """Runs of values drawn from `pool` (mean length 5)."""
+    flat = np.empty(B * S, pool.dtype)
+    pos = 0
+    while pos < B * S:
+        L = int(rng.geometric(0.2))
+        flat[pos:pos + L] = pool[rng.integers(0, len(pool))]
+        pos += L
+    return flat.reshape(B, S)
+
+
+INT64_POOL = np.array([0, 1, -1, 1 << 32, (1 << 32) + 1, 1 << 33, -(1 << 40), np.iinfo(np.int64).max,
+                       np.iinfo(np.int64).min], np.int64)
+INT32_POOL = np.array([0, 1, -1, 1 << 16, np.iinfo(np.int32).max, np.iinfo(np.int32).min], np.int32)
+
+
+@pytest.mark.parametrize("dtype", [np.int32, np.int64])
+def test_doc_ids_extreme_values(dtype):
+    # ids that differ only in their high 32 bits, negative ids and the type's
+    # limits: boundaries are decided on the whole value
+    rng = np.random.default_rng(77)
+    pool = INT64_POOL if dtype == np.int64 else INT32_POOL
+    for B, S in ((3, 40), (2, 20000), (1, 70001)):
+        d = extreme_runs(rng, pool, B, S)
+        check_doc_ids(d)
+        check_doc_ids(d, offset_elems=1)
+
+
 def test_doc_ids_many_tiles_chain():
     """Over a hundred tiles, so the look-back crosses several 32-tile windows."""
     rng = np.random.default_rng(11)
