@@ -160,6 +160,23 @@ def test_ffd_random(n):
         check_ffd(rng.integers(1, 50, size=n), int(rng.integers(50, 400)), multiple)
 
 
+def test_ffd_equal_size_runs():
+    # runs of equal sizes: zero sizes, runs longer than a warp, a run that
+    # opens the 33rd bin half way, runs that first top up open bins and then
+    # open new ones
+    check_ffd(np.zeros(50, np.int64), 10)
+    check_ffd(np.array([0] * 5 + [3] * 40 + [0] * 7), 10)
+    check_ffd(np.array([6] * 40), 10)
+    check_ffd(np.array([5] * 100), 10)
+    check_ffd(np.array([7] * 3 + [3] * 50), 10)
+    check_ffd(np.array([9] * 31 + [1] * 70 + [4] * 9), 10)
+    check_ffd(np.arange(1, 65), 4096, 64)  # every size rounds to 64
+    rng = np.random.default_rng(5)
+    for n in (300, 5000):
+        check_ffd(rng.choice([0, 1, 2, 3, 5, 8], size=n), 17)
+        check_ffd(rng.choice([16, 48, 64, 100], size=n), 128)
+
+
 def test_ffd_feeds_the_squeeze():
     """The squeeze workload, with bins from the GPU packer."""
     v = V()
