@@ -88,6 +88,13 @@ __device__ __forceinline__ unsigned inc_acq_rel(unsigned* p, unsigned limit) {
   return old;
 }
 
+// 64-bit add with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ unsigned long long add_acq_rel_u64(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

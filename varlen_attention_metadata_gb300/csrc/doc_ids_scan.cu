@@ -21,9 +21,12 @@
 // joins them with a shuffle tree.  A map that fits one tile skips all of this.  Waits are bounded by a time limit
 // and report PSEQ_ERR_TIMEOUT.  Boundaries are compacted through shared
 // memory (tile-relative 16-bit positions) and stored coalesced.  The CTA that
-// finishes its look-back last writes cu_seqlens[num_segments] and the info
-// block and clears the summary words, so the workspace is zero again for the
-// next call.
+// finishes last clears the summary words, so the workspace is zero again for
+// the next call.  The last tile, which holds the whole map's summary once its
+// look-back ends, writes cu_seqlens[num_segments] and the info block itself;
+// the tiles count themselves done (with any failure they met) in one 64-bit
+// word, and the one whose add completes the count only reports a failure, if
+// any, and clears the workspace: no tile summary is read back at the end.
 #include <mutex>
 
 #include "common.cuh"
@@ -87,10 +90,16 @@ __device__ __forceinline__ Bounds from_words(unsigned long long a, unsigned long
   return {(int)((a >> 32) & 0x7fffffffu), (int)(unsigned)b, (int)(unsigned)a, (int)((b >> 32) & 0x7fffffffu)};
 }
 
+// Header word: tiles done (bits 0..19), tiles whose wait hit its time limit
+// (bits 20..39), tiles that found a workspace that was not zero-filled
+// (bits 40..59).  A map has at most 2^17 tiles, so no field overflows; the
+// tile that completes the count resets the word to zero.
+constexpr int kTimeoutShift = 20, kBadShift = 40;
+constexpr unsigned long long kCountMask = (1ull << 20) - 1;
+
 struct Header {
-  unsigned int finished;  // tiles done with their look-back; wraps back to 0 after each call
-  unsigned int gave_up;   // nonzero when some wait hit its time limit
-  unsigned int pad[30];
+  unsigned long long state;
+  unsigned long long pad[15];
 };
 static_assert(sizeof(Header) == 128, "header is 128 bytes");
 
@@ -131,6 +140,7 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 512 ? 2 : 1)
   __shared__ Bounds s_warp[(THREADS / 32)];
   __shared__ Bounds s_prefix;
   __shared__ int s_last_cta;
+  __shared__ unsigned long long s_state;
   __shared__ unsigned short s_pos[(THREADS * kItems)];
 
   pdl_enter();
@@ -214,6 +224,8 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 512 ? 2 : 1)
   }
 
   // ---- publish the tile summary, then look back for the exclusive prefix
+  bool timed_out = withhold == tile;  // (thread 0) a withheld summary is reported as a failed wait
+  bool bad_ws = false;                // (thread 0)
   if (warp == 0) {
     Slot* mine_slot = ws.slots + tile;
     Bounds prefix = none();
@@ -315,14 +327,24 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 512 ? 2 : 1)
         if (stop_w < kPerLane) break;
         j -= 32 * kPerLane;
       }
-      if (__any_sync(~0u, gave_up) && lane == 0) atomicOr(&ws.hdr->gave_up, 1u);
+      if (__any_sync(~0u, gave_up)) timed_out = true;
       prefix = run;
     }
     if (lane == 0) {
+      const Bounds all = join(prefix, tile_sum);
       if (withhold != tile) {
-        const Bounds all = join(prefix, tile_sum);
         st_relaxed_u64(&mine_slot->inc_a, word_a(all));
         st_relaxed_u64(&mine_slot->inc_b, word_b(all));
+      }
+      if (tile == tiles - 1 && !timed_out) {
+        // the whole map: close the array and report (a failure elsewhere
+        // overwrites the report at the end)
+        if (all.count >= 1 && all.count <= N) {
+          cu[all.count] = N;
+          *info = {PSEQ_OK, all.count, max(all.gap, N - all.last), N};
+        } else {
+          bad_ws = true;
+        }
       }
       s_prefix = prefix;
     }
@@ -336,26 +358,25 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 512 ? 2 : 1)
   if (base >= 0 && base <= N - tile_sum.count) {
     for (int i = tid; i < tile_sum.count; i += THREADS) cu[base + i] = (int32_t)(tile_base + s_pos[i]);
   } else if (tid == 0) {
-    atomicOr(&ws.hdr->gave_up, 2u);  // only reachable from a workspace that was not zero-filled
+    bad_ws = true;  // only reachable from a workspace that was not zero-filled
   }
-  if (tid == 0) s_last_cta = inc_acq_rel(&ws.hdr->finished, (unsigned)(tiles - 1)) == (unsigned)(tiles - 1);
+  if (tid == 0) {
+    const unsigned long long add =
+        1ull | ((unsigned long long)timed_out << kTimeoutShift) | ((unsigned long long)bad_ws << kBadShift);
+    const unsigned long long old = add_acq_rel_u64(&ws.hdr->state, add);
+    s_last_cta = (old & kCountMask) == (unsigned long long)(tiles - 1);
+    s_state = old + add;
+  }
   __syncthreads();
   if (!s_last_cta) return;
 
-  // ---- last CTA: close the array, report, and clear the summary words
+  // ---- last CTA: report a failure, if any, and clear the workspace
   if (tid == 0) {
-    const Slot* sl = ws.slots + (tiles - 1);
-    const unsigned long long ia = ld_relaxed_u64(&sl->inc_a), ib = ld_relaxed_u64(&sl->inc_b);
-    const unsigned failed = atomicExch(&ws.hdr->gave_up, 0u);
-    const Bounds all = from_words(ia, ib);
-    pseq_info out;
-    if (failed || !(ia & ib & kValid) || all.count < 1 || all.count > N) {
-      out = {(failed & 2u) ? PSEQ_ERR_ARG : PSEQ_ERR_TIMEOUT, 0, 0, N};
-    } else {
-      cu[all.count] = N;
-      out = {PSEQ_OK, all.count, max(all.gap, N - all.last), N};
-    }
-    *info = out;
+    const unsigned long long all = s_state;
+    const bool timeouts = ((all >> kTimeoutShift) & kCountMask) != 0;
+    const bool bad = ((all >> kBadShift) & kCountMask) != 0;
+    if (timeouts || bad) *info = {bad ? PSEQ_ERR_ARG : PSEQ_ERR_TIMEOUT, 0, 0, N};
+    ws.hdr->state = 0;  // the next call starts after this grid completes
   }
   unsigned long long* words = reinterpret_cast<unsigned long long*>(ws.slots);
   for (int i = tid; i < 4 * tiles; i += THREADS) words[(i >> 2) * 16 + (i & 3)] = 0ull;  // the four words of each slot
