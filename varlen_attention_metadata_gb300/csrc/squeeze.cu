@@ -221,19 +221,28 @@ __global__ void __launch_bounds__(kThreads, SLOTS >= 16 ? 5 : (SLOTS >= 12 ? 6 :
   int status = PSEQ_OK;
   if (bad_offsets || s_bad) status = PSEQ_ERR_VALUE;
   else if (total_pad > a.capacity || (a.out && total_pad > a.width)) status = PSEQ_ERR_CAPACITY;
-  if (first) {
-    if (tid == 0) {
-      if (!bad_offsets) {
-        a.cu[hi + b] = (int32_t)carry.real;
-        a.cup[hi + b] = a.stretch ? (int32_t)a.capacity : (int32_t)total_pad;
-      }
-      a.rec[b] = BinRec{status, (int)min(total_pad, (long long)INT32_MAX), s_longest, bad_offsets ? 0 : hi - lo};
-      s_last = inc_acq_rel(&a.hdr->finished, (unsigned)a.num_bins - 1u) == (unsigned)a.num_bins - 1u;
+  // First windows publish their bin's record and count it in; the counter's
+  // old value is looked at only after the window has streamed, so that its
+  // round trip overlaps the copy.  The last record to arrive folds them all.
+  unsigned ticket = 0;
+  if (first && tid == 0) {
+    if (!bad_offsets) {
+      a.cu[hi + b] = (int32_t)carry.real;
+      a.cup[hi + b] = a.stretch ? (int32_t)a.capacity : (int32_t)total_pad;
     }
+    a.rec[b] = BinRec{status, (int)min(total_pad, (long long)INT32_MAX), s_longest, bad_offsets ? 0 : hi - lo};
+    ticket = inc_acq_rel(&a.hdr->finished, (unsigned)a.num_bins - 1u);
+  }
+  auto finish = [&]() {
+    if (!first) return;
+    if (tid == 0) s_last = ticket == (unsigned)a.num_bins - 1u;
     __syncthreads();
     if (s_last) fold_records(a);
+  };
+  if (status != PSEQ_OK || !a.out) {
+    finish();
+    return;
   }
-  if (status != PSEQ_OK || !a.out) return;
   // every slot of the window, once: loads first, then stores.  A thread's
   // slots ascend, so its member index only moves forward through the table.
   using T = typename Elem<EB>::T;
@@ -342,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, SLOTS >= 16 ? 5 : (SLOTS >= 12 ? 6 :
       }
     }
   }
+  finish();
 }
 
 __global__ void empty_squeeze_kernel(pseq_info* info) {
