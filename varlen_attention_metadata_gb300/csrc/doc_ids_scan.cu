@@ -18,15 +18,17 @@
 // a single poll returns the summary itself: no flag-then-value round trip and
 // no release fence on the publishing side.  A look-back round polls 32
 // predecessors at once (one per lane), all loads in flight together, and
-// joins them with a shuffle tree.  A map that fits one tile skips all of this.  Waits are bounded by a time limit
-// and report PSEQ_ERR_TIMEOUT.  Boundaries are compacted through shared
-// memory (tile-relative 16-bit positions) and stored coalesced.  The CTA that
-// finishes last clears the summary words, so the workspace is zero again for
-// the next call.  The last tile, which holds the whole map's summary once its
-// look-back ends, writes cu_seqlens[num_segments] and the info block itself;
-// the tiles count themselves done (with any failure they met) in one 64-bit
-// word, and the one whose add completes the count only reports a failure, if
-// any, and clears the workspace: no tile summary is read back at the end.
+// joins them with a shuffle tree.  A map that fits one tile skips all of
+// this.  Waits are bounded by a time limit and report PSEQ_ERR_TIMEOUT.
+// Boundaries are compacted through shared memory (tile-relative 16-bit
+// positions) and stored coalesced.
+//
+// The last tile, which holds the whole map's summary once its look-back
+// ends, writes cu_seqlens[num_segments] and the info block itself.  The tiles
+// count themselves done (with any failure they met) in one 64-bit word; the
+// CTA whose add completes the count only reports a failure, if any, and
+// clears the summary words, so the workspace is zero again for the next call
+// and no tile summary is read back at the end.
 #include <mutex>
 
 #include "common.cuh"

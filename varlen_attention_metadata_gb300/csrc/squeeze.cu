@@ -12,8 +12,8 @@
 // are disjoint and each at least `multiple` slots long, so the table never
 // holds more than min(window, window / multiple + 2) entries, whatever the
 // number of members; the launch sizes it so, which keeps shared memory from
-// limiting the CTAs resident on an SM.  Each thread then owns
-// a fixed number of slots of the window (interleaved across the CTA, so that a warp's
+// limiting the CTAs resident on an SM.  Each thread then owns a fixed number
+// of slots of the window (interleaved across the CTA, so that a warp's
 // accesses are contiguous): it looks up the member of each slot, issues every
 // load before any store, and writes the token or pad_value with its mask
 // byte.  Every output slot is written exactly once.
