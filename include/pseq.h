@@ -65,12 +65,17 @@ const char* pseq_last_error(void);
 int64_t pseq_launch_count(void);
 
 /* Bounded-wait controls, for failure-detection tests.  spin_limit_ns caps
- * every device-side wait of pseq_from_doc_ids and pseq_doc_ids_to_lengths
- * (default 1e9 ns); when withhold_tile >= 0 that scan tile (or bridge chunk,
- * counted row-major over rows and 4096-token chunks) never publishes its
- * partial result, so the ones after it run into the cap and report
- * PSEQ_ERR_TIMEOUT.  Process-wide; pass (-1, -1) to restore the defaults. */
+ * every device-side wait of pseq_from_doc_ids, pseq_doc_ids_to_lengths and
+ * the bulk-copy path of thd_from_batch; it is clamped to [0, 1e9] ns (the
+ * default, 1 s), so no setting makes a wait unbounded.  When withhold_tile
+ * >= 0 that scan tile (or bridge chunk, counted row-major over rows and
+ * 4096-token chunks) never publishes its partial result, so the ones after
+ * it run into the cap and report PSEQ_ERR_TIMEOUT.  Process-wide; pass
+ * (-1, -1) to restore the defaults. */
 void pseq_debug_set_wait(int64_t spin_limit_ns, int64_t withhold_tile);
+
+/* The wait cap in force, in nanoseconds (after clamping). */
+int64_t pseq_debug_wait_limit_ns(void);
 
 /* ------------------------------------------------------------------------
  * pseq_from_doc_ids

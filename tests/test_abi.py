@@ -86,6 +86,23 @@ def test_host_argument_errors_without_gpu(lib):
     assert lib.pseq_version() >= 100
 
 
+def test_debug_wait_limit_is_clamped(lib):
+    """No setting lifts the bound on device-side waits: a limit above the
+    1 s default is clamped to it, a negative one restores it."""
+    try:
+        lib.pseq_debug_set_wait(2**63 - 1, 5)
+        assert lib.pseq_debug_wait_limit_ns() == 1_000_000_000
+        lib.pseq_debug_set_wait(1_000_000, -1)
+        assert lib.pseq_debug_wait_limit_ns() == 1_000_000
+        lib.pseq_debug_set_wait(0, -1)
+        assert lib.pseq_debug_wait_limit_ns() == 0
+        lib.pseq_debug_set_wait(-7, -1)
+        assert lib.pseq_debug_wait_limit_ns() == 1_000_000_000
+    finally:
+        lib.pseq_debug_set_wait(-1, -1)
+    assert lib.pseq_debug_wait_limit_ns() == 1_000_000_000
+
+
 def test_product_path_refuses_cpu_tensors():
     import torch
 

@@ -62,6 +62,7 @@ SIGNATURES = {
     "pseq_last_error": (ctypes.c_char_p, []),
     "pseq_launch_count": (_I64, []),
     "pseq_debug_set_wait": (None, [_I64, _I64]),
+    "pseq_debug_wait_limit_ns": (_I64, []),
     "pseq_from_doc_ids_workspace_size": (_SZ, [_I64, _I64]),
     "pseq_from_doc_ids": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _P, _SZ, _P]),
     "pseq_from_doc_ids_static": (ctypes.c_int, [_P, _I32, _I64, _I64, _P, _P, _P]),

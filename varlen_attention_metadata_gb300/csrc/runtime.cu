@@ -100,8 +100,14 @@ const char* pseq_last_error(void) { return pseq::g_last_error; }
 int64_t pseq_launch_count(void) { return pseq::g_launches.load(std::memory_order_relaxed); }
 
 void pseq_debug_set_wait(int64_t spin_limit_ns, int64_t withhold_tile) {
-  pseq::g_wait_ns.store(spin_limit_ns >= 0 ? spin_limit_ns : pseq::kDefaultWaitNs);
+  // a negative limit restores the default; no limit may exceed it, so no
+  // caller can make a device-side wait (withheld tile or not) unbounded
+  int64_t ns = spin_limit_ns >= 0 ? spin_limit_ns : pseq::kDefaultWaitNs;
+  if (ns > pseq::kDefaultWaitNs) ns = pseq::kDefaultWaitNs;
+  pseq::g_wait_ns.store(ns);
   pseq::g_withhold.store(withhold_tile >= 0 ? withhold_tile : -1);
 }
+
+int64_t pseq_debug_wait_limit_ns(void) { return pseq::wait_limit_ns(); }
 
 }  // extern "C"
