@@ -222,14 +222,17 @@ pseq_status thd_gather(const pseq_field* fields, int32_t num_fields,
  * cu_seqlens, cu_seqlens_padded: int32 [num_chunks, B/num_chunks*num_packs+1];
  *   row c holds the chunk's n_c+1 boundaries followed by pad_value.
  *   cu_seqlens_padded may be NULL.
- * fields: as for thd_from_batch (src rows are rows of the whole batch).  The
- *   stream of chunk c starts planes*T_c*c rows into dst, so the results are
- *   stacked [num_chunks, planes, T, row_elems] when every chunk has the same
- *   stream length T.  dst room: planes * B * S * row_elems elements.
- * padding_mask: chunk c's T_c bytes start at byte c*T_c (room B*S); may be
+ * fields: as for thd_from_batch (src rows are rows of the whole batch).  With
+ *   Sc = (B / num_chunks) * S, the stream of chunk c starts c * planes * Sc
+ *   rows into dst and is [planes, T_c, row_elems] (planes T_c rows apart):
+ *   every chunk's stream is defined whatever the other chunks' lengths, and
+ *   dst viewed as [num_chunks, planes * Sc, row_elems] holds them at a fixed
+ *   stride.  dst room: planes * B * S * row_elems elements.
+ * padding_mask: chunk c's T_c bytes start at byte c * Sc (room B*S); may be
  *   NULL.  pad_between_seqs: num_chunks bytes; may be NULL.
  * infos: pseq_info [num_chunks], one per chunk (count n_c, max_seqlen,
- *   total T_c).  Stacking needs every T_c equal; compare infos[c].total.
+ *   total T_c).  Stacking the chunks into one tensor, as the page does, needs
+ *   every T_c equal; compare infos[c].total.
  * workspace: thd_workspace_size(B / num_chunks, num_packs) bytes.
  * ---------------------------------------------------------------------- */
 pseq_status thd_chunks_from_batch(const int64_t* seq_lens,

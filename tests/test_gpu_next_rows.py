@@ -281,9 +281,7 @@ def check_split(batch_np: dict, num_chunks: int, hidden=None, absorb=True):
                                 absorb)
     infos = r["infos"].cpu().numpy()
     Bc = B // num_chunks
-    # chunk c's stream starts c * T_c rows in: only equal lengths stack, and
-    # only then are the streams defined (the metadata always is)
-    stackable = len({int(t) for t in infos[:, 3]}) == 1 and bool(np.all(infos[:, 0] == 0))
+    Sc = Bc * S  # chunk c's stream starts c * planes * Sc rows in, its mask c * Sc bytes in: defined for any lengths
     for c in range(num_chunks):
         sl = slice(c * Bc, (c + 1) * Bc)
         try:
@@ -299,20 +297,19 @@ def check_split(batch_np: dict, num_chunks: int, hidden=None, absorb=True):
         if padded is not None:
             np.testing.assert_array_equal(r["cu_seqlens_padded"][c, : n + 1].cpu().numpy(), meta["cu_seqlens_padded"])
         assert bool(r["pad_between"][c].item()) == meta["pad_between_seqs"]
-        if not stackable:
-            continue
         for (a, planes), (dst, _, rowshape) in zip(fields_np, r["dst"]):
             sub = a[:, sl] if planes > 1 else a[sl]
             want = oracle.thd_gather(sub, meta, Bc, S, planes=planes)
-            start = c * want.size
+            start = c * planes * Sc
             got = dst[start:start + want.size].cpu().numpy().reshape(want.shape)
             np.testing.assert_array_equal(got, want)
         if hidden is not None:
             h = hidden[sl].cpu().view(torch.int16).numpy()
             want = oracle.thd_gather(h, meta, Bc, S)
-            got = r["dst"][-1][0][c * want.size:(c + 1) * want.size].cpu().view(torch.int16).numpy()
+            row = h.shape[2]
+            got = r["dst"][-1][0][c * Sc * row:c * Sc * row + want.size].cpu().view(torch.int16).numpy()
             np.testing.assert_array_equal(got.reshape(want.shape), want)
-        m = r["padding_mask"][c * T:(c + 1) * T].cpu().numpy()
+        m = r["padding_mask"][c * Sc:c * Sc + T].cpu().numpy()
         np.testing.assert_array_equal(m, oracle.thd_padding_mask(T, meta["seq_real"],
                                                                  meta["seq_padded"] if padded is not None else None))
 

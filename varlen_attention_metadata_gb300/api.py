@@ -544,6 +544,9 @@ def split_batch_into_thd_chunks(batch: dict, num_chunks: int, seq_lens_padding_v
     ``seq_lens_padding_value``.  ``max_seqlen`` becomes an int32 tensor
     [num_chunks] and ``pad_between_seqs`` a bool tensor [num_chunks].
     Chunks whose streams differ in length cannot be stacked: ValueError.
+    The stacked tensors are views of the library's chunked buffers, in which
+    chunk c starts at a fixed stride of (B / num_chunks) * S rows; they are
+    contiguous when every chunk's stream fills its rows (T == B/num_chunks*S).
     """
     if num_chunks <= 1:
         return process_input_for_thd(batch, seq_lens_padding_value, padding_token_id)
@@ -571,20 +574,22 @@ def split_batch_into_thd_chunks(batch: dict, num_chunks: int, seq_lens_padding_v
         raise ValueError(f"split_batch_into_thd_chunks: chunk streams have different lengths {sorted(totals)} "
                          "and cannot be stacked")
     T = totals.pop()
+    Sc = B // num_chunks * S  # the library writes chunk c's stream and mask at a fixed stride of Sc rows
     width = max(n for _, n, _, _ in infos) + 1
     out = {k: v for k, v in batch.items() if not isinstance(v, torch.Tensor) and k not in _THD_KEYS}
     for name, (dst, planes, row) in zip(names, r["dst"]):
-        flat = dst[: num_chunks * planes * T * (math.prod(row) if row else 1)]
+        # views of the chunks' streams, stacked on a leading axis (contiguous when T == Sc)
+        per_chunk = dst.view(num_chunks, planes * Sc, *row)[:, : planes * T]
         if name == "position_ids" and planes > 1:
-            out[name] = flat.view(num_chunks, planes, 1, T)
+            out[name] = per_chunk.view(num_chunks, planes, 1, T)
         else:
-            out[name] = flat.view(num_chunks, T, *row)
+            out[name] = per_chunk
     out["cu_seqlens"] = r["cu_seqlens"][:, :width]
     if r["cu_seqlens_padded"] is not None:
         out["cu_seqlens_padded"] = r["cu_seqlens_padded"][:, :width]
     out["pad_between_seqs"] = r["pad_between"].view(torch.bool)
     out["max_seqlen"] = r["infos"][:, 2]
-    out["padding_mask"] = r["padding_mask"][: num_chunks * T].view(num_chunks, T)
+    out["padding_mask"] = r["padding_mask"].view(num_chunks, Sc)[:, :T]
     return out
 
 

@@ -222,10 +222,11 @@ struct Fields {
 // Sequences j = 0..cnt-1 of the table start at stream row cup[j] (cup[cnt]
 // ends the last one) and at source token src_tok[j]; cup[0] <= lo and
 // hi <= cup[cnt].  B is the source's rows per plane; stream `chunk` of a
-// stacked result starts chunk * planes * T rows into each destination.
+// chunked result starts chunk * planes * chunk_rows rows into each
+// destination (its planes T rows apart), whatever the other chunks' lengths.
 __device__ void gather_rows(const Fields& f, int64_t B, int64_t S, int64_t T, uint8_t* mask, int64_t lo,
                             int64_t hi, const int32_t* cup, const int32_t* src_tok, const int32_t* real, int cnt,
-                            int64_t chunk) {
+                            int64_t chunk, int64_t chunk_rows) {
   if (lo >= hi) return;
   const int tid = threadIdx.x, nt = blockDim.x;
   const int64_t plane_in = B * S;
@@ -249,7 +250,7 @@ __device__ void gather_rows(const Fields& f, int64_t B, int64_t S, int64_t T, ui
           if (g + q < f.njobs) {
             const int i = f.job_field[g + q], p = f.job_plane[g + q];
             const int64_t rb = f.row_bytes[i];
-            store_row(f.dst[i] + ((chunk * f.planes[i] + p) * T + r) * rb, v[q], (int)rb);
+            store_row(f.dst[i] + (chunk * f.planes[i] * chunk_rows + p * T + r) * rb, v[q], (int)rb);
           }
         }
       }
@@ -266,7 +267,7 @@ __device__ void gather_rows(const Fields& f, int64_t B, int64_t S, int64_t T, ui
     for (int i = 0; i < f.num; ++i) {
       const int64_t rb = f.row_bytes[i];
       for (int p = 0; p < f.planes[i]; ++p)
-        block_copy(f.dst[i] + ((chunk * f.planes[i] + p) * T + a0) * rb,
+        block_copy(f.dst[i] + (chunk * f.planes[i] * chunk_rows + p * T + a0) * rb,
                    f.src[i] + ((int64_t)p * plane_in + tok) * rb, (a1 - a0) * rb);
     }
     if (mask) {
@@ -371,8 +372,9 @@ __global__ void __launch_bounds__(kRowThreads, 2)
   if (Tm > mask_cap || T > Tm || T > (int64_t)ac.B * ac.S) return;  // cannot happen for well-formed input
   int64_t r0, r1;
   slice_of(Tm, r0, r1);
-  uint8_t* m = mask ? mask + (int64_t)c * Tm : nullptr;
-  gather_rows(f, (int64_t)ac.B * a.chunks, ac.S, T, m, r0, min(r1, T), t.cup, t.src, t.real, n, c);
+  const int64_t chunk_rows = (int64_t)ac.B * ac.S;  // fixed stride of the chunks' streams and masks
+  uint8_t* m = mask ? mask + (int64_t)c * chunk_rows : nullptr;
+  gather_rows(f, (int64_t)ac.B * a.chunks, ac.S, T, m, r0, min(r1, T), t.cup, t.src, t.real, n, c, chunk_rows);
   if (m) {
     const int64_t tail = max(r0, T);
     if (tail < r1) block_fill_bytes(m + tail, r1 - tail, 1);
@@ -414,7 +416,8 @@ __global__ void __launch_bounds__(kRowThreads, 1)
   int64_t r0, r1;
   slice_of(Tm, r0, r1);
   const int64_t lo = r0, hi = min(r1, T);
-  uint8_t* m = mask ? mask + (int64_t)c * Tm : nullptr;
+  const int64_t chunk_rows = (int64_t)ac.B * ac.S;  // fixed stride of the chunks' streams and masks
+  uint8_t* m = mask ? mask + (int64_t)c * chunk_rows : nullptr;
   if (threadIdx.x == 0 && lo < hi) {
     const int64_t plane_in = (int64_t)ac.B * a.chunks * ac.S;
     // the slice's chunks: sequence pieces x fields x planes, cut at kStage bytes
@@ -432,7 +435,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
             if (off < piece) {
               const int64_t tok = (int64_t)t.src[j] + (a0 - cs);
               src = f.src[i] + ((int64_t)p * plane_in + tok) * rb + off;
-              dst = f.dst[i] + (((int64_t)c * f.planes[i] + p) * T + a0) * rb + off;
+              dst = f.dst[i] + ((int64_t)c * f.planes[i] * chunk_rows + p * T + a0) * rb + off;
               bytes = (uint32_t)min(piece - off, (int64_t)kStage);
               off += bytes;
               return true;
@@ -550,7 +553,7 @@ __global__ void __launch_bounds__(kRowThreads, 2)
   int64_t r0, r1;
   slice_of(Tm, r0, r1);
   if (r0 >= r1) return;
-  if (mask) mask += chunk * Tm;
+  if (mask) mask += chunk * max_rows;  // chunk streams and masks sit max_rows apart
   const int64_t g1 = min(r1, T);
   const int tid = threadIdx.x, lane = tid & 31;
   int64_t lo = r0;
@@ -578,7 +581,7 @@ __global__ void __launch_bounds__(kRowThreads, 2)
     }
     __syncthreads();
     const int64_t hi = min(g1, (int64_t)s_cup[cnt]);
-    gather_rows(f, plane_rows, S, T, mask, lo, hi, s_cup, s_src, s_real, cnt, chunk);
+    gather_rows(f, plane_rows, S, T, mask, lo, hi, s_cup, s_src, s_real, cnt, chunk, max_rows);
     lo = hi;
     __syncthreads();
   }
@@ -708,7 +711,8 @@ pseq_status launch_meta(const char* fn, const MetaArgs& a, void* workspace, cuda
 }
 
 // plane_rows: source rows per plane (B unless this is one chunk of a larger
-// batch); chunk: position of this stream in a stacked result.
+// batch); chunk: position of this stream in a chunked result (streams and
+// masks B * S rows apart).
 pseq_status launch_gather(const char* fn, const Fields& f, int64_t B, int64_t S, int64_t P, uint8_t* mask,
                           const void* workspace, cudaStream_t st, int64_t mask_rows, int64_t plane_rows = -1,
                           int64_t chunk = 0) {
