@@ -15,7 +15,8 @@ Workloads (shapes and distributions of packed supervised fine-tuning batches):
   clipped to the row, padded to a multiple of 64, unused slots -1000; int64
   ids and labels, mRoPE positions [3, 8, 8192].
 * ``thd_embeddings``  bf16 hidden [4, 8192, 4096] ~ N(0, 1) with the same
-  length distribution as ``thd_ids``.
+  length distribution as ``thd_ids``; ``thd_embeddings_ragged`` drops each
+  row's last sequence, so rows end short and sequences move.
 * ``squeeze``         256 sources in an int64 rectangle [256, 4096] with real
   lengths lognormal(6.5, 0.8) clipped to [1, 4096], multiple 64, bins by
   first-fit-decreasing at capacity 32768, output width 32768, stretched.
@@ -214,6 +215,21 @@ def thd_embeddings(seed: int = 0, B: int = 4, S: int = 8192, H: int = 4096, P: i
     x = rng.standard_normal(size=(B, S, H), dtype=np.float32)
     hidden = torch.from_numpy(x).to(torch.bfloat16)
     return {"hidden": hidden, "seq_lens": seq_lens, "seq_lens_padded": seq_lens_padded}
+
+
+def thd_embeddings_ragged(seed: int = 0, B: int = 4, S: int = 8192, H: int = 4096, P: int = 64) -> dict:
+    """``thd_embeddings`` with every row ending short: each row's last kept
+    sequence is set to -1000 in both length arrays (the slots stay in the
+    hidden tensor but are no longer part of the batch), so the stream is
+    shorter than B*S and every row after the first lands in the stream at a
+    different offset than it has in the batch."""
+    c = thd_embeddings(seed, B, S, H, P)
+    for b in range(B):
+        kept = np.nonzero(c["seq_lens"][b] != FILLER)[0]
+        if kept.size > 1:
+            c["seq_lens"][b, kept[-1]] = FILLER
+            c["seq_lens_padded"][b, kept[-1]] = FILLER
+    return c
 
 
 def random_thd(rng: np.random.Generator, B: int, S: int, P: int, multiple: int = 4,

@@ -364,8 +364,12 @@ def test_thd_wide_rows_bulk_copy(H):
     np.testing.assert_array_equal(r2["dst"][0][0][: T * H].view(torch.int16).cpu().numpy().reshape(T, H), want)
 
 
-def test_thd_embeddings_workload():
-    c = synth.thd_embeddings(0)
+@pytest.mark.parametrize("gen", ["thd_embeddings", "thd_embeddings_ragged"])
+def test_thd_embeddings_workload(gen):
+    """bf16 [4, 8192, 4096] at full size: rows that fill S (the stream is the
+    batch reshaped) and rows that end short (every row after the first moves
+    to a lower stream offset)."""
+    c = getattr(synth, gen)(0)
     hidden = c["hidden"].to(DEV)
     v = V()
     B, S, H = hidden.shape
