@@ -113,8 +113,9 @@ pseq_status pseq_from_doc_ids(const void* doc_ids, int32_t id_bytes, int64_t B,
  * callback that is handed only input and output pointers, or a process that
  * has reserved all of HBM up front.  This entry point takes the same inputs
  * and outputs as pseq_from_doc_ids and no workspace.  Its scratch is a
- * static device array of about 128 KiB inside libpseq.so, which every GPU
- * that loads the library holds until the process exits.
+ * static device array of about 16 KiB inside libpseq.so (a 128-byte header
+ * and 16 bytes per 16384-token tile), which every GPU that loads the library
+ * holds until the process exits.
  *  - B*S must not exceed PSEQ_STATIC_MAX_TOKENS; larger maps get
  *    PSEQ_ERR_ARG before anything is enqueued (use pseq_from_doc_ids).
  *  - The first call on each device looks up the array's device address
@@ -122,8 +123,9 @@ pseq_status pseq_from_doc_ids(const void* doc_ids, int32_t id_bytes, int64_t B,
  *    before any stream capture.
  *  - Every call clears the part of the array that must start at zero
  *    (cudaMemsetAsync on the caller's stream) and then runs the scan.  All
- *    calls share the one array, so calls that may overlap on the GPU (other
- *    streams, other host threads) race and must be serialised by the caller.
+ *    calls share the one array, so any two calls whose work may overlap on
+ *    the GPU race, whatever issued them (other streams, other host threads):
+ *    the caller must serialise them.
  *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  * Outputs and errors are those of pseq_from_doc_ids.
  * ---------------------------------------------------------------------- */

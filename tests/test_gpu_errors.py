@@ -32,7 +32,7 @@ def test_lookback_wait_gives_up_and_reports():
 
     lib = v.load_library()
     rng = np.random.default_rng(0)
-    d = synth.random_doc_ids(rng, 4, 16384, "runs", np.int32)  # 4 tiles of 16384 tokens
+    d = synth.random_doc_ids(rng, 4, 16384, "runs", np.int32)  # 65536 tokens: five tiles
     dt = torch.from_numpy(d).to(DEV)
     try:
         lib.pseq_debug_set_wait(1_000_000, 1)

@@ -6,29 +6,41 @@
 // padding runs are segments, cu_seqlens ends at B*S, max_seqlen is the
 // longest segment.
 //
-// One pass over doc_ids.  CTA t takes tile t (16384 tokens), flags the
-// boundaries in it and summarises them as (count, first, last, largest inner
+// One pass over doc_ids.  CTA t takes tile t (16384 tokens: 1024 threads x
+// 16; a 2M-token map is 128 tiles, one per SM), flags the boundaries in it and summarises them as (count, first, last, largest inner
 // gap) -- an associative "followed by" operation -- with a block scan.  A
 // decoupled look-back over the preceding tiles then gives the tile its
 // exclusive prefix: the output index of its first boundary and the position
-// of the boundary before it, which closes the segment crossing into the tile.
-// The gap term makes max_seqlen a by-product of the scan.
+// of the boundary before it, which closes the segment crossing into the
+// tile.  The gap term makes max_seqlen a by-product of the scan.
 //
-// Every published summary is two 64-bit words, each carrying a valid bit, so
-// a single poll returns the summary itself: no flag-then-value round trip and
-// no release fence on the publishing side.  A look-back round polls 32
-// predecessors at once (one per lane), all loads in flight together, and
-// joins them with a shuffle tree.  A map that fits one tile skips all of
-// this.  Waits are bounded by a time limit and report PSEQ_ERR_TIMEOUT.
-// Boundaries are compacted through shared memory (tile-relative 16-bit
-// positions) and stored coalesced.
+// A tile's summary is one 16-byte slot of two 64-bit words, published first
+// as the tile's own aggregate and then overwritten with the inclusive prefix
+// (everything up to and including the tile).  Each word carries a published
+// bit and an inclusive bit, so one poll returns the summary itself; a poll
+// that catches the two words in different states (mid-overwrite) is simply
+// repeated.  A look-back round polls 128 predecessors at once (four windows
+// of 32, one per lane), all loads in flight together, and joins each window
+// with one ballot, two warp reductions and three shuffles; a map of up to
+// 129 tiles needs one round.  (Four windows with these joins measured
+// faster than one or two on a 2M-token map; 896-thread tiles, which spread
+// that map over 147 SMs instead of 128, did not help.)  Waits are bounded by a time limit and report
+// PSEQ_ERR_TIMEOUT.
+//
+// Warp 0 runs the block scan's second level and the look-back; the other
+// warps are released by a named barrier as soon as the block prefix is
+// known and compact the tile's boundaries into shared memory (tile-relative
+// 16-bit positions) while the look-back runs.  After it, the positions are
+// stored coalesced with the prefix added.  A map that fits one tile skips
+// the look-back and the workspace.
 //
 // The last tile, which holds the whole map's summary once its look-back
-// ends, writes cu_seqlens[num_segments] and the info block itself.  The tiles
-// count themselves done (with any failure they met) in one 64-bit word; the
-// CTA whose add completes the count only reports a failure, if any, and
-// clears the summary words, so the workspace is zero again for the next call
-// and no tile summary is read back at the end.
+// ends, writes cu_seqlens[num_segments] and the info block itself.  Each tile
+// counts itself done (with any failure it met) in one 64-bit word; warp 1
+// issues that add while the other warps store, so its round trip is off the
+// critical path.  In the CTA whose add completes the count, warp 1 reports a
+// failure, if any, and clears the summary words, so the workspace is zero
+// again for the next call and no tile summary is read back at the end.
 #include <mutex>
 
 #include "common.cuh"
@@ -39,14 +51,20 @@ namespace {
 #ifndef PSEQ_SCAN_THREADS
 #define PSEQ_SCAN_THREADS 1024
 #endif
-#ifndef PSEQ_SCAN_ITEMS
-#define PSEQ_SCAN_ITEMS 16
+#ifndef PSEQ_SCAN_WINDOWS
+#define PSEQ_SCAN_WINDOWS 4
+#endif
+#ifndef PSEQ_SCAN_SLOT_BYTES
+#define PSEQ_SCAN_SLOT_BYTES 16
 #endif
 constexpr int kThreads = PSEQ_SCAN_THREADS;
-constexpr int kItems = PSEQ_SCAN_ITEMS;
-constexpr int kPerLane = 1;  // look-back windows of 32 tiles polled together (more unrolled code costs more on a cold instruction cache than extra rounds)
+constexpr int kItems = 16;
+constexpr int kWindows = PSEQ_SCAN_WINDOWS;  // windows of 32 predecessors polled per look-back round
+constexpr int kSlotWords = PSEQ_SCAN_SLOT_BYTES / 8;
 constexpr int kTile = kThreads * kItems;  // tokens per tile
 static_assert(kTile <= 65536, "tile-relative positions are 16-bit");
+static_assert(kThreads % 32 == 0 && kThreads <= 1024, "whole warps, one CTA");
+static_assert(kSlotWords >= 2 && PSEQ_SCAN_SLOT_BYTES % 16 == 0, "a slot holds the two summary words");
 
 // Boundaries inside a span of tokens: how many, the first and last boundary
 // position, and the largest distance between consecutive boundaries.
@@ -77,25 +95,33 @@ __device__ __forceinline__ Bounds shfl(const Bounds& v, int src) {
           __shfl_sync(~0u, v.gap, src)};
 }
 
-// A summary as two self-validating words: {valid, count, last} and
-// {valid, gap, first}.  count and gap are below 2^31, positions fit 32 bits
-// (-1 for "no boundary" round-trips through the unsigned field).
-constexpr unsigned long long kValid = 1ull << 63;
+// A summary as two self-validating words: {published, inclusive, count, last}
+// and {published, inclusive, gap, first}.  count and gap are below 2^31 and
+// take bits 31..61; positions are below 2^31 - 1 and take bits 0..30, with
+// all ones standing for "no boundary".
+constexpr unsigned long long kPublished = 1ull << 63;
+constexpr unsigned long long kInclusive = 1ull << 62;
+constexpr unsigned kNoPos = 0x7fffffffu;
 
-__device__ __forceinline__ unsigned long long word_a(const Bounds& b) {
-  return kValid | ((unsigned long long)(unsigned)b.count << 32) | (unsigned)b.last;
+__device__ __forceinline__ unsigned long long pos_bits(int p) { return p < 0 ? kNoPos : (unsigned)p; }
+__device__ __forceinline__ int pos_of(unsigned long long w) {
+  const unsigned v = (unsigned)(w & kNoPos);
+  return v == kNoPos ? -1 : (int)v;
 }
-__device__ __forceinline__ unsigned long long word_b(const Bounds& b) {
-  return kValid | ((unsigned long long)(unsigned)b.gap << 32) | (unsigned)b.first;
+__device__ __forceinline__ unsigned long long word_a(const Bounds& b, bool incl) {
+  return kPublished | (incl ? kInclusive : 0ull) | ((unsigned long long)(unsigned)b.count << 31) | pos_bits(b.last);
+}
+__device__ __forceinline__ unsigned long long word_b(const Bounds& b, bool incl) {
+  return kPublished | (incl ? kInclusive : 0ull) | ((unsigned long long)(unsigned)b.gap << 31) | pos_bits(b.first);
 }
 __device__ __forceinline__ Bounds from_words(unsigned long long a, unsigned long long b) {
-  return {(int)((a >> 32) & 0x7fffffffu), (int)(unsigned)b, (int)(unsigned)a, (int)((b >> 32) & 0x7fffffffu)};
+  return {(int)((a >> 31) & kNoPos), pos_of(b), pos_of(a), (int)((b >> 31) & kNoPos)};
 }
 
 // Header word: tiles done (bits 0..19), tiles whose wait hit its time limit
 // (bits 20..39), tiles that found a workspace that was not zero-filled
-// (bits 40..59).  A map has at most 2^17 tiles, so no field overflows; the
-// tile that completes the count resets the word to zero.
+// (bits 40..59).  A map has fewer than 2^18 tiles, so no field overflows;
+// the tile that completes the count resets the word to zero.
 constexpr int kTimeoutShift = 20, kBadShift = 40;
 constexpr unsigned long long kCountMask = (1ull << 20) - 1;
 
@@ -105,28 +131,22 @@ struct Header {
 };
 static_assert(sizeof(Header) == 128, "header is 128 bytes");
 
-// Per tile: its own summary and the inclusive one (everything up to it), one
-// 128-byte line per tile, so that a tile's publishing and its neighbours'
-// polls do not contend for one line (32-byte slots, four to a line, made the
-// 2M-token map 4% slower).
-struct Slot {
-  unsigned long long agg_a, agg_b, inc_a, inc_b;
-  unsigned long long pad[12];
-};
-static_assert(sizeof(Slot) == 128, "slot is 128 bytes");
-
 struct Workspace {
   Header* hdr;
-  Slot* slots;  // [tiles]
+  unsigned long long* slots;  // [tiles][kSlotWords]: word a, word b, padding
 };
 
-size_t workspace_bytes(int64_t tiles) { return sizeof(Header) + sizeof(Slot) * (size_t)tiles; }
+size_t workspace_bytes(int64_t tiles) { return sizeof(Header) + 8 * (size_t)kSlotWords * (size_t)tiles; }
 
-Workspace carve(void* base, int64_t tiles) {
+Workspace carve(void* base) {
   unsigned char* p = static_cast<unsigned char*>(base);
-  (void)tiles;
-  return {reinterpret_cast<Header*>(p), reinterpret_cast<Slot*>(p + sizeof(Header))};
+  return {reinterpret_cast<Header*>(p), reinterpret_cast<unsigned long long*>(p + sizeof(Header))};
 }
+
+// Named barrier 1: warp 0 arrives once the block prefix is in shared memory,
+// the other warps wait for it (barrier 0 stays with __syncthreads).
+__device__ __forceinline__ void bar_arrive_1(int threads) { asm volatile("bar.arrive 1, %0;" ::"r"(threads) : "memory"); }
+__device__ __forceinline__ void bar_sync_1(int threads) { asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory"); }
 
 template <typename Id>
 union Items {
@@ -134,15 +154,123 @@ union Items {
   Id v[kItems];
 };
 
+// Summary of one look-back window: lane L holds the summary of the L-th tile
+// back (higher lanes: earlier tiles); lanes with `use` false count as empty.
+// One ballot, two warp reductions and three shuffles, the same in every
+// lane.  The gap into a tile with boundaries is closed by the nearest
+// earlier tile with boundaries in the window (the one before the window is
+// handled when windows are joined).
+__device__ __forceinline__ Bounds window_sum(const Bounds& b, bool use) {
+  const int lane = threadIdx.x & 31;
+  const int cnt = use ? b.count : 0;
+  const unsigned nz = __ballot_sync(~0u, cnt > 0);
+  Bounds r = none();
+  r.count = (int)__reduce_add_sync(~0u, (unsigned)cnt);
+  const unsigned earlier = lane == 31 ? 0u : nz & (~0u << (lane + 1));
+  const int prev_last = __shfl_sync(~0u, b.last, earlier ? __ffs(earlier) - 1 : lane);
+  int g = 0;
+  if (cnt > 0) g = earlier ? max(b.gap, b.first - prev_last) : b.gap;
+  r.gap = (int)__reduce_max_sync(~0u, (unsigned)g);
+  if (nz) {
+    r.last = __shfl_sync(~0u, b.last, __ffs(nz) - 1);
+    r.first = __shfl_sync(~0u, b.first, 31 - __clz(nz));
+  }
+  return r;
+}
+
+// Joins the summaries of tiles j, j-1, ... going back until one of them is an
+// inclusive prefix; returns the summary of everything before tile j + 1.
+// Warp-wide; `gave_up` is set in every lane when a wait ran out.
+__device__ __forceinline__ Bounds look_back(const unsigned long long* slots, int j, int64_t wait_ns, bool& gave_up) {
+  const int lane = threadIdx.x & 31;
+  Bounds run = none();  // summary of the tiles between the polled span and tile j + 1
+  gave_up = false;
+  while (true) {
+    // lane L of window w looks at tile j - 32w - L
+    Bounds b[kWindows];
+    bool incl[kWindows], done[kWindows];
+#pragma unroll
+    for (int w = 0; w < kWindows; ++w) {
+      b[w] = none();
+      incl[w] = true;  // before tile 0: an empty inclusive prefix
+      done[w] = j - 32 * w - lane < 0;
+    }
+    int polls = 0;
+    uint64_t start = 0;
+    bool timed_out = false;
+    while (true) {
+      // every window's loads are issued before any is looked at, so a round
+      // costs one L2 round trip however many windows are open
+      unsigned long long wa[kWindows], wb[kWindows];
+#pragma unroll
+      for (int w = 0; w < kWindows; ++w) {
+        wa[w] = wb[w] = 0ull;
+        if (!done[w]) {
+          const unsigned long long* sl = slots + (size_t)(j - 32 * w - lane) * kSlotWords;
+          wa[w] = ld_relaxed_u64(sl);
+          wb[w] = ld_relaxed_u64(sl + 1);
+        }
+      }
+      bool all_done = true;
+#pragma unroll
+      for (int w = 0; w < kWindows; ++w) {
+        if (done[w]) continue;
+        // both words published and in the same state; otherwise poll again
+        if ((wa[w] & wb[w] & kPublished) && !((wa[w] ^ wb[w]) & kInclusive)) {
+          b[w] = from_words(wa[w], wb[w]);
+          incl[w] = (wa[w] & kInclusive) != 0;
+          done[w] = true;
+        } else {
+          all_done = false;
+        }
+      }
+      if (__all_sync(~0u, all_done)) break;
+      if (polls++ == 0) {
+        start = global_ns();
+      } else if ((int64_t)(global_ns() - start) >= wait_ns) {
+        timed_out = true;  // treat what is missing as an empty inclusive prefix and finish
+#pragma unroll
+        for (int w = 0; w < kWindows; ++w)
+          if (!done[w]) {
+            b[w] = none();
+            incl[w] = true;
+            done[w] = true;
+          }
+        break;
+      }
+    }
+    if (__any_sync(~0u, timed_out)) gave_up = true;
+    // nearest inclusive summary: lowest window, then lowest lane
+    int stop_w = kWindows, stop_l = 32;
+#pragma unroll
+    for (int w = kWindows - 1; w >= 0; --w) {
+      const unsigned m = __ballot_sync(~0u, incl[w]);
+      if (m) {
+        stop_w = w;
+        stop_l = __ffs(m) - 1;
+      }
+    }
+    // Join the counted tiles, farthest window first; tiles past the inclusive
+    // one count as empty.
+    Bounds span = none();
+#pragma unroll
+    for (int w = kWindows - 1; w >= 0; --w)
+      span = join(span, window_sum(b[w], w < stop_w || (w == stop_w && lane <= stop_l)));
+    run = join(span, run);
+    if (stop_w < kWindows) return run;
+    j -= 32 * kWindows;
+  }
+}
+
 template <typename Id, bool kVector, int THREADS>
-__global__ void __launch_bounds__(THREADS, THREADS <= 512 ? 2 : 1)
+__global__ void __launch_bounds__(THREADS, 1)
     doc_ids_scan_kernel(const Id* __restrict__ doc, int N, int S, int32_t* __restrict__ cu,
                         pseq_info* __restrict__ info, Workspace ws, int tiles, int64_t wait_ns,
                         int withhold) {
-  __shared__ Bounds s_warp[(THREADS / 32)];
+  constexpr int kWarps = THREADS / 32;
+  __shared__ Bounds s_warp[kWarps];
   __shared__ Bounds s_prefix;
-  __shared__ int s_last_cta;
-  __shared__ unsigned long long s_state;
+  __shared__ unsigned long long s_fail;  // this tile's failures, in the header word's layout
   __shared__ unsigned short s_pos[(THREADS * kItems)];
 
   pdl_enter();
@@ -188,7 +316,7 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 512 ? 2 : 1)
     }
   }
 
-  // ---- block-wide scan of the summaries (in token order)
+  // ---- warp-level scan of the summaries (in token order)
   Bounds inc = mine;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -197,26 +325,79 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 512 ? 2 : 1)
   }
   if (lane == 31) s_warp[warp] = inc;
   __syncthreads();
+  Bounds before_me = shfl_up(inc, 1);
+  if (lane == 0) before_me = none();
+
+  // Tile-relative boundary positions, in order, from the thread's index of
+  // its first boundary within the tile.
+  auto compact = [&](int li) {
+    for (unsigned m = flags; m; m &= m - 1) s_pos[li++] = (unsigned short)(t0 - tile_base + __ffs(m) - 1);
+  };
+
+  static_assert(THREADS >= 64, "warp 1 counts the tile done");
+  bool timed_out = withhold == tile;  // (warp 0) a withheld summary is reported as a failed wait
+  bool bad_ws = false;                // (thread 0)
+  Bounds tile_sum;
   if (warp == 0) {
-    Bounds w = lane < (THREADS / 32) ? s_warp[lane] : none();
+    // second level of the block scan: warp totals -> inclusive warp prefixes
+    Bounds w = lane < kWarps ? s_warp[lane] : none();
 #pragma unroll
-    for (int d = 1; d < (THREADS / 32); d <<= 1) {
+    for (int d = 1; d < kWarps; d <<= 1) {
       const Bounds o = shfl_up(w, d);
       if (lane >= d) w = join(o, w);
     }
-    if (lane < (THREADS / 32)) s_warp[lane] = w;
+    if (lane < kWarps) s_warp[lane] = w;
+    tile_sum = shfl(w, kWarps - 1);
+    bar_arrive_1(THREADS);  // the other warps may compact now
+    Bounds prefix = none();
+    if (tiles > 1) {
+      unsigned long long* mine_slot = ws.slots + (size_t)tile * kSlotWords;
+      // publish at once; tile 0's own summary is already its inclusive prefix
+      if (lane == 0 && withhold != tile) {
+        st_relaxed_u64(mine_slot, word_a(tile_sum, tile == 0));
+        st_relaxed_u64(mine_slot + 1, word_b(tile_sum, tile == 0));
+      }
+      compact(before_me.count);  // warp 0's own boundaries (block prefix: none)
+      if (tile > 0) {
+        bool gave_up;
+        prefix = look_back(ws.slots, tile - 1, wait_ns, gave_up);
+        if (gave_up) timed_out = true;
+      }
+      if (lane == 0) {
+        const Bounds all = join(prefix, tile_sum);
+        if (tile > 0 && withhold != tile) {
+          st_relaxed_u64(mine_slot, word_a(all, true));
+          st_relaxed_u64(mine_slot + 1, word_b(all, true));
+        }
+        if (tile == tiles - 1 && !timed_out) {
+          // the whole map: close the array and report (a failure elsewhere
+          // overwrites the report at the end)
+          if (all.count >= 1 && all.count <= N) {
+            cu[all.count] = N;
+            *info = {PSEQ_OK, all.count, max(all.gap, N - all.last), N};
+          } else {
+            bad_ws = true;
+          }
+        }
+        // a prefix that does not fit only comes from a workspace that was
+        // not zero-filled
+        if (prefix.count > N - tile_sum.count) bad_ws = true;
+        s_fail = ((unsigned long long)timed_out << kTimeoutShift) | ((unsigned long long)bad_ws << kBadShift);
+      }
+    } else {
+      compact(before_me.count);
+    }
+    if (lane == 0) s_prefix = prefix;
+  } else {
+    bar_sync_1(THREADS);
+    before_me = join(s_warp[warp - 1], before_me);
+    tile_sum = s_warp[kWarps - 1];
+    compact(before_me.count);
   }
   __syncthreads();
-  Bounds before_me = shfl_up(inc, 1);
-  if (lane == 0) before_me = none();
-  if (warp > 0) before_me = join(s_warp[warp - 1], before_me);
-  const Bounds tile_sum = s_warp[(THREADS / 32) - 1];
 
-  // ---- one tile: no neighbours, no workspace
+  // ---- store this tile's boundary positions at the prefix
   if (tiles == 1) {
-    int li = before_me.count;
-    for (unsigned m = flags; m; m &= m - 1) s_pos[li++] = (unsigned short)(t0 - tile_base + __ffs(m) - 1);
-    __syncthreads();
     for (int i = tid; i < tile_sum.count; i += THREADS) cu[i] = (int32_t)s_pos[i];
     if (tid == 0) {
       cu[tile_sum.count] = N;
@@ -224,164 +405,32 @@ __global__ void __launch_bounds__(THREADS, THREADS <= 512 ? 2 : 1)
     }
     return;
   }
-
-  // ---- publish the tile summary, then look back for the exclusive prefix
-  bool timed_out = withhold == tile;  // (thread 0) a withheld summary is reported as a failed wait
-  bool bad_ws = false;                // (thread 0)
-  if (warp == 0) {
-    Slot* mine_slot = ws.slots + tile;
-    Bounds prefix = none();
-    if (tile > 0) {
-      if (lane == 0 && withhold != tile) {
-        st_relaxed_u64(&mine_slot->agg_a, word_a(tile_sum));
-        st_relaxed_u64(&mine_slot->agg_b, word_b(tile_sum));
-      }
-      // Each round polls kPerLane windows of 32 predecessors at once (lane L
-      // of window w looks at tile j - 32w - L), waits until every one has
-      // published, and joins the tiles after the nearest inclusive summary.
-      Bounds run = none();  // summary of the tiles between the polled span and this one
-      int j = tile - 1;
-      bool gave_up = false;
-      while (true) {
-        Bounds b[kPerLane];
-        bool incl[kPerLane], done[kPerLane];
-#pragma unroll
-        for (int w = 0; w < kPerLane; ++w) {
-          b[w] = none();
-          incl[w] = true;  // before tile 0: an empty inclusive prefix
-          done[w] = j - 32 * w - lane < 0;
-        }
-        int polls = 0;
-        uint64_t start = 0;
-        while (true) {
-          // issue every window's loads before looking at any of them, so a
-          // round costs one L2 round trip however many windows are open
-          unsigned long long ia[kPerLane], ib[kPerLane], aa[kPerLane], ab[kPerLane];
-#pragma unroll
-          for (int w = 0; w < kPerLane; ++w) {
-            ia[w] = ib[w] = aa[w] = ab[w] = 0ull;
-            if (!done[w]) {
-              const Slot* sl = ws.slots + (j - 32 * w - lane);
-              ia[w] = ld_relaxed_u64(&sl->inc_a);
-              ib[w] = ld_relaxed_u64(&sl->inc_b);
-              aa[w] = ld_relaxed_u64(&sl->agg_a);
-              ab[w] = ld_relaxed_u64(&sl->agg_b);
-            }
-          }
-          bool all_done = true;
-#pragma unroll
-          for (int w = 0; w < kPerLane; ++w) {
-            if (done[w]) continue;
-            if (ia[w] & ib[w] & kValid) {
-              b[w] = from_words(ia[w], ib[w]);
-              done[w] = true;
-            } else if (aa[w] & ab[w] & kValid) {
-              b[w] = from_words(aa[w], ab[w]);
-              incl[w] = false;
-              done[w] = true;
-            } else {
-              all_done = false;
-            }
-          }
-          if (all_done) break;
-          if (polls++ == 0) {
-            start = global_ns();
-          } else if ((int64_t)(global_ns() - start) >= wait_ns) {
-            gave_up = true;  // treat what is missing as an empty inclusive prefix and finish
-#pragma unroll
-            for (int w = 0; w < kPerLane; ++w)
-              if (!done[w]) {
-                b[w] = none();
-                incl[w] = true;
-                done[w] = true;
-              }
-            break;
-          }
-        }
-        // nearest inclusive summary: lowest window, then lowest lane
-        int stop_w = kPerLane, stop_l = 32;
-#pragma unroll
-        for (int w = kPerLane - 1; w >= 0; --w) {
-          const unsigned m = __ballot_sync(~0u, incl[w]);
-          if (m) {
-            stop_w = w;
-            stop_l = __ffs(m) - 1;
-          }
-        }
-        // Join the counted tiles, farthest first.  Within a window a higher
-        // lane holds an earlier tile, so a shuffle-down tree leaves
-        // x_31 . x_30 . ... . x_0 in lane 0; tiles past the inclusive one
-        // count as empty.
-#pragma unroll
-        for (int w = 0; w < kPerLane; ++w) {
-          if (w > stop_w || (w == stop_w && lane > stop_l)) b[w] = none();
-#pragma unroll
-          for (int d = 1; d < 32; d <<= 1) {
-            const Bounds o = {__shfl_down_sync(~0u, b[w].count, d), __shfl_down_sync(~0u, b[w].first, d),
-                              __shfl_down_sync(~0u, b[w].last, d), __shfl_down_sync(~0u, b[w].gap, d)};
-            if (lane + d < 32) b[w] = join(o, b[w]);
-          }
-        }
-        Bounds span = none();
-#pragma unroll
-        for (int w = kPerLane - 1; w >= 0; --w) span = join(span, shfl(b[w], 0));
-        run = join(span, run);
-        if (stop_w < kPerLane) break;
-        j -= 32 * kPerLane;
-      }
-      if (__any_sync(~0u, gave_up)) timed_out = true;
-      prefix = run;
-    }
-    if (lane == 0) {
-      const Bounds all = join(prefix, tile_sum);
-      if (withhold != tile) {
-        st_relaxed_u64(&mine_slot->inc_a, word_a(all));
-        st_relaxed_u64(&mine_slot->inc_b, word_b(all));
-      }
-      if (tile == tiles - 1 && !timed_out) {
-        // the whole map: close the array and report (a failure elsewhere
-        // overwrites the report at the end)
-        if (all.count >= 1 && all.count <= N) {
-          cu[all.count] = N;
-          *info = {PSEQ_OK, all.count, max(all.gap, N - all.last), N};
-        } else {
-          bad_ws = true;
-        }
-      }
-      s_prefix = prefix;
-    }
+  // Warp 1 counts the tile done (with its failures): after the barrier,
+  // every read and write of the summaries by this tile has happened, and the
+  // add's round trip overlaps the stores.  The CTA whose add completes the
+  // count clears the workspace with warp 1 alone; every look-back has ended
+  // by then.
+  unsigned long long old = 0, add = 0;
+  if (tid == 32) {
+    add = 1ull | s_fail;
+    old = add_acq_rel_u64(&ws.hdr->state, add);
   }
-
-  // ---- compact this tile's boundary positions and store them
-  int li = before_me.count;
-  for (unsigned m = flags; m; m &= m - 1) s_pos[li++] = (unsigned short)(t0 - tile_base + __ffs(m) - 1);
-  __syncthreads();
   const int base = s_prefix.count;
-  if (base >= 0 && base <= N - tile_sum.count) {
+  if (base >= 0 && base <= N - tile_sum.count)  // else counted as a bad workspace above
     for (int i = tid; i < tile_sum.count; i += THREADS) cu[base + i] = (int32_t)(tile_base + s_pos[i]);
-  } else if (tid == 0) {
-    bad_ws = true;  // only reachable from a workspace that was not zero-filled
-  }
-  if (tid == 0) {
-    const unsigned long long add =
-        1ull | ((unsigned long long)timed_out << kTimeoutShift) | ((unsigned long long)bad_ws << kBadShift);
-    const unsigned long long old = add_acq_rel_u64(&ws.hdr->state, add);
-    s_last_cta = (old & kCountMask) == (unsigned long long)(tiles - 1);
-    s_state = old + add;
-  }
-  __syncthreads();
-  if (!s_last_cta) return;
+  if (warp != 1) return;
+  old = __shfl_sync(~0u, old, 0);
+  if ((old & kCountMask) != (unsigned long long)(tiles - 1)) return;
 
   // ---- last CTA: report a failure, if any, and clear the workspace
-  if (tid == 0) {
-    const unsigned long long all = s_state;
+  if (lane == 0) {
+    const unsigned long long all = old + add;
     const bool timeouts = ((all >> kTimeoutShift) & kCountMask) != 0;
     const bool bad = ((all >> kBadShift) & kCountMask) != 0;
     if (timeouts || bad) *info = {bad ? PSEQ_ERR_ARG : PSEQ_ERR_TIMEOUT, 0, 0, N};
     ws.hdr->state = 0;  // the next call starts after this grid completes
   }
-  unsigned long long* words = reinterpret_cast<unsigned long long*>(ws.slots);
-  for (int i = tid; i < 4 * tiles; i += THREADS) words[(i >> 2) * 16 + (i & 3)] = 0ull;  // the four words of each slot
+  for (int i = lane; i < 2 * tiles; i += 32) ws.slots[(size_t)(i >> 1) * kSlotWords + (i & 1)] = 0ull;
 }
 
 __global__ void empty_map_kernel(int32_t* cu, pseq_info* info) {
@@ -396,8 +445,8 @@ cudaError_t launch_scan(const void* doc, int N, int S, int32_t* cu, pseq_info* i
   const Id* d = static_cast<const Id*>(doc);
   const int64_t wait = wait_limit_ns();
   const int withhold = (int)(withhold_tile() < 0 ? -1 : (withhold_tile() > INT32_MAX ? -1 : withhold_tile()));
-  // a map that fits half a tile runs as one 512-thread CTA (a 1024-thread
-  // CTA would leave half its threads idle)
+  // a map of up to 8192 tokens runs as one 512-thread CTA (a full-size CTA
+  // would leave threads idle)
   constexpr int kSmall = 512;
   const bool small = tiles == 1 && N <= kSmall * kItems;
   if (aligned(doc, 16))
@@ -452,7 +501,7 @@ extern "C" pseq_status pseq_from_doc_ids(const void* doc_ids, int32_t id_bytes, 
   const size_t need = workspace_bytes(tiles);
   if (!workspace || ws_bytes < need || !aligned(workspace, 16))
     return fail(PSEQ_ERR_ARG, "pseq_from_doc_ids: workspace needs %zu bytes, 16-byte aligned (got %zu)", need, ws_bytes);
-  Workspace ws = carve(workspace, tiles);
+  Workspace ws = carve(workspace);
   const cudaError_t e = id_bytes == 4
                             ? launch_scan<int32_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st)
                             : launch_scan<int64_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st);
@@ -475,8 +524,8 @@ namespace pseq {
 namespace {
 
 constexpr int64_t kStaticMaxTokens = PSEQ_STATIC_MAX_TOKENS;  // B*S limit of the static scratch
-constexpr int64_t kStaticMaxTiles = kStaticMaxTokens / kTile;
-constexpr size_t kStaticBytes = sizeof(Header) + sizeof(Slot) * kStaticMaxTiles;
+constexpr int64_t kStaticMaxTiles = (kStaticMaxTokens + kTile - 1) / kTile;  // a map at the limit fits
+constexpr size_t kStaticBytes = sizeof(Header) + 8 * (size_t)kSlotWords * (size_t)kStaticMaxTiles;
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
 
@@ -536,7 +585,7 @@ extern "C" pseq_status pseq_from_doc_ids_static(const void* doc_ids, int32_t id_
   const size_t clear = workspace_bytes(tiles);
   cudaError_t e = cudaMemsetAsync(scratch, 0, clear, st);
   if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: cudaMemsetAsync: %s", fn, cudaGetErrorString(e));
-  Workspace ws = carve(scratch, tiles);
+  Workspace ws = carve(scratch);
   e = id_bytes == 4 ? launch_scan<int32_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st)
                     : launch_scan<int64_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st);
   count_launches(1);
