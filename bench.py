@@ -43,7 +43,7 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 METRIC = "packed tokens/sec and achieved HBM GB/s (% of GB300 peak), 1 GPU"
-EMB_SAMPLE = 8  # the embedding call is bracketed with events on every 8th timed step
+EMB_SAMPLE = 2  # the embedding call's end is marked with an event on every 2nd timed step
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
 WORKLOAD = ("packed-sequence preprocessing step: doc_ids map [4,2048] + its THD batch (int64 ids/labels/positions); "
@@ -121,6 +121,43 @@ def make_inputs(seed: int) -> dict:
         "thd_emb": synth.thd_embeddings(seed),
         "squeeze": synth.squeeze(seed),
         "map_stress": synth.doc_map_stress(seed),
+    }
+
+
+# fields each id-stream THD part moves (name, planes); int64 elements, one per token
+THD_FIELDS = {
+    "thd_small": (("input_ids", 1), ("labels", 1), ("position_ids", 1)),
+    "thd_ids": (("input_ids", 1), ("labels", 1), ("position_ids", 3)),
+}
+L2_NOTE = "flushed between steps outside the timed events (256 MiB write, then 256 MiB read of another buffer)"
+
+
+def part_bytes(name: str, part, count: int, total: int) -> int:
+    """Algorithmic bytes of one call -- what the method must read and write --
+    from the call's inputs and what it produced: ``count`` segments, kept
+    sequences or bin members, ``total`` tokens in the produced stream."""
+    if name.startswith("map"):
+        return part.size * 4 + 4 * (count + 1)
+    if name.startswith("thd"):
+        if "hidden" in part:
+            moved = 2 * total * part["hidden"].shape[2] * 2
+        else:
+            moved = sum(2 * planes * total * 8 for _, planes in THD_FIELDS[name])
+        return moved + total + 8 * (count + 1) + 2 * 8 * part["seq_lens"].size
+    nb = len(part["bin_offsets"]) - 1
+    return 8 * int(part["real_lens"].sum()) + 9 * nb * part["width"] + 8 * (count + nb)
+
+
+def step_config(tokens: dict, alg_bytes: dict, world: int) -> dict:
+    """The ``config`` of the JSON line, the same for both arms: the workload,
+    its tokens and algorithmic bytes per step, how L2 is handled."""
+    return {
+        "workload": WORKLOAD,
+        "tokens_per_step_per_gpu": int(sum(tokens.values())),
+        "parts_tokens": {k: int(v) for k, v in tokens.items()},
+        "algorithmic_bytes_per_step": int(sum(alg_bytes.values())),
+        "l2": L2_NOTE,
+        "parallelism": f"replicas x{world} (independent batches per GPU)",
     }
 
 
@@ -277,15 +314,20 @@ class NativeStep:
             self._squeeze("squeeze", h["squeeze"])
         if self._want("map_stress"):
             self._map("map_stress", h["map_stress"])
-        # a larger squeeze, timed on its own only (never part of the step)
+        # extras timed on their own only (never part of the step): a larger
+        # squeeze, and the embedding batch with rows that end short
         if self.only is not None and self._want("squeeze_scaled"):
             self._squeeze("squeeze_scaled", h["squeeze_scaled"])
+        if self.only is not None and self._want("thd_emb_ragged"):
+            self._thd("thd_emb_ragged", h["thd_emb_ragged"], [], hidden=h["thd_emb_ragged"]["hidden"])
         # the same calls with the side stream's handle (every ABI call takes its stream last)
         self.side_calls = [(name, fn, args[:-1] + (self.side_sh,)) for name, fn, args in self.calls]
         self.torch.cuda.synchronize(self.dev)
 
-    def run(self, emb_events=None, two_streams=False):
-        """Issue one step; optionally bracket the embedding call with events.
+    def run(self, emb_end=None, two_streams=False):
+        """Issue one step; optionally mark the end of the embedding call with
+        an event (it is the step's first call, so the step's start event
+        marks its start).
 
         The embedding conversion goes first, on self.stream.  With two_streams
         the other calls go to the side stream (forked from and joined back
@@ -300,11 +342,9 @@ class NativeStep:
         for name, fn, args in self.calls:
             if name != "thd_emb":
                 continue
-            if emb_events is not None:
-                emb_events[0].record(self.stream)
             self._ok(name, fn(*args))
-            if emb_events is not None:
-                emb_events[1].record(self.stream)
+            if emb_end is not None:
+                emb_end.record(self.stream)
         for name, fn, args in (self.side_calls if two else self.calls):
             if name != "thd_emb":
                 self._ok(name, fn(*args))
@@ -330,23 +370,17 @@ class NativeStep:
             if name.startswith("map"):
                 _, cu, d = res
                 self.outputs.append((cu, 4 * (info[1] + 1)))
-                self.alg_bytes[name] = d.numel() * 4 + 4 * (info[1] + 1)
             elif name.startswith("thd"):
                 _, cu, cup, mask, dsts = res
                 n, T = info[1], info[3]
                 self.tokens[name] = T
                 self.outputs += [(cu, 4 * (n + 1)), (cup, 4 * (n + 1)), (mask, T)]
-                moved = 0
                 for dst, planes, row, eb in dsts:
                     self.outputs.append((dst, planes * T * row * eb))
-                    moved += 2 * planes * T * row * eb
-                self.alg_bytes[name] = moved + T + 8 * (n + 1) + 2 * 8 * self.host[name]["seq_lens"].size
             else:
                 _, cu, cup, mask, out, ncu = res
                 self.outputs += [(cu, 4 * ncu), (cup, 4 * ncu), (mask, mask.numel()), (out, out.numel() * 8)]
-                c = self.host[name]
-                real_bytes = 8 * int(c["real_lens"].sum())
-                self.alg_bytes[name] = real_bytes + out.numel() * 8 + mask.numel() + 8 * ncu
+            self.alg_bytes[name] = part_bytes(name, self.host[name], info[1], info[3])
         self.emb_bytes = self.alg_bytes.get("thd_emb")
         self.h2d_bytes = sum(h.numel() * h.element_size() for _, h in self.inputs)
         self.d2h_bytes = sum(n for _, n in self.outputs)
@@ -553,26 +587,22 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "thd_fused_bulk_traffic.json")
+
+
 def profiled_traffic():
-    """DRAM bytes per launch of the embedding conversion from the committed
-    ncu summary, or None when the kernels changed since that capture."""
-    path = os.path.join(ROOT, "profiles", "per_kernel_dram.md")
+    """DRAM bytes (read + write) per launch of the embedding conversion from
+    the committed ncu figures, or None when the kernel's sources changed since
+    that capture."""
     try:
-        with open(path) as f:
-            text = f.read()
-    except OSError:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    vals = {}
-    for line in text.splitlines():
-        if ":" in line and line.strip().startswith("- "):
-            k, _, val = line.strip()[2:].partition(":")
-            vals[k.strip()] = val.strip().strip("`")
-    if vals.get("kernel_source_sha") != kernel_source_hash():
+    if rec.get("kernel_source_sha") != kernel_source_hash():
         return None
-    try:
-        return int(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    v = rec.get("dram_bytes_per_launch")
+    return int(v) if isinstance(v, (int, float)) else None
 
 
 class ClockSampler:
@@ -677,8 +707,7 @@ def run_native(args, dist: Dist):
     K = args.steps
     W = max(args.warmup, 3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) if i % EMB_SAMPLE == 0
-           else None for i in range(K)]
+    gev = [torch.cuda.Event(enable_timing=True) if i % EMB_SAMPLE == 0 else None for i in range(K)]
     with torch.cuda.stream(stream):
         for _ in range(W):
             flush_l2()
@@ -729,7 +758,7 @@ def run_native(args, dist: Dist):
     clocks.stop()
 
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    emb_ms = [g[0].elapsed_time(g[1]) for g in gev if g is not None]
+    emb_ms = [ev[i][0].elapsed_time(g) for i, g in enumerate(gev) if g is not None]
     total_ms = dist.max(sum(step_ms), dev)
     ms_per_step = total_ms / K
     all_tokens = dist.sum(float(tokens), dev)
@@ -799,6 +828,7 @@ def run_native(args, dist: Dist):
     per_config = torch_gpu = launch_floor = None
     if dist.rank == 0:
         host["squeeze_scaled"] = synth.squeeze(args.seed, N=16384)
+        host["thd_emb_ragged"] = synth.thd_embeddings_ragged(args.seed)
         per_config = time_per_config(step, host, dev, stream, flush_l2, peak)
         launch_floor = time_launch_floor(dev, stream, flush_l2)
         torch_gpu = time_torch_restatement(host, dev, stream, flush_l2, per_config)
@@ -806,7 +836,7 @@ def run_native(args, dist: Dist):
     achieved = step.emb_bytes / (emb_avg_ms / 1e3) / 1e9
     traffic = profiled_traffic()
     cpu = None
-    if dist.rank == 0:
+    if dist.rank == 0 and dist.world == 1:
         cpu = cpu_baseline(host, budget_s=10.0)
         cpu.update(cpu_description())
         cpu["per_config_full_size"] = oracle_per_config(host)
@@ -825,13 +855,8 @@ def run_native(args, dist: Dist):
             "vs_baseline": None,
             "dtype": "int64",
             "data": "synthetic (seeded generators; shapes and length mixes of packed SFT batches)",
-            "config": {
-                "workload": WORKLOAD,
-                "tokens_per_step_per_gpu": tokens,
-                "parts_tokens": step.tokens,
-                "l2": "flushed between steps outside the timed events (256 MiB write, then 256 MiB read of another buffer)",
-                "parallelism": f"replicas x{dist.world} (independent batches per GPU)",
-                "algorithmic_bytes_per_step": sum(step.alg_bytes.values()),
+            "config": step_config(step.tokens, step.alg_bytes, dist.world),
+            "step_variants": {
                 "launch": "direct C ABI calls from prebuilt ctypes arguments; the embedding conversion first "
                           "on the step's stream, the other five calls on a second stream forked from and joined "
                           "back into it",
@@ -852,9 +877,11 @@ def run_native(args, dist: Dist):
                 "traffic": traffic,
                 "algorithmic_bytes_per_launch": step.emb_bytes,
                 "avg_launch_us": round(emb_avg_ms * 1e3, 3),
-                "timed_as": f"CUDA events on the step's stream around the call, on every {EMB_SAMPLE}th timed step "
-                            f"({len(emb_ms)} launches; the event pair costs about 4 us of step time, so it is "
-                            "not recorded on every step)",
+                "launch_us_min_median_max": [round(min(emb_ms) * 1e3, 3), round(statistics.median(emb_ms) * 1e3, 3),
+                                             round(max(emb_ms) * 1e3, 3)],
+                "timed_as": f"CUDA events on the step's stream: the step's start event (the call is the step's "
+                            f"first) to an event recorded right after the call, on every {EMB_SAMPLE}nd timed step "
+                            f"({len(emb_ms)} launches)",
                 "whole_step": {"achieved": round(sum(step.alg_bytes.values()) / (ms_per_step / 1e3) / 1e9, 1),
                                "frac": round(sum(step.alg_bytes.values()) / (ms_per_step / 1e3) / 1e9 / peak, 4),
                                "what": "algorithmic bytes of all six calls per step over ms_per_step: the step "
@@ -900,6 +927,8 @@ PER_CONFIG = (
     ("squeeze", "C3 squeeze int64 [256,4096] -> FFD bins x 32768, stretched"),
     ("map_stress", "C4 doc_ids int32 [64,32768], ~250k segments"),
     ("squeeze_scaled", "scaled squeeze (labelled extra, not a config): int64 [16384,4096] -> FFD bins x 32768"),
+    ("thd_emb_ragged", "C2 with rows ending short (labelled extra, not a config): bf16 hidden [4,8192,4096], each "
+                       "row's last sequence dropped, so T < B*S and every later row moves to a lower stream offset"),
 )
 ROTATE_MAX_SETS = 4096
 
@@ -1234,40 +1263,74 @@ def cpu_description() -> dict:
     return {"cpu_model": model, "os_cpu_count": os.cpu_count(), "cores_used": 1}
 
 
+class OracleStep:
+    """One whole step on the host: the oracle's function for every call of the
+    step, each on its full-size input.  ``run`` returns, per part, the
+    produced (count, stream tokens) -- the same figures the native arm reads
+    from each call's info block."""
+
+    def __init__(self, host: dict):
+        import oracle
+        import torch
+
+        self.host = host
+
+        def map_call(d):
+            def run():
+                cu, _ = oracle.from_doc_ids(d)
+                return len(cu) - 1, d.size
+            return run
+
+        def thd_call(bt):
+            def run():
+                r = oracle.process_input_for_thd(bt)
+                return len(r["cu_seqlens"]) - 1, r["total_tokens"]
+            return run
+
+        def emb_call(emb):
+            h = emb["hidden"].view(torch.int16).numpy()
+
+            def run():
+                meta = oracle.thd_meta(emb["seq_lens"], emb["seq_lens_padded"], h.shape[1])
+                oracle.thd_gather(h, meta, h.shape[0], h.shape[1])
+                oracle.thd_padding_mask(meta["total_tokens"], meta["seq_real"], meta["seq_padded"])
+                return meta["num_sequences"], meta["total_tokens"]
+            return run
+
+        def squeeze_call(sq):
+            def run():
+                oracle.pack_squeeze(sq["src"], sq["real_lens"], sq["bin_offsets"], sq["bin_members"], sq["multiple"],
+                                    sq["capacity"], sq["stretch"], sq["width"], sq["pad_value"])
+                return int(sq["bin_offsets"][-1]), (len(sq["bin_offsets"]) - 1) * sq["width"]
+            return run
+
+        self.calls = {"map_small": map_call(host["map_small"]), "thd_small": thd_call(host["thd_small"]),
+                      "thd_ids": thd_call(host["thd_ids"]), "thd_emb": emb_call(host["thd_emb"]),
+                      "squeeze": squeeze_call(host["squeeze"]), "map_stress": map_call(host["map_stress"])}
+        self.extras = {}
+        if "squeeze_scaled" in host:
+            self.extras["squeeze_scaled"] = squeeze_call(host["squeeze_scaled"])
+        if "thd_emb_ragged" in host:
+            self.extras["thd_emb_ragged"] = emb_call(host["thd_emb_ragged"])
+
+    def run(self) -> dict:
+        return {name: fn() for name, fn in self.calls.items()}
+
+    def tokens_and_bytes(self, produced: dict):
+        """Per-part stream tokens and algorithmic bytes of one step."""
+        tokens = {k: t for k, (_, t) in produced.items()}
+        alg = {k: part_bytes(k, self.host[k], c, t) for k, (c, t) in produced.items()}
+        return tokens, alg
+
+
 def oracle_per_config(host: dict) -> dict:
     """Wall-clock time of the oracle on every configuration at full size,
-    single-threaded: median of 5 runs (3 for the embedding batch)."""
-    import oracle
-    import torch
-
-    def map_call(d):
-        return lambda: oracle.from_doc_ids(d)
-
-    def thd_call(bt):
-        return lambda: oracle.process_input_for_thd(bt)
-
-    def emb_call(emb):
-        h = emb["hidden"].view(torch.int16).numpy()
-
-        def run():
-            meta = oracle.thd_meta(emb["seq_lens"], emb["seq_lens_padded"], h.shape[1])
-            oracle.thd_gather(h, meta, h.shape[0], h.shape[1])
-            oracle.thd_padding_mask(meta["total_tokens"], meta["seq_real"], meta["seq_padded"])
-        return run
-
-    def squeeze_call(sq):
-        return lambda: oracle.pack_squeeze(sq["src"], sq["real_lens"], sq["bin_offsets"], sq["bin_members"],
-                                           sq["multiple"], sq["capacity"], sq["stretch"], sq["width"],
-                                           sq["pad_value"])
-
-    calls = {"map_small": map_call(host["map_small"]), "thd_small": thd_call(host["thd_small"]),
-             "thd_ids": thd_call(host["thd_ids"]), "thd_emb": emb_call(host["thd_emb"]),
-             "squeeze": squeeze_call(host["squeeze"]), "map_stress": map_call(host["map_stress"])}
-    if "squeeze_scaled" in host:
-        calls["squeeze_scaled"] = squeeze_call(host["squeeze_scaled"])
+    single-threaded: median of 5 runs (3 for the embedding batches and the
+    scaled squeeze)."""
+    step = OracleStep(host)
     out = {}
-    for name, fn in calls.items():
-        n = 3 if name in ("thd_emb", "squeeze_scaled") else 5
+    for name, fn in list(step.calls.items()) + list(step.extras.items()):
+        n = 3 if name in ("thd_emb", "thd_emb_ragged", "squeeze_scaled") else 5
         ts = []
         for _ in range(n):
             t0 = time.perf_counter()
@@ -1281,13 +1344,12 @@ def oracle_per_config(host: dict) -> dict:
 # oracle arms: cpu_baseline (inside the native run) and --impl reference
 # ----------------------------------------------------------------------------
 class OracleUnits:
-    """The composite workload cut into small independent units for the oracle.
-
-    Units: one row of a doc_ids map (rows are independent: every row start is
-    a boundary), one row of a THD batch, one sequence of the embedding batch,
-    one bin of the squeeze.  Each unit runs the oracle function on its own
-    sub-problem; rates are kept per part.
-    """
+    """The step cut into small independent units for a bounded sample: one
+    row of a doc_ids map (rows are independent: every row start is a
+    boundary), one row of a THD batch, one sequence of the embedding batch,
+    one bin of the squeeze.  ``step(fraction)`` runs that fraction of every
+    part's units (at least one each), cycling through them, and returns the
+    tokens produced and the seconds spent."""
 
     def __init__(self, host: dict):
         import oracle
@@ -1295,22 +1357,19 @@ class OracleUnits:
 
         self.oracle = oracle
         self.parts = {}
-        ms = host["map_small"]
-        self.parts["map_small"] = ([ms[b:b + 1] for b in range(ms.shape[0])], ms.size)
-        mst = host["map_stress"]
-        self.parts["map_stress"] = ([mst[b:b + 1] for b in range(mst.shape[0])], mst.size)
+        for name in ("map_small", "map_stress"):
+            m = host[name]
+            self.parts[name] = [m[b:b + 1] for b in range(m.shape[0])]
         for name in ("thd_small", "thd_ids"):
             bt = host[name]
-            B = bt["input_ids"].shape[0]
             units = []
-            for b in range(B):
+            for b in range(bt["input_ids"].shape[0]):
                 sub = {"input_ids": bt["input_ids"][b:b + 1], "labels": bt["labels"][b:b + 1],
                        "seq_lens": bt["seq_lens"][b:b + 1], "seq_lens_padded": bt["seq_lens_padded"][b:b + 1]}
                 pos = bt["position_ids"]
                 sub["position_ids"] = pos[:, b:b + 1] if pos.ndim == 3 else pos[b:b + 1]
                 units.append(sub)
-            meta = oracle.thd_meta(bt["seq_lens"], bt["seq_lens_padded"], bt["input_ids"].shape[1])
-            self.parts[name] = (units, meta["total_tokens"])
+            self.parts[name] = units
         emb = host["thd_emb"]
         h = emb["hidden"].view(torch.int16).numpy()
         meta = oracle.thd_meta(emb["seq_lens"], emb["seq_lens_padded"], h.shape[1])
@@ -1319,17 +1378,11 @@ class OracleUnits:
             b, o, r, p = (int(meta[k][i]) for k in ("seq_row", "seq_off", "seq_real", "seq_padded"))
             units.append({"hidden": h[b:b + 1, o:o + p], "seq_lens": np.array([[r]], np.int64),
                           "seq_lens_padded": np.array([[p]], np.int64)})
-        self.parts["thd_emb"] = (units, meta["total_tokens"])
+        self.parts["thd_emb"] = units
         sq = host["squeeze"]
-        units = []
-        for members in sq["bins"]:
-            offs, mem = oracle.bins_to_csr([members])
-            units.append((sq["src"], sq["real_lens"], offs, mem))
-        self.parts["squeeze"] = (units, len(sq["bins"]) * sq["width"])
+        self.parts["squeeze"] = [(sq["src"], sq["real_lens"]) + tuple(oracle.bins_to_csr([m])) for m in sq["bins"]]
         self.sq = sq
         self.next = {k: 0 for k in self.parts}
-        self.done_tokens = {k: 0 for k in self.parts}
-        self.done_s = {k: 0.0 for k in self.parts}
 
     def _run(self, name, u):
         o = self.oracle
@@ -1349,85 +1402,103 @@ class OracleUnits:
                        sq["pad_value"])
         return sq["width"]
 
-    def step(self):
-        """One unit of every part; returns the seconds spent."""
-        spent = 0.0
-        for name, (units, _) in self.parts.items():
-            u = units[self.next[name] % len(units)]
-            self.next[name] += 1
-            t0 = time.perf_counter()
-            tok = self._run(name, u)
-            dt = time.perf_counter() - t0
-            self.done_tokens[name] += tok
-            self.done_s[name] += dt
-            spent += dt
-        return spent
-
-    def composite(self):
-        """Seconds the oracle needs for one whole step, from per-part rates."""
-        total_s, tokens = 0.0, 0
-        for name, (_, part_tokens) in self.parts.items():
-            rate = self.done_tokens[name] / max(self.done_s[name], 1e-12)
-            total_s += part_tokens / rate
-            tokens += part_tokens
-        return total_s, tokens
-
-    def units_done(self):
-        return sum(self.next.values())
+    def step(self, fraction: float):
+        tokens, spent = 0, 0.0
+        for name, units in self.parts.items():
+            for _ in range(max(1, int(round(fraction * len(units))))):
+                u = units[self.next[name] % len(units)]
+                self.next[name] += 1
+                t0 = time.perf_counter()
+                tokens += self._run(name, u)
+                spent += time.perf_counter() - t0
+        return tokens, spent
 
 
 def cpu_baseline(host: dict, budget_s: float = 10.0) -> dict:
-    u = OracleUnits(host)
+    """The oracle, single-threaded, on whole steps of the same workload for
+    about ``budget_s`` seconds (at least two steps)."""
+    step = OracleStep(host)
+    step.run()  # warm-up
     t0 = time.perf_counter()
-    steps = 0
-    while time.perf_counter() - t0 < budget_s or steps < 2:
-        u.step()
-        steps += 1
-    step_s, tokens = u.composite()
-    return {"value": round(tokens / step_s, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{u.units_done()} oracle units ({steps} rounds of one map row, one THD row per batch, one "
-                      f"embedding sequence and one squeeze bin), {time.perf_counter() - t0:.1f} s single-threaded; "
-                      f"per-part rates combined over one whole step ({tokens} tokens)",
-            "oracle_ms_per_step": round(step_s * 1e3, 3)}
+    n, tokens = 0, 0
+    while time.perf_counter() - t0 < budget_s or n < 2:
+        produced = step.run()
+        tokens += sum(t for _, t in produced.values())
+        n += 1
+    wall = time.perf_counter() - t0
+    return {"value": round(tokens / wall, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} whole steps (all six calls of the step at full size, one after another) in {wall:.1f} s "
+                      f"on one core, after one warm-up step",
+            "oracle_ms_per_step": round(wall / n * 1e3, 3)}
+
+
+REF_BUDGET_S = 150.0  # the reference arm's timed steps stay within about this many seconds
 
 
 def run_reference(args, dist: Dist):
+    """The oracle arm: the oracle as it stands, on one host core, on whole
+    steps of the native arm's workload (each step a bounded sample of it when
+    --steps is too large to finish within a few minutes).  Under torchrun
+    rank 0 alone runs and prints; the other ranks exit without work."""
     if dist.world > 1:
         dist.init("gloo")
         if dist.rank != 0:
             dist.close()
             return
     host = make_inputs(args.seed)
-    u = OracleUnits(host)
-    for _ in range(max(args.warmup, 3)):
-        u.step()
-    u.done_tokens = {k: 0 for k in u.parts}
-    u.done_s = {k: 0.0 for k in u.parts}
+    step = OracleStep(host)
+    K, W = args.steps, max(args.warmup, 3)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        u.step()
-    wall = time.perf_counter() - t0
-    step_s, tokens = u.composite()
-    value = tokens / step_s
+    produced = step.run()
+    est = time.perf_counter() - t0
+    tokens_by_part, alg = step.tokens_and_bytes(produced)
+    step_tokens = sum(tokens_by_part.values())
+    whole = (K + W) * est <= REF_BUDGET_S
+    if whole:
+        for _ in range(W - 1):
+            step.run()
+        t0 = time.perf_counter()
+        for _ in range(K):
+            step.run()
+        wall = time.perf_counter() - t0
+        value = K * step_tokens / wall
+        ms_per_step = wall / K * 1e3
+        sample = (f"{K} whole steps (all six calls of the step at full size, one after another) after {W} warm-up "
+                  f"steps, {wall:.1f} s on one core")
+    else:
+        units = OracleUnits(host)
+        fraction = min(1.0, REF_BUDGET_S / ((K + W) * est))
+        for _ in range(W):
+            units.step(fraction)
+        tokens, spent = 0, 0.0
+        t0 = time.perf_counter()
+        for _ in range(K):
+            tk, sp = units.step(fraction)
+            tokens += tk
+            spent += sp
+        wall = time.perf_counter() - t0
+        value = tokens / wall
+        ms_per_step = wall / K * 1e3
+        sample = (f"{K} steps, each a bounded sample ({fraction:.3f} of the units of every part: map rows, THD rows, "
+                  f"embedding sequences, squeeze bins) of the whole step, {wall:.1f} s on one core")
+    if dist.world > 1:
+        sample += f"; rank 0 of {dist.world} alone (one host core), the other ranks exit without work"
     line = {
         "impl": "reference",
         "metric": METRIC,
         "value": round(value, 1),
         "unit": UNIT,
         "n_gpus": dist.world,
-        "steps": args.steps,
-        "warmup": max(args.warmup, 3),
-        "ms_per_step": round(step_s * 1e3, 4),
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "int64",
         "data": "synthetic (seeded generators; shapes and length mixes of packed SFT batches)",
-        "config": {"workload": WORKLOAD, "tokens_per_step_per_gpu": tokens},
-        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"each step one unit of every part (a map row, a THD row, one embedding "
-                                   f"sequence, one squeeze bin); {args.steps} steps in {wall:.1f} s; per-part "
-                                   f"rates combined over one whole step"},
+        "config": step_config(tokens_by_part, alg, dist.world),
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -1437,8 +1508,8 @@ def run_reference(args, dist: Dist):
 
 def profile_calls(args):
     """The workload for a per-kernel profiler capture: two rounds of every
-    configuration's ABI call and the scaled squeeze, then six of each
-    next-row call.  Nothing is timed."""
+    configuration's ABI call, the scaled squeeze and the ragged embedding
+    batch, then six of each next-row call.  Nothing is timed."""
     import torch
 
     dev = torch.device("cuda", 0)
@@ -1448,9 +1519,10 @@ def profile_calls(args):
     build.build()
     host = make_inputs(args.seed)
     host["squeeze_scaled"] = synth.squeeze(args.seed, N=16384)
+    host["thd_emb_ragged"] = synth.thd_embeddings_ragged(args.seed)
     stream = torch.cuda.Stream(dev)
     step = NativeStep(host, dev, stream)
-    scaled = NativeStep(host, dev, stream, host_pinned=step.pinned, only=("squeeze_scaled",))
+    scaled = NativeStep(host, dev, stream, host_pinned=step.pinned, only=("squeeze_scaled", "thd_emb_ragged"))
     with torch.cuda.stream(stream):
         for _ in range(2):
             for s in (step, scaled):

@@ -52,6 +52,35 @@ def test_reference_arm_under_torchrun_two_ranks():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert "whole steps" in line["cpu_baseline"]["sample"] and "rank 0 of 2" in line["cpu_baseline"]["sample"]
+    cfg = line["config"]
+    assert set(cfg) == {"workload", "tokens_per_step_per_gpu", "parts_tokens", "algorithmic_bytes_per_step", "l2",
+                        "parallelism"}
+    assert cfg["tokens_per_step_per_gpu"] == sum(cfg["parts_tokens"].values())
+    assert cfg["parallelism"].startswith("replicas x2")
+
+
+def test_algorithmic_bytes_per_part():
+    """The byte counts both arms put in ``config``, on hand-sized parts."""
+    import numpy as np
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    # a [2, 3] map with 4 segments: read 24 bytes, write 5 boundaries
+    assert bench.part_bytes("map_small", np.zeros((2, 3), np.int32), 4, 6) == 24 + 20
+    # ids/labels/one position plane, 3 kept sequences, T = 10, a [2, 2] length table
+    thd = {"seq_lens": np.zeros((2, 2), np.int64)}
+    assert bench.part_bytes("thd_small", thd, 3, 10) == 3 * 2 * 10 * 8 + 10 + 8 * 4 + 2 * 8 * 4
+    # mRoPE counts three planes of positions
+    assert bench.part_bytes("thd_ids", thd, 3, 10) == 5 * 2 * 10 * 8 + 10 + 8 * 4 + 2 * 8 * 4
+    # bf16 rows of 6: two copies of T rows of 12 bytes
+    emb = {"seq_lens": np.zeros((2, 2), np.int64), "hidden": np.zeros((2, 5, 6), np.int16)}
+    assert bench.part_bytes("thd_emb", emb, 3, 10) == 2 * 10 * 6 * 2 + 10 + 8 * 4 + 2 * 8 * 4
+    # two bins of width 8, members of 3 and 5 real tokens: read the real tokens,
+    # write every slot (8 bytes) and its mask byte, and both cu arrays
+    sq = {"bin_offsets": np.array([0, 1, 2]), "real_lens": np.array([3, 5]), "width": 8}
+    assert bench.part_bytes("squeeze", sq, 2, 0) == 8 * 8 + 9 * 2 * 8 + 8 * 4
 
 
 def test_native_arm_refuses_multi_gpu_without_torchrun():
