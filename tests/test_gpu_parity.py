@@ -597,6 +597,67 @@ def test_squeeze_wide_windows():
     check_squeeze(d, d["multiple"], d["capacity"], False, d["capacity"] + 8, pad_value=7)
 
 
+def bulk_problem(rng, dtype, multiple, width, out_bytes, W=1024):
+    """Bins filled greedily from sources of uniform random length (odd and
+    zero lengths included) until the output reaches out_bytes."""
+    eb = np.dtype(dtype).itemsize
+    nb = -(-out_bytes // (width * eb))
+    real, bins, n = [], [], 0
+    for _ in range(nb):
+        members, used = [], 0
+        while True:
+            r = int(rng.integers(0, W + 1))
+            p = -(-r // multiple) * multiple
+            if used + p > width - int(rng.integers(0, 3 * multiple)):
+                break
+            members.append(n)
+            real.append(r)
+            used += p
+            n += 1
+        if not members:  # a bin is never empty
+            members.append(n)
+            real.append(0)
+            n += 1
+        bins.append(members)
+    offs, mem = oracle.bins_to_csr(bins)
+    info = np.iinfo(dtype)
+    src = rng.integers(max(info.min, -30000), min(info.max, 30000), size=(n, W)).astype(dtype)
+    return {"src": src, "real_lens": np.asarray(real, np.int64), "bin_offsets": offs, "bin_members": mem,
+            "bins": bins}
+
+
+@pytest.mark.parametrize("dtype,multiple", [(np.int8, 16), (np.int16, 32), (np.int32, 16), (np.int64, 64)])
+def test_squeeze_large_outputs(dtype, multiple):
+    """Outputs of 32 MB and more on 16-byte boundaries (the 16-byte vector
+    path at its widest grids): runs that end inside 16 bytes, zero lengths,
+    hundreds to thousands of bins, stretched and trainer-style rows."""
+    eb = np.dtype(dtype).itemsize
+    rng = np.random.default_rng(300 + eb)
+    width = 16384
+    prob = bulk_problem(rng, dtype, multiple, width, 33 << 20)
+    check_squeeze(prob, multiple, width, True, width, pad_value=-7)
+    check_squeeze(prob, multiple, width + 4096, False, width, pad_value=5)
+
+
+def test_squeeze_large_output_without_mask_and_errors():
+    v = V()
+    rng = np.random.default_rng(31)
+    prob = bulk_problem(rng, np.int64, 64, 32768, 40 << 20)
+    src, real = dev(prob["src"]), dev(prob["real_lens"])
+    bins = (dev(prob["bin_offsets"]), dev(prob["bin_members"]))
+    r = v.pack_squeeze(src, real, bins, 64, 32768, True, 32768, 3, want_mask=False)
+    assert r["padding_mask"] is None and info_of(r["info"])[0] == 0
+    ref = oracle.pack_squeeze(prob["src"], prob["real_lens"], prob["bin_offsets"], prob["bin_members"], 64, 32768,
+                              True, 32768, 3)
+    np.testing.assert_array_equal(r["packed"].cpu().numpy(), ref["packed"])
+    # a bin over capacity and a member out of range are reported, not copied
+    assert check_squeeze(prob, 64, 16384, False, 32768) is None
+    bad = dict(prob)
+    bad["bin_members"] = prob["bin_members"].copy()
+    bad["bin_members"][5] = len(prob["real_lens"]) + 3
+    assert check_squeeze(bad, 64, 32768, True, 32768) is None
+
+
 def test_squeeze_scaled_workload():
     c = synth.squeeze(0, N=16384)
     check_squeeze(c, c["multiple"], c["capacity"], c["stretch"], c["width"], c["pad_value"])

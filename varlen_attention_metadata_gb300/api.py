@@ -295,11 +295,13 @@ def _bins_csr(bins, dev):
 
 
 def pack_squeeze(src: torch.Tensor, real_lens: torch.Tensor, bins, multiple: int, capacity: int,
-                 stretch_to_capacity: bool, width: int | None, pad_value: int = 0, with_output: bool = True):
+                 stretch_to_capacity: bool, width: int | None, pad_value: int = 0, with_output: bool = True,
+                 want_mask: bool = True):
     """Enqueue the squeeze.  ``bins`` is a list of lists of row indices or a
     ``(bin_offsets, bin_members)`` pair of int32 CUDA tensors.  With
-    ``with_output`` false only the metadata is produced.  Returns a dict of
-    device tensors and the info block."""
+    ``with_output`` false only the metadata is produced; with ``want_mask``
+    false the packed rows are produced without the padding mask.  Returns a
+    dict of device tensors and the info block."""
     lib = _lib.load()
     _require_cuda("src", src)
     dev = src.device
@@ -311,7 +313,7 @@ def pack_squeeze(src: torch.Tensor, real_lens: torch.Tensor, bins, multiple: int
     if width is None:
         width = 0
     out = torch.empty((num_bins, width), dtype=src.dtype, device=dev) if with_output else None
-    mask = torch.empty((num_bins, width), dtype=torch.bool, device=dev) if with_output else None
+    mask = torch.empty((num_bins, width), dtype=torch.bool, device=dev) if with_output and want_mask else None
     cu = torch.empty(M + num_bins + 1, dtype=torch.int32, device=dev)
     cup = torch.empty(M + num_bins + 1, dtype=torch.int32, device=dev)
     info = _new_info(dev)

@@ -279,8 +279,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int64_t tile_base = (int64_t)tile * (THREADS * kItems);
   const int64_t t0 = tile_base + (int64_t)tid * kItems;
 
-  // ---- this thread's 16 tokens and the token to their left
+  // ---- this thread's 16 tokens and the token to their left (the previous
+  // lane's last token; lane 0 loads its own)
   Items<Id> it;
+  const Id left0 = (lane == 0 && t0 > 0 && t0 < N) ? __ldg(doc + t0 - 1) : Id(0);
   if (kVector && t0 + kItems <= N) {
     const int4* p = reinterpret_cast<const int4*>(doc + t0);
 #pragma unroll
@@ -289,7 +291,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
     for (int k = 0; k < kItems; ++k) it.v[k] = (t0 + k < N) ? __ldg(doc + t0 + k) : Id(0);
   }
-  const Id left = (t0 > 0 && t0 < N) ? __ldg(doc + t0 - 1) : Id(0);
+  Id left = __shfl_up_sync(~0u, it.v[kItems - 1], 1);
+  if (lane == 0) left = left0;
 
   // ---- boundary flags, one bit per token: a different index than the left
   // token, or a row start (the first at (S - t0 % S) % S, then every S).
