@@ -154,7 +154,7 @@ def step_config(tokens: dict, alg_bytes: dict, world: int) -> dict:
     return {
         "workload": WORKLOAD,
         "tokens_per_step_per_gpu": int(sum(tokens.values())),
-        "parts_tokens": {k: int(v) for k, v in tokens.items()},
+        "parts_tokens": {k: int(tokens[k]) for k in sorted(tokens)},
         "algorithmic_bytes_per_step": int(sum(alg_bytes.values())),
         "l2": L2_NOTE,
         "parallelism": f"replicas x{world} (independent batches per GPU)",
