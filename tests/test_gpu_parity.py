@@ -639,6 +639,16 @@ def test_squeeze_large_outputs(dtype, multiple):
     check_squeeze(prob, multiple, width + 4096, False, width, pad_value=5)
 
 
+def test_squeeze_many_windows_unaligned():
+    """An odd row pitch (element-wise path) over 700 bins: 2100 window CTAs,
+    several waves of them."""
+    rng = np.random.default_rng(123)
+    m, width = 8, 8002
+    prob = bulk_problem(rng, np.int64, m, width, 700 * width * 8, W=301)
+    check_squeeze(prob, m, width, True, width, pad_value=-9)
+    check_squeeze(prob, m, width + 100, False, width, pad_value=4)
+
+
 def test_squeeze_large_output_without_mask_and_errors():
     v = V()
     rng = np.random.default_rng(31)
