@@ -35,12 +35,13 @@
 // the look-back and the workspace.
 //
 // The last tile, which holds the whole map's summary once its look-back
-// ends, writes cu_seqlens[num_segments] and the info block itself.  Each tile
-// counts itself done (with any failure it met) in one 64-bit word; warp 1
-// issues that add while the other warps store, so its round trip is off the
-// critical path.  In the CTA whose add completes the count, warp 1 reports a
-// failure, if any, and clears the summary words, so the workspace is zero
-// again for the next call and no tile summary is read back at the end.
+// ends, writes cu_seqlens[num_segments] and the info block itself.  Every
+// other tile counts itself done (with any failure it met) in one 64-bit word
+// with a release add that returns nothing, so no CTA waits for that round
+// trip.  In the last tile, warp 1 waits for the count after its stores,
+// then reports a failure, if any, and clears the summary words,
+// so the workspace is zero again for the next call and no tile summary is
+// read back at the end.
 #include <mutex>
 
 #include "common.cuh"
@@ -124,6 +125,10 @@ __device__ __forceinline__ Bounds from_words(unsigned long long a, unsigned long
 // the tile that completes the count resets the word to zero.
 constexpr int kTimeoutShift = 20, kBadShift = 40;
 constexpr unsigned long long kCountMask = (1ull << 20) - 1;
+// The last tile's wait for every other tile to count itself done.  Every
+// other tile's own waits end within the wait limit (at most 1 s), so this
+// bound is only reached after a device fault.
+constexpr int64_t kArrivalWaitNs = 2000000000;
 
 struct Header {
   unsigned long long state;
@@ -270,7 +275,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int kWarps = THREADS / 32;
   __shared__ Bounds s_warp[kWarps];
   __shared__ Bounds s_prefix;
-  __shared__ unsigned long long s_fail;  // this tile's failures, in the header word's layout
+  __shared__ unsigned long long s_fail;    // this tile's failures, in the header word's layout
   __shared__ unsigned short s_pos[(THREADS * kItems)];
 
   pdl_enter();
@@ -408,32 +413,39 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     return;
   }
-  // Warp 1 counts the tile done (with its failures): after the barrier,
-  // every read and write of the summaries by this tile has happened, and the
-  // add's round trip overlaps the stores.  The CTA whose add completes the
-  // count clears the workspace with warp 1 alone; every look-back has ended
-  // by then.
-  unsigned long long old = 0, add = 0;
-  if (tid == 32) {
-    add = 1ull | s_fail;
-    old = add_acq_rel_u64(&ws.hdr->state, add);
-  }
+  // Every tile but the last counts itself done (with its failures) with a
+  // release add that returns nothing: after the barrier, every read and
+  // write of the summaries by this tile has happened, and nobody waits for
+  // the round trip.
+  const bool last_tile = tile == tiles - 1;
+  if (!last_tile && tid == 32) red_release_add_u64(&ws.hdr->state, 1ull | s_fail);
   const int base = s_prefix.count;
   if (base >= 0 && base <= N - tile_sum.count)  // else counted as a bad workspace above
     for (int i = tid; i < tile_sum.count; i += THREADS) cu[base + i] = (int32_t)(tile_base + s_pos[i]);
-  if (warp != 1) return;
-  old = __shfl_sync(~0u, old, 0);
-  if ((old & kCountMask) != (unsigned long long)(tiles - 1)) return;
+  if (!last_tile || warp != 1) return;
 
-  // ---- last CTA: report a failure, if any, and clear the workspace
+  // ---- last tile: once every other tile has counted itself done, report a
+  // failure, if any, and clear the workspace (warp 1, after its stores)
+  unsigned long long others = 0;
   if (lane == 0) {
-    const unsigned long long all = old + add;
-    const bool timeouts = ((all >> kTimeoutShift) & kCountMask) != 0;
+    others = ld_acquire_u64(&ws.hdr->state);
+    const uint64_t start = global_ns();
+    while ((others & kCountMask) < (unsigned long long)(tiles - 1) &&
+           (int64_t)(global_ns() - start) < kArrivalWaitNs)
+      others = ld_acquire_u64(&ws.hdr->state);
+  }
+  others = __shfl_sync(~0u, others, 0);
+  const unsigned long long all = others + s_fail;
+  const bool complete = (others & kCountMask) == (unsigned long long)(tiles - 1);
+  if (lane == 0) {
+    const bool timeouts = !complete || ((all >> kTimeoutShift) & kCountMask) != 0;
     const bool bad = ((all >> kBadShift) & kCountMask) != 0;
     if (timeouts || bad) *info = {bad ? PSEQ_ERR_ARG : PSEQ_ERR_TIMEOUT, 0, 0, N};
-    ws.hdr->state = 0;  // the next call starts after this grid completes
+    if (complete) ws.hdr->state = 0;  // the next call starts after this grid completes
   }
-  for (int i = lane; i < 2 * tiles; i += 32) ws.slots[(size_t)(i >> 1) * kSlotWords + (i & 1)] = 0ull;
+  // every look-back has ended: no tile reads a summary any more
+  if (complete)
+    for (int i = lane; i < 2 * tiles; i += 32) ws.slots[(size_t)(i >> 1) * kSlotWords + (i & 1)] = 0ull;
 }
 
 __global__ void empty_map_kernel(int32_t* cu, pseq_info* info) {
