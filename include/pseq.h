@@ -89,14 +89,19 @@ int64_t pseq_debug_wait_limit_ns(void);
  *   boundaries: cu_seqlens[0] = 0, cu_seqlens[num_segments] = B*S.
  * info: count = num_segments, max_seqlen = longest segment (padding runs
  *   included; 0 when B*S == 0), total = B*S.
- * workspace: pseq_from_doc_ids_workspace_size(B, S) bytes, 16-byte aligned,
- *   ZERO-FILLED before its first use.  Every call that runs to completion
- *   leaves it zero-filled again, so one buffer serves any number of calls on
- *   one stream; calls that may overlap need separate workspaces.
+ * workspace: pseq_from_doc_ids_workspace_size(B, S) bytes or more, 16-byte
+ *   aligned, ZERO-FILLED before its first use.  Each call stamps what it
+ *   writes there with a number one above the previous call's (kept in the
+ *   buffer), so nothing a call leaves behind is read by the next: one buffer
+ *   serves any number of calls on one stream, of any map size it has room
+ *   for, also after a call that failed.  The call that takes the last
+ *   number (one call in 2^32 - 1) zero-fills all workspace_bytes and starts
+ *   the numbering again.  Calls that may overlap need separate workspaces.
  * Host errors: PSEQ_ERR_ARG (NULL, negative B or S, id_bytes, alignment,
  *   workspace), PSEQ_ERR_OVERFLOW (B*S > INT32_MAX).
  * Device errors: PSEQ_ERR_TIMEOUT (a tile's wait for its predecessor hit the
- *   cap set by pseq_debug_set_wait).
+ *   cap set by pseq_debug_set_wait); PSEQ_ERR_ARG (a workspace that was not
+ *   zero-filled before its first use, where that shows).
  * ---------------------------------------------------------------------- */
 size_t pseq_from_doc_ids_workspace_size(int64_t B, int64_t S);
 pseq_status pseq_from_doc_ids(const void* doc_ids, int32_t id_bytes, int64_t B,
@@ -113,8 +118,8 @@ pseq_status pseq_from_doc_ids(const void* doc_ids, int32_t id_bytes, int64_t B,
  * callback that is handed only input and output pointers, or a process that
  * has reserved all of HBM up front.  This entry point takes the same inputs
  * and outputs as pseq_from_doc_ids and no workspace.  Its scratch is a
- * static device array of about 16 KiB inside libpseq.so (a 128-byte header
- * and 16 bytes per 16384-token tile), which every GPU that loads the library
+ * static device array of about 32 KiB inside libpseq.so (a 128-byte header
+ * and 32 bytes per 16384-token tile), which every GPU that loads the library
  * holds until the process exits.
  *  - B*S must not exceed PSEQ_STATIC_MAX_TOKENS; larger maps get
  *    PSEQ_ERR_ARG before anything is enqueued (use pseq_from_doc_ids).

@@ -63,6 +63,21 @@ def test_doc_ids_scan_at_two_billion_tokens():
     del d, cu, c
 
 
+@pytest.mark.parametrize("B,S", [(2, 2**30 - 1), (3, 715_827_882)])
+def test_doc_ids_rows_at_the_widest(B, S):
+    """One document per row at the widest rows a map can have (B*S just
+    under 2^31): the boundaries are the row starts b*S, which the kernel
+    finds with a precomputed reciprocal of S."""
+    import varlen_attention_metadata_gb300 as v
+
+    assert B * S <= INT32_MAX
+    d = torch.full((B, S), 3, dtype=torch.int32, device=DEV)
+    cu, info = v.pseq_from_doc_ids(d)
+    assert info_of(info) == [0, B, S, B * S]
+    assert cu[: B + 1].tolist() == [b * S for b in range(B + 1)]
+    del d, cu
+
+
 def test_squeeze_with_the_most_bins():
     import varlen_attention_metadata_gb300 as v
 

@@ -156,11 +156,126 @@ def test_doc_ids_stress_map_workload(seed):
     check_doc_ids(synth.doc_map_stress(seed))
 
 
-def test_doc_ids_workspace_is_left_clean():
-    """Back-to-back calls of different sizes on one cached workspace."""
+def test_doc_ids_workspace_serves_any_sequence_of_calls():
+    """Back-to-back calls of different sizes on one cached workspace: slots
+    of an earlier, bigger map are never read as this call's."""
     rng = np.random.default_rng(3)
     for S in (50_000, 4096 * 5, 999, 120_000, 7):
         check_doc_ids(synth.random_doc_ids(rng, 3, S, "runs", np.int32))
+
+
+def row_start_widths():
+    widths = set(range(1, 40))
+    for k in range(5, 27):
+        widths |= {2**k - 1, 2**k, 2**k + 1}
+    return sorted(widths | {3 * 16384 + 5, 65535, 100_003, 1_000_003})
+
+
+@pytest.mark.parametrize("dtype", [torch.int32, torch.int64])
+def test_doc_ids_row_starts_at_every_width(dtype):
+    """One document filling every row: the boundaries are exactly the row
+    starts b*S, whatever the row width (the kernel finds them with a
+    precomputed reciprocal of S instead of a division).  At least three rows,
+    so the quotients reach 2; up to 2^26 tokens."""
+    v = V()
+    for S in row_start_widths():
+        B = max(3, min(4096, (1 << 26) // S))
+        x = torch.full((B, S), 5, dtype=dtype, device=DEV)
+        cu, info = v.pseq_from_doc_ids(x)
+        assert info_of(info) == (0, B, S, B * S), S
+        assert torch.equal(cu[: B + 1].to(torch.int64), torch.arange(0, B * S + 1, S, device=DEV)), S
+        del x, cu
+
+
+def test_doc_ids_random_at_widths_near_powers_of_two():
+    rng = np.random.default_rng(17)
+    for S in (15, 16, 17, 31, 33, 255, 257, 1023, 1025, 16383, 16384, 16385, 32767, 32769):
+        B = max(2, 120_000 // S)
+        check_doc_ids(synth.random_doc_ids(rng, B, S, "runs", np.int32))
+
+
+def raw_scan(d: np.ndarray, ws: torch.Tensor):
+    """pseq_from_doc_ids through the C ABI with the caller's workspace."""
+    import ctypes
+
+    v = V()
+    lib = v.load_library()
+    B, S = d.shape
+    x = dev(d)
+    cu = torch.empty(B * S + 1, dtype=torch.int32, device=DEV)
+    info = torch.zeros(32, dtype=torch.uint8, device=DEV)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = lib.pseq_from_doc_ids(P(x), x.element_size(), B, S, P(cu), P(info), P(ws), ws.numel(),
+                               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    return cu, info_of(info)
+
+
+def header_tag(ws: torch.Tensor) -> int:
+    """The workspace header's first word: the last call's tag (little-endian)."""
+    return int(ws[:8].cpu().numpy().view(np.uint64)[0])
+
+
+def check_raw(d, ws):
+    cu, (st, count, mx, total) = raw_scan(d, ws)
+    ref_cu, ref_mx = oracle.from_doc_ids(d)
+    assert (st, count, mx, total) == (0, len(ref_cu) - 1, ref_mx, d.size)
+    np.testing.assert_array_equal(cu[:count + 1].cpu().numpy(), ref_cu)
+
+
+@pytest.mark.parametrize("withheld", [None, 1])
+def test_doc_ids_tag_wraps_around(withheld):
+    """Each call stamps its slots with the header's tag plus one.  The call
+    that takes the last tag (2^32 - 1) zero-fills the whole buffer, slots of
+    earlier bigger maps included, and resets the header, also when one of
+    its tiles failed; the calls around it are exact."""
+    v = V()
+    lib = v.load_library()
+    rng = np.random.default_rng(21)
+    big = synth.random_doc_ids(rng, 6, 80_000, "runs", np.int32)    # 30 tiles
+    small = synth.random_doc_ids(rng, 3, 50_000, "runs", np.int32)  # 10 tiles
+    ws = torch.zeros(lib.pseq_from_doc_ids_workspace_size(*big.shape) + 1000, dtype=torch.uint8, device=DEV)
+    check_raw(big, ws)
+    assert header_tag(ws) == 1
+    check_raw(small, ws)
+    assert header_tag(ws) == 2
+    ws[:8] = torch.from_numpy(np.array([2**32 - 2], np.uint64).view(np.uint8)).to(DEV)
+    try:
+        if withheld is not None:
+            lib.pseq_debug_set_wait(1_000_000, withheld)
+        cu, info = raw_scan(small, ws)
+    finally:
+        lib.pseq_debug_set_wait(-1, -1)
+    if withheld is None:
+        ref_cu, ref_mx = oracle.from_doc_ids(small)
+        assert info == (0, len(ref_cu) - 1, ref_mx, small.size)
+        np.testing.assert_array_equal(cu[:info[1] + 1].cpu().numpy(), ref_cu)
+    else:
+        assert info[0] == v._lib.PSEQ_ERR_TIMEOUT
+    assert int(ws.count_nonzero()) == 0
+    check_raw(big, ws)
+    assert header_tag(ws) == 1
+
+
+@pytest.mark.parametrize("withheld", [0, 1, 4])
+def test_doc_ids_failed_call_leaves_workspace_usable(withheld):
+    """A tile that never publishes (the first, a middle one, the last of
+    five): the call reports PSEQ_ERR_TIMEOUT whichever tile waited in vain,
+    and the next call on the same buffer is exact."""
+    v = V()
+    lib = v.load_library()
+    rng = np.random.default_rng(22)
+    d = synth.random_doc_ids(rng, 4, 20_000, "runs", np.int32)  # 5 tiles
+    ws = torch.zeros(lib.pseq_from_doc_ids_workspace_size(*d.shape), dtype=torch.uint8, device=DEV)
+    check_raw(d, ws)
+    try:
+        lib.pseq_debug_set_wait(1_000_000, withheld)
+        _, info = raw_scan(d, ws)
+    finally:
+        lib.pseq_debug_set_wait(-1, -1)
+    assert info[0] == v._lib.PSEQ_ERR_TIMEOUT
+    check_raw(d, ws)
+    check_raw(synth.random_doc_ids(rng, 4, 20_000, "iid", np.int32), ws)
 
 
 def test_packed_seq_params_api():

@@ -84,8 +84,9 @@ class _WorkspaceCache:
     """One workspace buffer per (kind, device, stream), grown on demand.
 
     Kinds in ``ZEROED`` are zero-filled when allocated: those kernels need
-    a zeroed workspace and leave it zeroed after every call, so reuse on the
-    same stream needs no further clearing.  Each kind has its own buffer, so
+    a zeroed workspace at first use and leave it fit for the next call (the
+    scan's stamped slots, the others' counters back at zero), so reuse on
+    the same stream needs no further clearing.  Each kind has its own buffer, so
     one kernel's scratch never lands in another's.  Other kinds hold
     per-call scratch.
     """

@@ -79,6 +79,33 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+// The same on two adjacent words (16-byte aligned): each word is read or
+// written whole, the pair is not.
+__device__ __forceinline__ void ld_relaxed_v2_u64(const unsigned long long* p, unsigned long long& x,
+                                                  unsigned long long& y) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_v2_u64(unsigned long long* p, unsigned long long x, unsigned long long y) {
+  asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(x), "l"(y) : "memory");
+}
+// Four adjacent words (32-byte aligned) in one access of 256 bits; each word
+// is read or written whole, the four together are not.
+__device__ __forceinline__ void ld_relaxed_v4_u64(const unsigned long long* p, unsigned long long& x,
+                                                  unsigned long long& y, unsigned long long& z,
+                                                  unsigned long long& w) {
+  asm volatile("ld.relaxed.gpu.global.v4.u64 {%0, %1, %2, %3}, [%4];"
+               : "=l"(x), "=l"(y), "=l"(z), "=l"(w)
+               : "l"(p)
+               : "memory");
+}
+__device__ __forceinline__ void st_relaxed_v4_u64(unsigned long long* p, unsigned long long x, unsigned long long y,
+                                                  unsigned long long z, unsigned long long w) {
+  asm volatile("st.relaxed.gpu.global.v4.u64 [%0], {%1, %2, %3, %4};" ::"l"(p), "l"(x), "l"(y), "l"(z), "l"(w)
+               : "memory");
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 
 // Wrapping counter of finished CTAs (acq_rel): returns the old value; the
 // value after `limit` is 0, so the last of limit+1 arrivals leaves it zero.

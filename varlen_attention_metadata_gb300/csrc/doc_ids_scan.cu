@@ -7,41 +7,47 @@
 // longest segment.
 //
 // One pass over doc_ids.  CTA t takes tile t (16384 tokens: 1024 threads x
-// 16; a 2M-token map is 128 tiles, one per SM), flags the boundaries in it and summarises them as (count, first, last, largest inner
-// gap) -- an associative "followed by" operation -- with a block scan.  A
-// decoupled look-back over the preceding tiles then gives the tile its
-// exclusive prefix: the output index of its first boundary and the position
-// of the boundary before it, which closes the segment crossing into the
-// tile.  The gap term makes max_seqlen a by-product of the scan.
+// 16; a 2M-token map is 128 tiles, one per SM), flags the boundaries in it
+// and summarises them as (count, first, last, largest inner gap) -- an
+// associative "followed by" operation.  A decoupled look-back over the
+// preceding tiles then gives the tile its exclusive prefix: the output index
+// of its first boundary and the position of the boundary before it, which
+// closes the segment crossing into the tile.  The gap term makes max_seqlen
+// a by-product of the scan.
 //
-// A tile's summary is one 16-byte slot of two 64-bit words, published first
+// What the look-back waits for comes first: the tile's summary is a
+// reduction (per warp one ballot, two warp reductions and three shuffles,
+// then the same over the warps in warp 0), published at once.  Row starts
+// are found with a multiplication by a precomputed reciprocal of S, not a
+// division.  The running count each thread needs to place its boundaries is
+// a separate one-field scan, done while warp 0 looks back: every warp
+// compacts the tile's boundaries into shared memory as tile-relative 16-bit
+// positions, and after the look-back they are stored coalesced with the
+// prefix added.  A map that fits one tile skips the look-back and the
+// workspace.
+//
+// A tile's summary is one 32-byte slot of four 64-bit words, published first
 // as the tile's own aggregate and then overwritten with the inclusive prefix
-// (everything up to and including the tile).  Each word carries a published
-// bit and an inclusive bit, so one poll returns the summary itself; a poll
-// that catches the two words in different states (mid-overwrite) is simply
+// (everything up to and including the tile).  Each word carries the call's
+// tag and an inclusive bit, so one poll returns the summary itself; a poll
+// that catches the words in different states (mid-overwrite) is simply
 // repeated.  A look-back round polls 128 predecessors at once (four windows
 // of 32, one per lane), all loads in flight together, and joins each window
 // with one ballot, two warp reductions and three shuffles; a map of up to
-// 129 tiles needs one round.  (Four windows with these joins measured
-// faster than one or two on a 2M-token map; 896-thread tiles, which spread
-// that map over 147 SMs instead of 128, did not help.)  Waits are bounded by a time limit and report
+// 129 tiles needs one round.  Waits are bounded by a time limit and report
 // PSEQ_ERR_TIMEOUT.
 //
-// Warp 0 runs the block scan's second level and the look-back; the other
-// warps are released by a named barrier as soon as the block prefix is
-// known and compact the tile's boundaries into shared memory (tile-relative
-// 16-bit positions) while the look-back runs.  After it, the positions are
-// stored coalesced with the prefix added.  A map that fits one tile skips
-// the look-back and the workspace.
-//
-// The last tile, which holds the whole map's summary once its look-back
-// ends, writes cu_seqlens[num_segments] and the info block itself.  Every
-// other tile counts itself done (with any failure it met) in one 64-bit word
-// with a release add that returns nothing, so no CTA waits for that round
-// trip.  In the last tile, warp 1 waits for the count after its stores,
-// then reports a failure, if any, and clears the summary words,
-// so the workspace is zero again for the next call and no tile summary is
-// read back at the end.
+// The tag is one more than the previous call's, read from the workspace
+// header, so the slots a call leaves behind are never read as this call's
+// and nothing has to be cleared: the kernel ends when the last tile's
+// stores do.  The last tile, which holds the whole map's summary once its
+// look-back ends, writes cu_seqlens[num_segments] and the counts of the
+// info block, and advances the header.  Tile 0, which has no look-back,
+// writes the success status early and marks it written (a release off every
+// critical path); a tile whose wait ran out waits for that mark and then
+// overwrites the status.  The call that takes the last tag zero-fills the
+// whole buffer once every tile has counted itself done, and the numbering
+// starts again.
 #include <mutex>
 
 #include "common.cuh"
@@ -55,17 +61,13 @@ namespace {
 #ifndef PSEQ_SCAN_WINDOWS
 #define PSEQ_SCAN_WINDOWS 4
 #endif
-#ifndef PSEQ_SCAN_SLOT_BYTES
-#define PSEQ_SCAN_SLOT_BYTES 16
-#endif
 constexpr int kThreads = PSEQ_SCAN_THREADS;
 constexpr int kItems = 16;
 constexpr int kWindows = PSEQ_SCAN_WINDOWS;  // windows of 32 predecessors polled per look-back round
-constexpr int kSlotWords = PSEQ_SCAN_SLOT_BYTES / 8;
-constexpr int kTile = kThreads * kItems;  // tokens per tile
+constexpr int kSlotWords = 4;                // a tile's summary: count, last, first, gap
+constexpr int kTile = kThreads * kItems;     // tokens per tile
 static_assert(kTile <= 65536, "tile-relative positions are 16-bit");
 static_assert(kThreads % 32 == 0 && kThreads <= 1024, "whole warps, one CTA");
-static_assert(kSlotWords >= 2 && PSEQ_SCAN_SLOT_BYTES % 16 == 0, "a slot holds the two summary words");
 
 // Boundaries inside a span of tokens: how many, the first and last boundary
 // position, and the largest distance between consecutive boundaries.
@@ -86,70 +88,71 @@ __device__ __forceinline__ Bounds join(const Bounds& a, const Bounds& b) {
   return r;
 }
 
-__device__ __forceinline__ Bounds shfl_up(const Bounds& v, int d) {
-  return {__shfl_up_sync(~0u, v.count, d), __shfl_up_sync(~0u, v.first, d), __shfl_up_sync(~0u, v.last, d),
-          __shfl_up_sync(~0u, v.gap, d)};
-}
-
-__device__ __forceinline__ Bounds shfl(const Bounds& v, int src) {
-  return {__shfl_sync(~0u, v.count, src), __shfl_sync(~0u, v.first, src), __shfl_sync(~0u, v.last, src),
-          __shfl_sync(~0u, v.gap, src)};
-}
-
-// A summary as two self-validating words: {published, inclusive, count, last}
-// and {published, inclusive, gap, first}.  count and gap are below 2^31 and
-// take bits 31..61; positions are below 2^31 - 1 and take bits 0..30, with
-// all ones standing for "no boundary".
-constexpr unsigned long long kPublished = 1ull << 63;
-constexpr unsigned long long kInclusive = 1ull << 62;
+// A published summary is four 64-bit words, one per field.  Each carries the
+// tag of the call that wrote it (bits 32..63), whether it is an inclusive
+// prefix (bit 31) and the field (bits 0..30; a position of all ones stands
+// for "no boundary").  Tags run 1, 2, ..., 2^32 - 1 from the workspace
+// header; 0 never matches, so a zero-filled slot reads as unpublished.
+constexpr unsigned long long kInclusive = 1ull << 31;
 constexpr unsigned kNoPos = 0x7fffffffu;
+constexpr unsigned kLastTag = 0xffffffffu;
 
-__device__ __forceinline__ unsigned long long pos_bits(int p) { return p < 0 ? kNoPos : (unsigned)p; }
+__device__ __forceinline__ unsigned pos_bits(int p) { return p < 0 ? kNoPos : (unsigned)p; }
 __device__ __forceinline__ int pos_of(unsigned long long w) {
-  const unsigned v = (unsigned)(w & kNoPos);
+  const unsigned v = (unsigned)w & kNoPos;
   return v == kNoPos ? -1 : (int)v;
 }
-__device__ __forceinline__ unsigned long long word_a(const Bounds& b, bool incl) {
-  return kPublished | (incl ? kInclusive : 0ull) | ((unsigned long long)(unsigned)b.count << 31) | pos_bits(b.last);
+__device__ __forceinline__ unsigned long long tagged(unsigned tag, bool incl, unsigned v) {
+  return ((unsigned long long)tag << 32) | (incl ? kInclusive : 0ull) | v;
 }
-__device__ __forceinline__ unsigned long long word_b(const Bounds& b, bool incl) {
-  return kPublished | (incl ? kInclusive : 0ull) | ((unsigned long long)(unsigned)b.gap << 31) | pos_bits(b.first);
-}
-__device__ __forceinline__ Bounds from_words(unsigned long long a, unsigned long long b) {
-  return {(int)((a >> 31) & kNoPos), pos_of(b), pos_of(a), (int)((b >> 31) & kNoPos)};
+__device__ __forceinline__ void publish(unsigned long long* slot, const Bounds& b, bool incl, unsigned tag) {
+  st_relaxed_v4_u64(slot, tagged(tag, incl, (unsigned)b.count), tagged(tag, incl, pos_bits(b.last)),
+                    tagged(tag, incl, pos_bits(b.first)), tagged(tag, incl, (unsigned)b.gap));
 }
 
-// Header word: tiles done (bits 0..19), tiles whose wait hit its time limit
-// (bits 20..39), tiles that found a workspace that was not zero-filled
-// (bits 40..59).  A map has fewer than 2^18 tiles, so no field overflows;
-// the tile that completes the count resets the word to zero.
+// Header.  epoch: the tag of the last call (low 32 bits).  reported: the
+// tag of the call whose success status has been written (a tile that failed
+// writes its status after that).  state, used only by the call that takes
+// the last tag: tiles done (bits 0..19), tiles whose wait hit its time limit
+// (bits 20..39), tiles that found a workspace that was not zero-filled (bits
+// 40..59); a map has fewer than 2^18 tiles, so no field overflows.
 constexpr int kTimeoutShift = 20, kBadShift = 40;
 constexpr unsigned long long kCountMask = (1ull << 20) - 1;
-// The last tile's wait for every other tile to count itself done.  Every
-// other tile's own waits end within the wait limit (at most 1 s), so this
-// bound is only reached after a device fault.
+// A failed tile's wait for the success status to be written, or the last tile's wait for
+// every other tile to count itself done.  Every look-back wait ends within
+// the wait limit (at most 1 s), so this bound is only reached after a
+// device fault.
 constexpr int64_t kArrivalWaitNs = 2000000000;
 
 struct Header {
+  unsigned long long epoch;
+  unsigned long long reported;
   unsigned long long state;
-  unsigned long long pad[15];
+  unsigned long long pad[13];
 };
 static_assert(sizeof(Header) == 128, "header is 128 bytes");
 
 struct Workspace {
   Header* hdr;
-  unsigned long long* slots;  // [tiles][kSlotWords]: word a, word b, padding
+  unsigned long long* slots;  // [capacity][kSlotWords]
+  int64_t capacity;           // slots the caller's buffer holds
 };
 
-size_t workspace_bytes(int64_t tiles) { return sizeof(Header) + 8 * (size_t)kSlotWords * (size_t)tiles; }
+// The slots start at the first 32-byte boundary after the header (one
+// 256-bit access per slot); a 16-byte aligned buffer needs 16 bytes of slack.
+constexpr size_t kSlotBytes = 8 * kSlotWords;
+constexpr size_t workspace_bytes(int64_t tiles) { return sizeof(Header) + 16 + kSlotBytes * (size_t)tiles; }
 
-Workspace carve(void* base) {
-  unsigned char* p = static_cast<unsigned char*>(base);
-  return {reinterpret_cast<Header*>(p), reinterpret_cast<unsigned long long*>(p + sizeof(Header))};
+Workspace carve(void* base, size_t bytes) {
+  const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+  const uintptr_t s = (b + sizeof(Header) + kSlotBytes - 1) & ~(uintptr_t)(kSlotBytes - 1);
+  return {reinterpret_cast<Header*>(base), reinterpret_cast<unsigned long long*>(s),
+          (int64_t)((b + bytes - s) / kSlotBytes)};
 }
 
-// Named barrier 1: warp 0 arrives once the block prefix is in shared memory,
-// the other warps wait for it (barrier 0 stays with __syncthreads).
+// Named barrier 1: warp 0 arrives once the tile's output index and its
+// boundary positions are in shared memory; the other warps wait for it and
+// store (barrier 0 stays with __syncthreads).
 __device__ __forceinline__ void bar_arrive_1(int threads) { asm volatile("bar.arrive 1, %0;" ::"r"(threads) : "memory"); }
 __device__ __forceinline__ void bar_sync_1(int threads) { asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory"); }
 
@@ -159,46 +162,73 @@ union Items {
   Id v[kItems];
 };
 
-// Summary of one look-back window: lane L holds the summary of the L-th tile
-// back (higher lanes: earlier tiles); lanes with `use` false count as empty.
-// One ballot, two warp reductions and three shuffles, the same in every
-// lane.  The gap into a tile with boundaries is closed by the nearest
-// earlier tile with boundaries in the window (the one before the window is
-// handled when windows are joined).
-__device__ __forceinline__ Bounds window_sum(const Bounds& b, bool use) {
+// Summary of the 32 lanes' spans taken in lane order (lane 0 first), in
+// every lane: one ballot, two warp reductions (redux add and max) and three
+// shuffles.  The gap into a lane with boundaries is closed by the nearest
+// lower lane with boundaries.
+__device__ __forceinline__ Bounds lanes_sum(const Bounds& b) {
   const int lane = threadIdx.x & 31;
-  const int cnt = use ? b.count : 0;
-  const unsigned nz = __ballot_sync(~0u, cnt > 0);
+  const unsigned nz = __ballot_sync(~0u, b.count > 0);
   Bounds r = none();
-  r.count = (int)__reduce_add_sync(~0u, (unsigned)cnt);
-  const unsigned earlier = lane == 31 ? 0u : nz & (~0u << (lane + 1));
-  const int prev_last = __shfl_sync(~0u, b.last, earlier ? __ffs(earlier) - 1 : lane);
+  r.count = (int)__reduce_add_sync(~0u, (unsigned)b.count);
+  const unsigned earlier = nz & ((1u << lane) - 1u);
+  const int prev_last = __shfl_sync(~0u, b.last, earlier ? 31 - __clz(earlier) : lane);
   int g = 0;
-  if (cnt > 0) g = earlier ? max(b.gap, b.first - prev_last) : b.gap;
+  if (b.count > 0) g = earlier ? max(b.gap, b.first - prev_last) : b.gap;
   r.gap = (int)__reduce_max_sync(~0u, (unsigned)g);
   if (nz) {
-    r.last = __shfl_sync(~0u, b.last, __ffs(nz) - 1);
-    r.first = __shfl_sync(~0u, b.first, 31 - __clz(nz));
+    r.first = __shfl_sync(~0u, b.first, __ffs(nz) - 1);
+    r.last = __shfl_sync(~0u, b.last, 31 - __clz(nz));
   }
   return r;
 }
 
+// Division by an invariant divisor d < 2^31 for dividends n < 2^31: with
+// l = ceil(log2 d) and m = ceil(2^(31+l) / d), floor(n / d) =
+// floor(n * m / 2^(31+l)) (Granlund and Montgomery, "Division by invariant
+// integers using multiplication", 1994, Theorem 4.2 with N = 31), and
+// m < 2^32.
+struct DivBy {
+  unsigned d, m;
+  int shift;  // l - 1, or -1 for d == 1
+};
+
+DivBy div_by(unsigned d) {
+  int l = 0;
+  while ((1ull << l) < d) ++l;
+  if (l == 0) return {d, 0u, -1};
+  return {d, (unsigned)(((1ull << (31 + l)) + d - 1) / d), l - 1};
+}
+
+__device__ __forceinline__ unsigned mod_by(unsigned n, DivBy v) {
+  const unsigned q = v.shift < 0 ? n : (__umulhi(n, v.m) >> v.shift);
+  return n - q * v.d;
+}
+
 // Joins the summaries of tiles j, j-1, ... going back until one of them is an
-// inclusive prefix; returns the summary of everything before tile j + 1.
+// inclusive prefix of this call (tag); returns the summary of everything
+// before tile j + 1.  The boundary count of that span is known before its
+// other fields and goes to on_count(count) first (every lane calls it once).
 // Warp-wide; `gave_up` is set in every lane when a wait ran out.
-__device__ __forceinline__ Bounds look_back(const unsigned long long* slots, int j, int64_t wait_ns, bool& gave_up) {
+template <typename OnCount>
+__device__ __forceinline__ Bounds look_back(const unsigned long long* slots, int j, unsigned tag, int64_t wait_ns,
+                                            bool& gave_up, OnCount&& on_count) {
   const int lane = threadIdx.x & 31;
   Bounds run = none();  // summary of the tiles between the polled span and tile j + 1
   gave_up = false;
+  // the words of an empty inclusive prefix: what lies before tile 0, and what
+  // a wait that ran out stands in for
+  const unsigned long long e_count = tagged(tag, true, 0u), e_pos = tagged(tag, true, kNoPos);
   while (true) {
-    // lane L of window w looks at tile j - 32w - L
-    Bounds b[kWindows];
-    bool incl[kWindows], done[kWindows];
+    // lane L of window w looks at tile j - 32w - L; the raw words stay live
+    // while polling and are decoded once every window is in
+    unsigned long long w0[kWindows], w1[kWindows], w2[kWindows], w3[kWindows];
+    bool done[kWindows];
 #pragma unroll
     for (int w = 0; w < kWindows; ++w) {
-      b[w] = none();
-      incl[w] = true;  // before tile 0: an empty inclusive prefix
       done[w] = j - 32 * w - lane < 0;
+      w0[w] = w3[w] = e_count;
+      w1[w] = w2[w] = e_pos;
     }
     int polls = 0;
     uint64_t start = 0;
@@ -206,28 +236,21 @@ __device__ __forceinline__ Bounds look_back(const unsigned long long* slots, int
     while (true) {
       // every window's loads are issued before any is looked at, so a round
       // costs one L2 round trip however many windows are open
-      unsigned long long wa[kWindows], wb[kWindows];
 #pragma unroll
-      for (int w = 0; w < kWindows; ++w) {
-        wa[w] = wb[w] = 0ull;
+      for (int w = 0; w < kWindows; ++w)
         if (!done[w]) {
           const unsigned long long* sl = slots + (size_t)(j - 32 * w - lane) * kSlotWords;
-          wa[w] = ld_relaxed_u64(sl);
-          wb[w] = ld_relaxed_u64(sl + 1);
+          ld_relaxed_v4_u64(sl, w0[w], w1[w], w2[w], w3[w]);
         }
-      }
       bool all_done = true;
 #pragma unroll
       for (int w = 0; w < kWindows; ++w) {
         if (done[w]) continue;
-        // both words published and in the same state; otherwise poll again
-        if ((wa[w] & wb[w] & kPublished) && !((wa[w] ^ wb[w]) & kInclusive)) {
-          b[w] = from_words(wa[w], wb[w]);
-          incl[w] = (wa[w] & kInclusive) != 0;
-          done[w] = true;
-        } else {
-          all_done = false;
-        }
+        // all four words written by this call and in the same state;
+        // otherwise poll again
+        const unsigned long long a = w0[w] & w1[w] & w2[w] & w3[w], o = w0[w] | w1[w] | w2[w] | w3[w];
+        done[w] = (unsigned)(a >> 32) == tag && (unsigned)(o >> 32) == tag && !((a ^ o) & kInclusive);
+        all_done = all_done && done[w];
       }
       if (__all_sync(~0u, all_done)) break;
       if (polls++ == 0) {
@@ -237,12 +260,18 @@ __device__ __forceinline__ Bounds look_back(const unsigned long long* slots, int
 #pragma unroll
         for (int w = 0; w < kWindows; ++w)
           if (!done[w]) {
-            b[w] = none();
-            incl[w] = true;
-            done[w] = true;
+            w0[w] = w3[w] = e_count;
+            w1[w] = w2[w] = e_pos;
           }
         break;
       }
+    }
+    Bounds b[kWindows];
+    bool incl[kWindows];
+#pragma unroll
+    for (int w = 0; w < kWindows; ++w) {
+      b[w] = {(int)((unsigned)w0[w] & kNoPos), pos_of(w2[w]), pos_of(w1[w]), (int)((unsigned)w3[w] & kNoPos)};
+      incl[w] = (w0[w] & kInclusive) != 0;
     }
     if (__any_sync(~0u, timed_out)) gave_up = true;
     // nearest inclusive summary: lowest window, then lowest lane
@@ -255,12 +284,47 @@ __device__ __forceinline__ Bounds look_back(const unsigned long long* slots, int
         stop_l = __ffs(m) - 1;
       }
     }
-    // Join the counted tiles, farthest window first; tiles past the inclusive
-    // one count as empty.
+    // The span from the inclusive tile (or the farthest polled one) up to tile
+    // j, in one pass over all windows: tiles past the inclusive one count as
+    // empty.  Each tile with boundaries closes the gap from the nearest
+    // earlier tile with boundaries: in its window the next lane up that has
+    // some, else the lowest such lane of the nearest earlier window.
+    int cnt[kWindows];
+    unsigned nz[kWindows];
+    int low_last[kWindows];  // last boundary of the window's nearest tile with boundaries
+#pragma unroll
+    for (int w = 0; w < kWindows; ++w) {
+      cnt[w] = (w < stop_w || (w == stop_w && lane <= stop_l)) ? b[w].count : 0;
+      nz[w] = __ballot_sync(~0u, cnt[w] > 0);
+    }
+    int sum = 0;
+#pragma unroll
+    for (int w = 0; w < kWindows; ++w) {
+      sum += cnt[w];
+      low_last[w] = __shfl_sync(~0u, b[w].last, nz[w] ? __ffs(nz[w]) - 1 : 0);
+    }
     Bounds span = none();
+    span.count = (int)__reduce_add_sync(~0u, (unsigned)sum);
+    if (stop_w < kWindows) on_count(span.count + run.count);
+    int g = 0, carry = -1;  // carry: last boundary before window w, within the span
+#pragma unroll
+    for (int w = kWindows - 1; w >= 0; --w) {
+      const unsigned up = lane == 31 ? 0u : nz[w] & (~0u << (lane + 1));
+      const int v = __shfl_sync(~0u, b[w].last, up ? __ffs(up) - 1 : lane);
+      const int prev = up ? v : carry;
+      if (cnt[w] > 0) g = max(g, prev >= 0 ? max(b[w].gap, b[w].first - prev) : b[w].gap);
+      if (nz[w]) carry = low_last[w];
+    }
+    span.gap = (int)__reduce_max_sync(~0u, (unsigned)g);
+    // first: the farthest tile with boundaries; last: the nearest
+#pragma unroll
+    for (int w = 0; w < kWindows; ++w) {
+      const int f = __shfl_sync(~0u, b[w].first, nz[w] ? 31 - __clz(nz[w]) : 0);
+      if (nz[w]) span.first = f;
+    }
 #pragma unroll
     for (int w = kWindows - 1; w >= 0; --w)
-      span = join(span, window_sum(b[w], w < stop_w || (w == stop_w && lane <= stop_l)));
+      if (nz[w]) span.last = low_last[w];
     run = join(span, run);
     if (stop_w < kWindows) return run;
     j -= 32 * kWindows;
@@ -269,13 +333,13 @@ __device__ __forceinline__ Bounds look_back(const unsigned long long* slots, int
 
 template <typename Id, bool kVector, int THREADS>
 __global__ void __launch_bounds__(THREADS, 1)
-    doc_ids_scan_kernel(const Id* __restrict__ doc, int N, int S, int32_t* __restrict__ cu,
+    doc_ids_scan_kernel(const Id* __restrict__ doc, int N, DivBy S, int32_t* __restrict__ cu,
                         pseq_info* __restrict__ info, Workspace ws, int tiles, int64_t wait_ns,
                         int withhold) {
   constexpr int kWarps = THREADS / 32;
+  static_assert(kWarps >= 2 && kWarps <= 32, "one lane per warp; warp 1 takes the last tile's tail");
   __shared__ Bounds s_warp[kWarps];
-  __shared__ Bounds s_prefix;
-  __shared__ unsigned long long s_fail;    // this tile's failures, in the header word's layout
+  __shared__ int s_base;  // the tile's first output index
   __shared__ unsigned short s_pos[(THREADS * kItems)];
 
   pdl_enter();
@@ -283,6 +347,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int tile = blockIdx.x;
   const int64_t tile_base = (int64_t)tile * (THREADS * kItems);
   const int64_t t0 = tile_base + (int64_t)tid * kItems;
+  // the previous call's tag (warp 0, which publishes and polls, and tile 0's
+  // warp 1, which writes the success status; the load's latency hides
+  // behind the token loads)
+  unsigned e0 = 0;
+  if ((warp == 0 || (warp == 1 && tile == 0)) && tiles > 1) e0 = (unsigned)ld_relaxed_u64(&ws.hdr->epoch);
 
   // ---- this thread's 16 tokens and the token to their left (the previous
   // lane's last token; lane 0 loads its own)
@@ -308,8 +377,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   unsigned flags = 0;
 #pragma unroll
   for (int k = 0; k < kItems; ++k) flags |= (unsigned)(it.v[k] != (k ? it.v[k - 1] : left)) << k;
-  for (unsigned q = ((unsigned)S - pos0 % (unsigned)S) % (unsigned)S; q < (unsigned)kItems; q += (unsigned)S)
-    flags |= 1u << q;
+  {
+    const unsigned r = mod_by(pos0, S);  // meaningless past the map (t0 >= N), where every flag is masked off
+    for (unsigned q = r ? S.d - r : 0u; q < (unsigned)kItems; q += S.d) flags |= 1u << q;
+  }
   flags &= live >= 32 ? ~0u : (1u << live) - 1u;
   Bounds mine = none();
   if (flags) {
@@ -324,108 +395,127 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
 
-  // ---- warp-level scan of the summaries (in token order)
-  Bounds inc = mine;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const Bounds o = shfl_up(inc, d);
-    if (lane >= d) inc = join(o, inc);
+  // ---- the tile's summary first, since the look-back waits for it: each
+  // warp's span, then (warp 0) the block's
+  {
+    const Bounds w = lanes_sum(mine);
+    if (lane == 0) s_warp[warp] = w;
   }
-  if (lane == 31) s_warp[warp] = inc;
   __syncthreads();
-  Bounds before_me = shfl_up(inc, 1);
-  if (lane == 0) before_me = none();
 
-  // Tile-relative boundary positions, in order, from the thread's index of
-  // its first boundary within the tile.
-  auto compact = [&](int li) {
+  // Tile-relative boundary positions, in token order: this thread's first
+  // goes after the boundaries of the warps before it and of the lanes
+  // before it.
+  auto compact = [&]() {
+    int li = (int)__reduce_add_sync(~0u, (unsigned)(lane < warp ? s_warp[lane].count : 0));
+    int c = mine.count;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(~0u, c, d);
+      if (lane >= d) c += o;
+    }
+    li += c - mine.count;
     for (unsigned m = flags; m; m &= m - 1) s_pos[li++] = (unsigned short)(t0 - tile_base + __ffs(m) - 1);
   };
 
-  static_assert(THREADS >= 64, "warp 1 counts the tile done");
-  bool timed_out = withhold == tile;  // (warp 0) a withheld summary is reported as a failed wait
-  bool bad_ws = false;                // (thread 0)
-  Bounds tile_sum;
-  if (warp == 0) {
-    // second level of the block scan: warp totals -> inclusive warp prefixes
-    Bounds w = lane < kWarps ? s_warp[lane] : none();
-#pragma unroll
-    for (int d = 1; d < kWarps; d <<= 1) {
-      const Bounds o = shfl_up(w, d);
-      if (lane >= d) w = join(o, w);
+  const bool last_tile = tile == tiles - 1;
+  if (warp != 0) {
+    if (tiles > 1 && tile == 0 && tid == 32) {
+      // the success status, before any tile can have failed (a failure
+      // takes a wait that ran out, or a look-back; tile 0 has none); a tile
+      // that failed sees `reported` and then overwrites it
+      const unsigned tag = e0 < kLastTag ? e0 + 1 : 1u;
+      info->status = PSEQ_OK;
+      st_release_u64(&ws.hdr->reported, tag);
     }
-    if (lane < kWarps) s_warp[lane] = w;
-    tile_sum = shfl(w, kWarps - 1);
-    bar_arrive_1(THREADS);  // the other warps may compact now
-    Bounds prefix = none();
-    if (tiles > 1) {
-      unsigned long long* mine_slot = ws.slots + (size_t)tile * kSlotWords;
-      // publish at once; tile 0's own summary is already its inclusive prefix
-      if (lane == 0 && withhold != tile) {
-        st_relaxed_u64(mine_slot, word_a(tile_sum, tile == 0));
-        st_relaxed_u64(mine_slot + 1, word_b(tile_sum, tile == 0));
-      }
-      compact(before_me.count);  // warp 0's own boundaries (block prefix: none)
-      if (tile > 0) {
-        bool gave_up;
-        prefix = look_back(ws.slots, tile - 1, wait_ns, gave_up);
-        if (gave_up) timed_out = true;
-      }
-      if (lane == 0) {
-        const Bounds all = join(prefix, tile_sum);
-        if (tile > 0 && withhold != tile) {
-          st_relaxed_u64(mine_slot, word_a(all, true));
-          st_relaxed_u64(mine_slot + 1, word_b(all, true));
-        }
-        if (tile == tiles - 1 && !timed_out) {
-          // the whole map: close the array and report (a failure elsewhere
-          // overwrites the report at the end)
-          if (all.count >= 1 && all.count <= N) {
-            cu[all.count] = N;
-            *info = {PSEQ_OK, all.count, max(all.gap, N - all.last), N};
-          } else {
-            bad_ws = true;
-          }
-        }
-        // a prefix that does not fit only comes from a workspace that was
-        // not zero-filled
-        if (prefix.count > N - tile_sum.count) bad_ws = true;
-        s_fail = ((unsigned long long)timed_out << kTimeoutShift) | ((unsigned long long)bad_ws << kBadShift);
-      }
-    } else {
-      compact(before_me.count);
-    }
-    if (lane == 0) s_prefix = prefix;
-  } else {
+    const int tile_count = (int)__reduce_add_sync(~0u, (unsigned)(lane < kWarps ? s_warp[lane].count : 0));
+    compact();
+    // ---- once warp 0 has the tile's output index: its boundary positions
     bar_sync_1(THREADS);
-    before_me = join(s_warp[warp - 1], before_me);
-    tile_sum = s_warp[kWarps - 1];
-    compact(before_me.count);
+    const int base = s_base;
+    if (base >= 0 && base <= N - tile_count)  // else reported as a bad workspace
+      for (int i = tid - 32; i < tile_count; i += THREADS - 32) cu[base + i] = (int32_t)(tile_base + s_pos[i]);
+    return;
   }
-  __syncthreads();
 
-  // ---- store this tile's boundary positions at the prefix
+  // ---- warp 0: the tile's summary, the look-back and the reports
+  const Bounds tile_sum = lanes_sum(lane < kWarps ? s_warp[lane] : none());
+  // hands the tile's output index to the other warps, which store
+  auto release_stores = [&](int base) {
+    if (lane == 0) s_base = base;
+    __syncwarp();
+    bar_arrive_1(THREADS);
+  };
   if (tiles == 1) {
-    for (int i = tid; i < tile_sum.count; i += THREADS) cu[i] = (int32_t)s_pos[i];
-    if (tid == 0) {
+    compact();
+    release_stores(0);
+    if (lane == 0) {
       cu[tile_sum.count] = N;
       *info = {PSEQ_OK, tile_sum.count, max(tile_sum.gap, N - tile_sum.last), N};
     }
     return;
   }
-  // Every tile but the last counts itself done (with its failures) with a
-  // release add that returns nothing: after the barrier, every read and
-  // write of the summaries by this tile has happened, and nobody waits for
-  // the round trip.
-  const bool last_tile = tile == tiles - 1;
-  if (!last_tile && tid == 32) red_release_add_u64(&ws.hdr->state, 1ull | s_fail);
-  const int base = s_prefix.count;
-  if (base >= 0 && base <= N - tile_sum.count)  // else counted as a bad workspace above
-    for (int i = tid; i < tile_sum.count; i += THREADS) cu[base + i] = (int32_t)(tile_base + s_pos[i]);
-  if (!last_tile || warp != 1) return;
+  const unsigned tag = e0 < kLastTag ? e0 + 1 : 1u;
+  unsigned long long* mine_slot = ws.slots + (size_t)tile * kSlotWords;
+  // publish at once; tile 0's own summary is already its inclusive prefix
+  if (lane == 0 && withhold != tile) publish(mine_slot, tile_sum, tile == 0, tag);
+  compact();  // warp 0's own boundaries
+  bool timed_out = withhold == tile;  // a withheld summary is reported as a failed wait
+  Bounds prefix = none();
+  if (tile > 0) {
+    bool gave_up;
+    prefix = look_back(ws.slots, tile - 1, tag, wait_ns, gave_up, release_stores);
+    if (gave_up) timed_out = true;
+  } else {
+    release_stores(0);
+  }
+  // a prefix that does not fit only comes from a workspace that was not
+  // zero-filled before its first use
+  bool bad_ws = prefix.count > N - tile_sum.count;
+  if (lane == 0) {
+    const Bounds all = join(prefix, tile_sum);
+    if (!last_tile) {
+      if (tile > 0 && withhold != tile) publish(mine_slot, all, true, tag);
+    } else {
+      // the whole map: close the array and report (tile 0 writes the
+      // status).  Every tile read the header before publishing, and this
+      // look-back ended only after every tile had published: the header may
+      // take this call's tag.
+      if (all.count < 1 || all.count > N) bad_ws = true;
+      if (!timed_out && !bad_ws) {
+        cu[all.count] = N;
+        info->count = all.count;
+        info->max_seqlen = max(all.gap, N - all.last);
+        info->total = N;
+      }
+      if (tag != kLastTag) st_relaxed_u64(&ws.hdr->epoch, tag);
+    }
+  }
+  bad_ws = __shfl_sync(~0u, bad_ws, 0);
+  const unsigned long long fail =
+      ((unsigned long long)timed_out << kTimeoutShift) | ((unsigned long long)bad_ws << kBadShift);
 
-  // ---- last tile: once every other tile has counted itself done, report a
-  // failure, if any, and clear the workspace (warp 1, after its stores)
+  // A tile that failed writes its status once the success status is out.
+  auto report_failure = [&](bool bad) {
+    const uint64_t start = global_ns();
+    while ((unsigned)ld_acquire_u64(&ws.hdr->reported) != tag && (int64_t)(global_ns() - start) < kArrivalWaitNs) {
+    }
+    *info = {bad ? PSEQ_ERR_ARG : PSEQ_ERR_TIMEOUT, 0, 0, N};
+  };
+  if (tag != kLastTag) {
+    if (lane == 0 && fail) report_failure(bad_ws);
+    return;
+  }
+
+  // ---- the call with the last tag (one in 2^32 - 1): every tile counts
+  // itself done once it reads no summary any more; the last tile, once all
+  // have, reports their failures, zero-fills every slot of the buffer and
+  // resets the header, so the next call starts the tags again at 1 and no
+  // stale slot can carry them
+  if (!last_tile) {
+    if (lane == 0) red_release_add_u64(&ws.hdr->state, 1ull | fail);
+    return;
+  }
   unsigned long long others = 0;
   if (lane == 0) {
     others = ld_acquire_u64(&ws.hdr->state);
@@ -434,18 +524,21 @@ __global__ void __launch_bounds__(THREADS, 1)
            (int64_t)(global_ns() - start) < kArrivalWaitNs)
       others = ld_acquire_u64(&ws.hdr->state);
   }
-  others = __shfl_sync(~0u, others, 0);
-  const unsigned long long all = others + s_fail;
+  others = __shfl_sync(~0u, others, 0) + fail;
   const bool complete = (others & kCountMask) == (unsigned long long)(tiles - 1);
   if (lane == 0) {
-    const bool timeouts = !complete || ((all >> kTimeoutShift) & kCountMask) != 0;
-    const bool bad = ((all >> kBadShift) & kCountMask) != 0;
-    if (timeouts || bad) *info = {bad ? PSEQ_ERR_ARG : PSEQ_ERR_TIMEOUT, 0, 0, N};
-    if (complete) ws.hdr->state = 0;  // the next call starts after this grid completes
+    const bool timeouts = !complete || ((others >> kTimeoutShift) & kCountMask) != 0;
+    const bool bad = ((others >> kBadShift) & kCountMask) != 0;
+    if (timeouts || bad) report_failure(bad);
   }
-  // every look-back has ended: no tile reads a summary any more
-  if (complete)
-    for (int i = lane; i < 2 * tiles; i += 32) ws.slots[(size_t)(i >> 1) * kSlotWords + (i & 1)] = 0ull;
+  if (!complete) return;  // the header keeps the previous tag: the next call takes the last tag again
+  for (int64_t i = lane; i < ws.capacity * kSlotWords; i += 32) ws.slots[i] = 0ull;
+  __syncwarp();
+  if (lane == 0) {
+    ws.hdr->state = 0;
+    ws.hdr->reported = 0;
+    ws.hdr->epoch = 0;
+  }
 }
 
 __global__ void empty_map_kernel(int32_t* cu, pseq_info* info) {
@@ -464,14 +557,15 @@ cudaError_t launch_scan(const void* doc, int N, int S, int32_t* cu, pseq_info* i
   // would leave threads idle)
   constexpr int kSmall = 512;
   const bool small = tiles == 1 && N <= kSmall * kItems;
+  const DivBy Sd = div_by((unsigned)S);
   if (aligned(doc, 16))
-    return small ? launch_pdl(doc_ids_scan_kernel<Id, true, kSmall>, dim3(1), dim3(kSmall), 0, st, d, N, S, cu, info,
+    return small ? launch_pdl(doc_ids_scan_kernel<Id, true, kSmall>, dim3(1), dim3(kSmall), 0, st, d, N, Sd, cu, info,
                               ws, tiles, wait, withhold)
-                 : launch_pdl(doc_ids_scan_kernel<Id, true, kThreads>, dim3(tiles), dim3(kThreads), 0, st, d, N, S, cu,
+                 : launch_pdl(doc_ids_scan_kernel<Id, true, kThreads>, dim3(tiles), dim3(kThreads), 0, st, d, N, Sd, cu,
                               info, ws, tiles, wait, withhold);
-  return small ? launch_pdl(doc_ids_scan_kernel<Id, false, kSmall>, dim3(1), dim3(kSmall), 0, st, d, N, S, cu, info,
+  return small ? launch_pdl(doc_ids_scan_kernel<Id, false, kSmall>, dim3(1), dim3(kSmall), 0, st, d, N, Sd, cu, info,
                             ws, tiles, wait, withhold)
-               : launch_pdl(doc_ids_scan_kernel<Id, false, kThreads>, dim3(tiles), dim3(kThreads), 0, st, d, N, S, cu,
+               : launch_pdl(doc_ids_scan_kernel<Id, false, kThreads>, dim3(tiles), dim3(kThreads), 0, st, d, N, Sd, cu,
                             info, ws, tiles, wait, withhold);
 }
 
@@ -516,7 +610,7 @@ extern "C" pseq_status pseq_from_doc_ids(const void* doc_ids, int32_t id_bytes, 
   const size_t need = workspace_bytes(tiles);
   if (!workspace || ws_bytes < need || !aligned(workspace, 16))
     return fail(PSEQ_ERR_ARG, "pseq_from_doc_ids: workspace needs %zu bytes, 16-byte aligned (got %zu)", need, ws_bytes);
-  Workspace ws = carve(workspace);
+  Workspace ws = carve(workspace, ws_bytes);
   const cudaError_t e = id_bytes == 4
                             ? launch_scan<int32_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st)
                             : launch_scan<int64_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st);
@@ -540,7 +634,7 @@ namespace {
 
 constexpr int64_t kStaticMaxTokens = PSEQ_STATIC_MAX_TOKENS;  // B*S limit of the static scratch
 constexpr int64_t kStaticMaxTiles = (kStaticMaxTokens + kTile - 1) / kTile;  // a map at the limit fits
-constexpr size_t kStaticBytes = sizeof(Header) + 8 * (size_t)kSlotWords * (size_t)kStaticMaxTiles;
+constexpr size_t kStaticBytes = workspace_bytes(kStaticMaxTiles);  // a map at the limit, slack included
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
 
@@ -600,7 +694,7 @@ extern "C" pseq_status pseq_from_doc_ids_static(const void* doc_ids, int32_t id_
   const size_t clear = workspace_bytes(tiles);
   cudaError_t e = cudaMemsetAsync(scratch, 0, clear, st);
   if (e != cudaSuccess) return fail(PSEQ_ERR_CUDA, "%s: cudaMemsetAsync: %s", fn, cudaGetErrorString(e));
-  Workspace ws = carve(scratch);
+  Workspace ws = carve(scratch, kStaticBytes);
   e = id_bytes == 4 ? launch_scan<int32_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st)
                     : launch_scan<int64_t>(doc_ids, (int)N, (int)S, cu_seqlens, info, ws, (int)tiles, st);
   count_launches(1);
