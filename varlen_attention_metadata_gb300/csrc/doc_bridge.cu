@@ -308,20 +308,20 @@ __global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restric
   // Positions after the chunk's first run start do not depend on the row
   // prefix: write them now, while warp 0 looks back.  Only the pairs before
   // this thread's first known run start wait for the prefix.
+  // publish this chunk's summary first: the later chunks of the row wait for it
+  Slot* row_slots = a.slots + (int64_t)row * a.chunks;
+  const bool publish = a.chunks > 1 && (int64_t)row * a.chunks + ch != a.withhold;
+  if (ch > 0 && tid == 0 && publish) {
+    st_relaxed_u64(&row_slots[ch].agg_a, word_a(chunk_sum));
+    st_relaxed_u64(&row_slots[ch].agg_b, word_b(chunk_sum));
+  }
   int64_t* prow = a.positions ? a.positions + (int64_t)row * S : nullptr;
   const int known = before.last_run >= 0 ? 0 : (runs ? (__ffs(runs) - 1 + 1) & ~1 : kItems);
   if (prow) write_positions(prow, S, s0, runs, nz, before.last_run, known, kItems);
-  // publish this chunk's summary, then the row prefix from the chunks before it
+  // then the row prefix from the chunks before it
   if (warp == 0) {
-    Slot* row_slots = a.slots + (int64_t)row * a.chunks;
-    const int64_t linear = (int64_t)row * a.chunks + ch;
-    const bool publish = a.chunks > 1 && linear != a.withhold;
     Marks prefix = {0, -1, -1};
     if (ch > 0) {
-      if (lane == 0 && publish) {
-        st_relaxed_u64(&row_slots[ch].agg_a, word_a(chunk_sum));
-        st_relaxed_u64(&row_slots[ch].agg_b, word_b(chunk_sum));
-      }
       bool gave_up = false;
       prefix = row_prefix(a, row_slots, ch, gave_up);
       if (gave_up && lane == 0) atomicOr(&a.hdr->gave_up, 1u);
