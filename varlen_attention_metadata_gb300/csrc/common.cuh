@@ -237,37 +237,35 @@ __device__ __forceinline__ void block_copy(void* dst_, const void* src_, int64_t
   else block_copy_vec<unsigned char, 4>(dst, src, bytes);
 }
 
-// Fill `count` elements of elem_bytes at dst with the low elem_bytes of
-// `value` (little-endian), with every thread of the block.  dst must start
-// on an element boundary.
-__device__ __forceinline__ void block_fill(void* dst_, int64_t count, int elem_bytes, int64_t value) {
+// Fill `count` elements of EB bytes (1, 2, 4 or 8) at dst with the low EB
+// bytes of `value` (little-endian), with every thread of the block.  dst
+// must start on an element boundary.  Byte j of the region holds byte
+// j mod EB of the element; EB is a power of two, so that is a mask.
+template <int EB>
+__device__ __forceinline__ void block_fill(void* dst_, int64_t count, int64_t value) {
+  static_assert(EB == 1 || EB == 2 || EB == 4 || EB == 8, "element of 1, 2, 4 or 8 bytes");
   unsigned char* dst = static_cast<unsigned char*>(dst_);
   if (count <= 0) return;
   const int tid = threadIdx.x, nt = blockDim.x;
   const uint64_t v = (uint64_t)value;
-  const int64_t bytes = count * elem_bytes;
-  const uintptr_t d = reinterpret_cast<uintptr_t>(dst);
-  int64_t head = (int64_t)((16 - (d & 15)) & 15);
-  if (head > bytes) head = bytes;
-  // byte j of the region holds byte (j % elem_bytes) of the element
-  for (int64_t i = tid; i < head; i += nt) dst[i] = (unsigned char)(v >> (8 * (int)(i % elem_bytes)));
+  const int64_t bytes = count * EB;
+  const unsigned head = (unsigned)min((int64_t)((16 - (reinterpret_cast<uintptr_t>(dst) & 15)) & 15), bytes);
+  auto byte_at = [&](int64_t j) { return (unsigned char)(v >> (8 * ((unsigned)j & (EB - 1)))); };
+  for (unsigned i = tid; i < head; i += nt) dst[i] = byte_at(i);
   uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const uint32_t byte = (uint32_t)(v >> (8 * (int)((head + k) % elem_bytes))) & 0xffu;
-    w[k >> 2] |= byte << (8 * (k & 3));
-  }
+  for (int k = 0; k < 16; ++k) w[k >> 2] |= (uint32_t)byte_at(head + k) << (8 * (k & 3));
   const int4 q = make_int4((int)w[0], (int)w[1], (int)w[2], (int)w[3]);
   const int64_t nvec = (bytes - head) >> 4;
   int4* vd = reinterpret_cast<int4*>(dst + head);
   for (int64_t i = tid; i < nvec; i += nt) st_stream(vd + i, q);
   const int64_t done = head + (nvec << 4);
-  for (int64_t j = done + tid; j < bytes; j += nt) dst[j] = (unsigned char)(v >> (8 * (int)(j % elem_bytes)));
+  for (int64_t j = done + tid; j < bytes; j += nt) dst[j] = byte_at(j);
 }
 
 // Fill `count` bytes with `b` using every thread of the block.
 __device__ __forceinline__ void block_fill_bytes(uint8_t* dst, int64_t count, uint8_t b) {
-  block_fill(dst, count, 1, b);
+  block_fill<1>(dst, count, b);
 }
 
 // ----------------------------------------------------------------------------

@@ -390,8 +390,8 @@ __global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restric
   // writes only slots below `used`, so the fill never meets it.
   if (a.chunks == 1) {
     const int used = min(row_so_far.seqs, P);
-    block_fill(real_out + used, P - used, 8, a.pad_value);
-    block_fill(pad_out + used, P - used, 8, a.pad_value);
+    block_fill<8>(real_out + used, P - used, a.pad_value);
+    block_fill<8>(pad_out + used, P - used, a.pad_value);
   } else if (!row_end) {
     if (tid == 0) {
       const Slot* last = a.slots + (int64_t)row * a.chunks + (a.chunks - 1);
@@ -417,8 +417,8 @@ __global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restric
     if (used >= 0) {
       const int64_t rest = P - used, shares = a.chunks - 1;
       const int64_t lo = used + rest * ch / shares, hi = used + rest * (ch + 1) / shares;
-      block_fill(real_out + lo, hi - lo, 8, a.pad_value);
-      block_fill(pad_out + lo, hi - lo, 8, a.pad_value);
+      block_fill<8>(real_out + lo, hi - lo, a.pad_value);
+      block_fill<8>(pad_out + lo, hi - lo, a.pad_value);
     }
   }
   __syncthreads();
