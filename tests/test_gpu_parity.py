@@ -257,6 +257,42 @@ def test_doc_ids_tag_wraps_around(withheld):
     assert header_tag(ws) == 1
 
 
+def test_doc_ids_graph_replays_share_a_workspace():
+    """Two maps captured as CUDA graphs on one workspace and replayed in
+    turn: each replay takes the next tag from the header at run time (a
+    captured launch carries no tag), so every replay is exact."""
+    import ctypes
+
+    v = V()
+    lib = v.load_library()
+    rng = np.random.default_rng(23)
+    maps = [synth.random_doc_ids(rng, 5, 70_000, "runs", np.int32), synth.random_doc_ids(rng, 2, 40_000, "iid", np.int32)]
+    refs = [oracle.from_doc_ids(m) for m in maps]
+    nbytes = max(lib.pseq_from_doc_ids_workspace_size(*m.shape) for m in maps)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    stream = torch.cuda.Stream()
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    bufs, graphs = [], []
+    for m in maps:
+        x = dev(m)
+        cu = torch.full((m.size + 1,), -1, dtype=torch.int32, device=DEV)
+        info = torch.zeros(32, dtype=torch.uint8, device=DEV)
+        bufs.append((x, cu, info))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            assert lib.pseq_from_doc_ids(P(x), 4, m.shape[0], m.shape[1], P(cu), P(info), P(ws), ws.numel(),
+                                         ctypes.c_void_p(stream.cuda_stream)) == 0
+        graphs.append(g)
+    for rep in range(6):
+        k = rep % 2
+        bufs[k][1].fill_(-1)
+        graphs[k].replay()
+        torch.cuda.synchronize()
+        ref_cu, ref_mx = refs[k]
+        assert info_of(bufs[k][2]) == (0, len(ref_cu) - 1, ref_mx, maps[k].size), rep
+        np.testing.assert_array_equal(bufs[k][1][: len(ref_cu)].cpu().numpy(), ref_cu)
+
+
 @pytest.mark.parametrize("withheld", [0, 1, 4])
 def test_doc_ids_failed_call_leaves_workspace_usable(withheld):
     """A tile that never publishes (the first, a middle one, the last of
