@@ -214,9 +214,71 @@ struct Fields {
   int narrow;  // every row of every field is one aligned access of <= 16 bytes
   int bulk;    // every row of every field is >= 256 bytes, a multiple of 16, 16-byte aligned
   int njobs;   // (field, plane) pairs, for the row-by-row path
-  unsigned char job_field[kMaxJobs];
-  unsigned char job_plane[kMaxJobs];
+  int rb_all;  // every field's row is this many bytes (8: int64 ids, labels, positions), else 0
+  // per (field, plane) job of the row-by-row path, read at fixed offsets in
+  // an unrolled loop: field base pointers, plane, the field's planes, row bytes
+  const unsigned char* job_src[kMaxJobs];
+  unsigned char* job_dst[kMaxJobs];
+  int job_plane[kMaxJobs];
+  int job_planes[kMaxJobs];
+  int job_rb[kMaxJobs];
 };
+
+// The row-by-row path: one thread per stream row, every (field, plane) load
+// issued before any store.  A warp finds the sequence of its first row with
+// one search that every lane runs alike (broadcast shared-memory reads), and
+// each lane walks forward over the few sequence starts among the warp's 32
+// rows (a search of its own after 8 steps).  RB = 8 when every row is 8
+// bytes (no size switch), else 0.
+template <int RB>
+__device__ __forceinline__ void narrow_rows(const Fields& f, int64_t plane_in, int64_t T, uint8_t* mask, int64_t lo,
+                                            int64_t hi, const int32_t* cup, const int32_t* src_tok,
+                                            const int32_t* real, int cnt, int64_t chunk, int64_t chunk_rows) {
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31;
+  for (int64_t rw = lo + (tid - lane); rw < hi; rw += nt) {
+    const int64_t r = rw + lane;
+    int j = seq_of(cup, cnt, rw);
+    if (r < hi) {
+      int steps = 0;
+      while ((int64_t)cup[j + 1] <= r && steps < 8) {
+        ++j;
+        ++steps;
+      }
+      if ((int64_t)cup[j + 1] <= r) j = seq_of(cup, cnt, r);
+      const int64_t off = r - cup[j];
+      const int64_t tok = (int64_t)src_tok[j] + off;
+      for (int g = 0; g < f.njobs; g += 8) {
+        int4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (g + q < f.njobs) {
+            const int rb = RB ? RB : f.job_rb[g + q];
+            const unsigned char* p = f.job_src[g + q] + ((int64_t)f.job_plane[g + q] * plane_in + tok) * rb;
+            if (RB == 8) {
+              const uint2 t = __ldg(reinterpret_cast<const uint2*>(p));
+              v[q] = make_int4((int)t.x, (int)t.y, 0, 0);
+            } else {
+              v[q] = load_row(p, rb);
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (g + q < f.njobs) {
+            const int rb = RB ? RB : f.job_rb[g + q];
+            unsigned char* p =
+                f.job_dst[g + q] + (chunk * f.job_planes[g + q] * chunk_rows + f.job_plane[g + q] * T + r) * rb;
+            if (RB == 8)
+              *reinterpret_cast<uint2*>(p) = make_uint2((unsigned)v[q].x, (unsigned)v[q].y);
+            else
+              store_row(p, v[q], rb);
+          }
+        }
+      }
+      if (mask) mask[r] = off >= real[j] ? 1 : 0;
+    }
+  }
+}
 
 // Move stream rows [lo, hi) of every field and write their mask bytes.
 // Sequences j = 0..cnt-1 of the table start at stream row cup[j] (cup[cnt]
@@ -231,31 +293,10 @@ __device__ void gather_rows(const Fields& f, int64_t B, int64_t S, int64_t T, ui
   const int tid = threadIdx.x, nt = blockDim.x;
   const int64_t plane_in = B * S;
   if (f.narrow) {
-    for (int64_t r = lo + tid; r < hi; r += nt) {
-      const int j = seq_of(cup, cnt, r);
-      const int64_t off = r - cup[j];
-      const int64_t tok = (int64_t)src_tok[j] + off;
-      for (int g = 0; g < f.njobs; g += 8) {
-        int4 v[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (g + q < f.njobs) {
-            const int i = f.job_field[g + q], p = f.job_plane[g + q];
-            const int64_t rb = f.row_bytes[i];
-            v[q] = load_row(f.src[i] + ((int64_t)p * plane_in + tok) * rb, (int)rb);
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (g + q < f.njobs) {
-            const int i = f.job_field[g + q], p = f.job_plane[g + q];
-            const int64_t rb = f.row_bytes[i];
-            store_row(f.dst[i] + (chunk * f.planes[i] * chunk_rows + p * T + r) * rb, v[q], (int)rb);
-          }
-        }
-      }
-      if (mask) mask[r] = off >= real[j] ? 1 : 0;
-    }
+    if (f.rb_all == 8)
+      narrow_rows<8>(f, plane_in, T, mask, lo, hi, cup, src_tok, real, cnt, chunk, chunk_rows);
+    else
+      narrow_rows<0>(f, plane_in, T, mask, lo, hi, cup, src_tok, real, cnt, chunk, chunk_rows);
     return;
   }
   for (int j = seq_of(cup, cnt, lo); j < cnt; ++j) {
@@ -654,14 +695,20 @@ pseq_status build_fields(const char* fn, const pseq_field* fields, int num_field
     if (!one_access) f.narrow = 0;
     for (int p = 0; p < x.planes; ++p) {
       if (jobs < kMaxJobs) {
-        f.job_field[jobs] = (unsigned char)i;
-        f.job_plane[jobs] = (unsigned char)p;
+        f.job_src[jobs] = f.src[i];
+        f.job_dst[jobs] = f.dst[i];
+        f.job_plane[jobs] = p;
+        f.job_planes[jobs] = x.planes;
+        f.job_rb[jobs] = (int)rb;
       }
       ++jobs;
     }
   }
   if (jobs > kMaxJobs) f.narrow = 0;
   f.njobs = f.narrow ? jobs : 0;
+  f.rb_all = 8;
+  for (int i = 0; i < num_fields; ++i)
+    if (f.row_bytes[i] != 8) f.rb_all = 0;
   f.bulk = num_fields > 0;
   for (int i = 0; i < num_fields; ++i) {
     const int64_t rb = f.row_bytes[i];
