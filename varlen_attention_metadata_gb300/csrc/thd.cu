@@ -114,15 +114,25 @@ struct ScanResult {
 // Walk the tables in row-major order, dropping filler entries, and call
 // put(k, b, o, real, padded, R, Pd) for kept entry k of row b at in-row
 // offset o, where R and Pd are the real and padded sums of the kept entries
-// before it.  Every thread returns the same totals; the flags are in *fl.
+// before it.  Every thread returns the same totals; the flags are in *fl,
+// complete after the caller's next barrier (the last round ends without
+// one).  Three barriers per round: the warp sums, their scan in warp 0, and
+// the round's end (left to the caller in the last round).  A row's start
+// (the padded prefix at its first entry) comes from the warp sums and the
+// first entry's in-warp prefix, which that thread leaves in row_pfx before
+// the first barrier; in later rounds row_pfx holds the finished value.
 template <int THREADS, typename Put>
 __device__ ScanResult scan_lengths(const MetaArgs& a, int64_t* row_pfx, Triple* scratch, ScanFlags* fl, Put put) {
-  const int tid = threadIdx.x;
-  if (tid == 0) *fl = {0, 0, -1, 0};
-  __syncthreads();
+  constexpr int kW = THREADS / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) *fl = {0, 0, -1, 0};  // ordered before every update by the round's barriers
   const int E = a.B * a.P;
   Triple carry = {0, 0, 0};
+  int done_row = -1;       // the row this thread started in the last round, and its start
+  long long done_pfx = 0;
   for (int base = 0; base < E; base += THREADS) {
+    if (done_row >= 0) row_pfx[done_row] = done_pfx;  // read after this round's barriers
+    done_row = -1;
     const int e = base + tid;
     const bool valid = e < E;
     long long real = 0, padded = 0;
@@ -139,17 +149,48 @@ __device__ ScanResult scan_lengths(const MetaArgs& a, int64_t* row_pfx, Triple* 
         if (real < 0 || padded < real) bad = true;
       }
     }
-    Triple total;
-    const Triple ex = block_exclusive<THREADS / 32>({keep ? 1 : 0, keep ? real : 0, keep ? padded : 0}, scratch,
-                                                    total);
-    const int k = carry.count + ex.count;
-    const long long R = carry.real + ex.real;
-    const long long Pd = carry.padded + ex.padded;
+    const Triple x = {keep ? 1 : 0, keep ? real : 0, keep ? padded : 0};
+    Triple inc = x;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const Triple o = shfl_up(inc, d);
+      if (lane >= d) inc = add(o, inc);
+    }
+    const Triple wex = {inc.count - x.count, inc.real - x.real, inc.padded - x.padded};
     const int b = valid ? e / a.P : 0;
-    if (valid && e % a.P == 0) row_pfx[b] = Pd;
+    const bool row_first = valid && e % a.P == 0;
+    if (lane == 31) scratch[warp] = inc;
+    if (row_first) row_pfx[b] = wex.padded;  // this round's part: completed below from the warp sums
     __syncthreads();
+    if (warp == 0) {
+      Triple w = lane < kW ? scratch[lane] : Triple{0, 0, 0};
+#pragma unroll
+      for (int d = 1; d < kW; d <<= 1) {
+        const Triple o = shfl_up(w, d);
+        if (lane >= d) w = add(o, w);
+      }
+      if (lane < kW) scratch[lane] = w;
+    }
+    __syncthreads();
+    const Triple total = scratch[kW - 1];
+    const Triple wpre = warp > 0 ? scratch[warp - 1] : Triple{0, 0, 0};
+    const int k = carry.count + wpre.count + wex.count;
+    const long long R = carry.real + wpre.real + wex.real;
+    const long long Pd = carry.padded + wpre.padded + wex.padded;
+    if (row_first) {
+      done_row = b;
+      done_pfx = Pd;
+    }
     if (keep) {
-      const long long o = Pd - row_pfx[b];
+      const int e0 = b * a.P;  // the row's first entry
+      long long start;
+      if (e0 >= base) {
+        const int w0 = (e0 - base) >> 5;
+        start = carry.padded + (w0 > 0 ? scratch[w0 - 1].padded : 0) + row_pfx[b];
+      } else {
+        start = row_pfx[b];
+      }
+      const long long o = Pd - start;
       if (o + padded > a.S) bad = true;
       put(k, b, o, real, padded, R, Pd);
       if (real != padded) {
@@ -160,7 +201,7 @@ __device__ ScanResult scan_lengths(const MetaArgs& a, int64_t* row_pfx, Triple* 
     }
     if (bad) fl->bad = 1;
     carry = add(carry, total);
-    __syncthreads();
+    if (base + THREADS < E) __syncthreads();  // the next round reuses scratch and row_pfx
   }
   return {carry.count, carry.real, carry.padded};
 }
@@ -386,12 +427,10 @@ __device__ __forceinline__ Summary fused_scan(const MetaArgs& ac, const Tables& 
     }
   };
   const ScanResult r = scan_lengths<kRowThreads>(ac, t.row, scratch, fl, put);
+  if (threadIdx.x == 0) t.cup[r.n] = (int32_t)r.padded;  // the stream's end (= T)
+  __syncthreads();  // the tables and the flags are complete
   const Summary s = summarize(ac, r, *fl, r.n ? t.real[r.n - 1] : 0);
-  if (threadIdx.x == 0) {
-    t.cup[r.n] = (int32_t)s.T;
-    if (lead) write_meta(ac, s);
-  }
-  __syncthreads();
+  if (lead && threadIdx.x == 0) write_meta(ac, s);
   n = r.n;
   return s;
 }
@@ -564,6 +603,7 @@ __global__ void __launch_bounds__(kMetaThreads) thd_meta_kernel(const __grid_con
     if (a.cu_padded) a.cu_padded[k] = (int32_t)Pd;
   };
   const ScanResult r = scan_lengths<kMetaThreads>(a, ws.row_pfx, scratch, &fl, put);
+  __syncthreads();  // the flags and the tables are complete
   if (threadIdx.x != 0) return;
   const Summary s = summarize(a, r, fl, r.n ? ws.seq_real[r.n - 1] : 0);
   ws.seq_cup[r.n] = (int32_t)s.T;
