@@ -20,11 +20,13 @@
 // predecessors per poll round, stopping at the nearest inclusive prefix,
 // bounded waits).  It then walks its tokens: every run end writes its
 // sequence's real length, every sequence start closes the padded length of
-// the one before it, and the row's last chunk closes the row; the row's
-// other chunks then share the fill of its unused slots.  Each chunk writes its own statistics record; the CTA that finishes
-// last (a wrapping acq_rel counter) folds the records into the info block
-// and clears the summary words, so the workspace is zero again for the next
-// call.
+// the one before it, and the row's last chunk closes the row.  One more CTA
+// per row, dispatched after the row's chunks, waits for the row's sequence
+// count (the last chunk's inclusive summary) and fills the row's unused
+// slots, so no chunk waits for that.  Each chunk writes its own statistics
+// record; the CTA that finishes last (a wrapping acq_rel counter) folds the
+// records into the info block and clears the summary words, so the
+// workspace is zero again for the next call.
 #include "common.cuh"
 
 namespace pseq {
@@ -278,6 +280,55 @@ __global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restric
     s_longest = 0;
     s_overflow = 0;
   }
+  const unsigned ctas = gridDim.x * gridDim.y;
+  // The CTA that finishes last folds every chunk's record into the info
+  // block and leaves the workspace zero.
+  auto finish = [&]() {
+    __syncthreads();
+    if (!s_last) return;
+    fold_stats(a);
+    if (a.chunks > 1) {
+      unsigned long long* words = reinterpret_cast<unsigned long long*>(a.slots);
+      const int64_t n = 4 * (int64_t)a.B * a.chunks;
+      for (int64_t i = tid; i < n; i += kThreads) words[i] = 0ull;
+    }
+  };
+  if (a.chunks > 1 && ch == a.chunks) {
+    // ---- the row's fill CTA (dispatched right after its chunks): once the
+    // row's last chunk has published the row's sequence count, its unused
+    // slots [used, P) take pad_value.  The chunks' walks write only slots
+    // below `used`, so the fill never meets them.
+    if (tid == 0) {
+      const Slot* last = a.slots + (int64_t)row * a.chunks + (a.chunks - 1);
+      int used = -1, polls = 0;
+      uint64_t start = 0;
+      while (true) {
+        const unsigned long long ia = ld_relaxed_u64(&last->inc_a), ib = ld_relaxed_u64(&last->inc_b);
+        if (ia & ib & kValid) {
+          used = min(from_words(ia, ib).seqs, P);
+          break;
+        }
+        if (polls++ == 0) {
+          start = global_ns();
+        } else if ((int64_t)(global_ns() - start) >= a.wait_ns) {
+          atomicOr(&a.hdr->gave_up, 1u);  // reported as PSEQ_ERR_TIMEOUT; the slots are left unfilled
+          break;
+        }
+      }
+      s_used = used;
+    }
+    __syncthreads();
+    const int used = s_used;
+    if (used >= 0) {
+      block_fill<8>(real_out + used, P - used, a.pad_value);
+      block_fill<8>(pad_out + used, P - used, a.pad_value);
+    }
+    __syncthreads();
+    // this CTA reads no more summary words (release); the last to arrive acquires all
+    if (tid == 0) s_last = inc_acq_rel(&a.hdr->finished, ctas - 1u) == ctas - 1u;
+    finish();
+    return;
+  }
   unsigned runs, seqs, nz, pnz;
   const int s0 = ch * kTile + tid * kItems;
   const Marks mine = chunk_flags(d, S, s0, runs, seqs, nz, pnz);
@@ -381,45 +432,12 @@ __global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restric
     }
     if (total - 1 < P) pad_out[total - 1] = S - row_so_far.last_seq;
   }
-  // The row's unused slots [used, P) take pad_value.  With one chunk per row
-  // that chunk fills them.  Otherwise the row's other chunks share the fill:
-  // each waits for the last chunk's inclusive summary (the row's sequence
-  // count, published right after that chunk's look-back; the last chunk is
-  // dispatched right after them and waits only on earlier chunks) and fills
-  // one share, so the last chunk is not left with the whole fill.  The walk
-  // writes only slots below `used`, so the fill never meets it.
+  // With one chunk per row, that chunk fills the row's unused slots [used, P);
+  // otherwise the row's fill CTA does.
   if (a.chunks == 1) {
     const int used = min(row_so_far.seqs, P);
     block_fill<8>(real_out + used, P - used, a.pad_value);
     block_fill<8>(pad_out + used, P - used, a.pad_value);
-  } else if (!row_end) {
-    if (tid == 0) {
-      const Slot* last = a.slots + (int64_t)row * a.chunks + (a.chunks - 1);
-      int used = -1, polls = 0;
-      uint64_t start = 0;
-      while (true) {
-        const unsigned long long ia = ld_relaxed_u64(&last->inc_a), ib = ld_relaxed_u64(&last->inc_b);
-        if (ia & ib & kValid) {
-          used = min(from_words(ia, ib).seqs, P);
-          break;
-        }
-        if (polls++ == 0) {
-          start = global_ns();
-        } else if ((int64_t)(global_ns() - start) >= a.wait_ns) {
-          atomicOr(&a.hdr->gave_up, 1u);  // reported as PSEQ_ERR_TIMEOUT; the share is left unfilled
-          break;
-        }
-      }
-      s_used = used;
-    }
-    __syncthreads();
-    const int used = s_used;
-    if (used >= 0) {
-      const int64_t rest = P - used, shares = a.chunks - 1;
-      const int64_t lo = used + rest * ch / shares, hi = used + rest * (ch + 1) / shares;
-      block_fill<8>(real_out + lo, hi - lo, a.pad_value);
-      block_fill<8>(pad_out + lo, hi - lo, a.pad_value);
-    }
   }
   __syncthreads();
   const int64_t linear = (int64_t)row * a.chunks + ch;
@@ -427,18 +445,9 @@ __global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restric
     a.stats[linear] = Stat{s_longest, s_overflow, row_end ? row_so_far.seqs : 0, row_end ? 1 : 0};
     // this CTA reads no more summary words and has written its record
     // (release); the last one to arrive acquires them all
-    const unsigned ctas = gridDim.x * gridDim.y;
     s_last = inc_acq_rel(&a.hdr->finished, ctas - 1u) == ctas - 1u;
   }
-  __syncthreads();
-  if (!s_last) return;
-  // ---- last CTA: fold the records, report, leave the workspace zero
-  fold_stats(a);
-  if (a.chunks > 1) {
-    unsigned long long* words = reinterpret_cast<unsigned long long*>(a.slots);
-    const int64_t n = 4 * (int64_t)a.B * a.chunks;
-    for (int64_t i = tid; i < n; i += kThreads) words[i] = 0ull;
-  }
+  finish();
 }
 
 // A row of length 0 still has its slots filled; nothing else to do.
@@ -511,7 +520,8 @@ extern "C" pseq_status pseq_doc_ids_to_lengths(const void* doc_ids, int32_t id_b
     a.stats = reinterpret_cast<Stat*>(a.slots + (int64_t)B * a.chunks);
     a.wait_ns = wait_limit_ns();
     a.withhold = withhold_tile();
-    const dim3 grid((unsigned)a.chunks, (unsigned)B);
+    // each row's chunks, then (with more than one chunk) the row's fill CTA
+    const dim3 grid((unsigned)(a.chunks + (a.chunks > 1 ? 1 : 0)), (unsigned)B);
     e = id_bytes == 4 ? launch_pdl(bridge_kernel<int32_t>, grid, dim3(kThreads), 0, st,
                                    static_cast<const int32_t*>(doc_ids), a)
                       : launch_pdl(bridge_kernel<int64_t>, grid, dim3(kThreads), 0, st,
