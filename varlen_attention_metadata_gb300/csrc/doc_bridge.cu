@@ -232,6 +232,9 @@ __device__ __noinline__ void fold_stats(const BridgeArgs& a) {
   const int tid = threadIdx.x, lane = tid & 31;
   __shared__ int f_longest, f_overflow, f_most, f_total;
   if (tid == 0) f_longest = f_overflow = f_most = f_total = 0;
+  // an L2 load beside the records': the counter this CTA acquired ordered
+  // every CTA's flag update before it
+  const unsigned failed = tid == 0 ? __ldcg(&a.hdr->gave_up) : 0u;
   __syncthreads();
   int lng = 0, over = 0, most = 0, total = 0;
   const int64_t n = (int64_t)a.B * a.chunks;
@@ -258,7 +261,7 @@ __device__ __noinline__ void fold_stats(const BridgeArgs& a) {
   }
   __syncthreads();
   if (tid == 0) {
-    const unsigned failed = atomicExch(&a.hdr->gave_up, 0u);
+    if (failed) a.hdr->gave_up = 0u;  // every CTA has counted itself done: no writer is left
     const int status = failed ? PSEQ_ERR_TIMEOUT : (f_overflow ? PSEQ_ERR_CAPACITY : PSEQ_OK);
     *a.info = pseq_info{status, f_most, f_longest, f_total};
   }
