@@ -257,6 +257,20 @@ def test_doc_ids_tag_wraps_around(withheld):
     assert header_tag(ws) == 1
 
 
+def test_doc_ids_random_sequence_of_calls():
+    """Sixty calls on the one cached workspace with random shapes (1 to 40
+    tiles), kinds and id widths: every call leaves summaries of its own size
+    behind, and every later call must ignore them."""
+    rng = np.random.default_rng(29)
+    kinds = ["runs", "iid", "zeros", "const", "alternating", "long"]
+    for i in range(60):
+        tiles = int(rng.integers(1, 41))
+        B = int(rng.integers(1, 9))
+        S = max(1, int(tiles * 16384 // B - rng.integers(0, 4000)))
+        dtype = np.int64 if rng.random() < 0.3 else np.int32
+        check_doc_ids(synth.random_doc_ids(rng, B, S, kinds[i % len(kinds)], dtype))
+
+
 def test_doc_ids_graph_replays_share_a_workspace():
     """Two maps captured as CUDA graphs on one workspace and replayed in
     turn: each replay takes the next tag from the header at run time (a
