@@ -23,10 +23,11 @@
 // the one before it, and the row's last chunk closes the row.  One more CTA
 // per row, dispatched after the row's chunks, waits for the row's sequence
 // count (the last chunk's inclusive summary) and fills the row's unused
-// slots, so no chunk waits for that.  Each chunk writes its own statistics
-// record; the CTA that finishes last (a wrapping acq_rel counter) folds the
-// records into the info block and clears the summary words, so the
-// workspace is zero again for the next call.
+// slots, so no chunk waits for that.  Each chunk adds its share to the
+// call's totals in the workspace header (atomics that return nothing); the
+// CTA that finishes last (a wrapping acq_rel counter) reads them into the
+// info block, resets them and clears the summary words, so the workspace is
+// zero again for the next call.
 #include "common.cuh"
 
 namespace pseq {
@@ -39,15 +40,13 @@ constexpr int kTile = kThreads * kItems;
 struct Header {
   unsigned finished;  // CTAs done with their look-back; wraps back to 0 after each call
   unsigned gave_up;   // a wait hit its time limit
-  unsigned pad[30];
+  // the call's running totals, reset by the CTA that finishes last: longest
+  // document run, a row that overflowed its slots, most sequences in a row,
+  // sequences in all rows
+  unsigned longest, overflow, most, total;
+  unsigned pad[26];
 };
 
-// Per chunk, written by its own CTA every call and folded by the last one:
-// longest document run ending in the chunk, whether the row overflowed its
-// slots there, and (for a row's last chunk) the row's sequence count.
-struct Stat {
-  int longest, overflow, row_seqs, row_end;
-};
 static_assert(sizeof(Header) == 128, "header is 128 bytes");
 
 // Per chunk: its own summary and the inclusive one (the row up to it), each
@@ -58,7 +57,7 @@ struct Slot {
 
 size_t workspace_bytes(int64_t B, int64_t S) {
   const int64_t chunks = S > 0 ? (S + kTile - 1) / kTile : 1;
-  return sizeof(Header) + (sizeof(Slot) + sizeof(Stat)) * (size_t)(B > 0 ? B : 1) * (size_t)chunks;
+  return sizeof(Header) + sizeof(Slot) * (size_t)(B > 0 ? B : 1) * (size_t)chunks;
 }
 
 constexpr unsigned long long kValid = 1ull << 63;
@@ -99,7 +98,6 @@ struct BridgeArgs {
   pseq_info* info;
   Header* hdr;
   Slot* slots;         // [B * chunks]
-  Stat* stats;         // [B * chunks]
   int64_t wait_ns;
   int64_t withhold;    // chunk (row-major) that never publishes: failure tests only
 };
@@ -227,44 +225,19 @@ __device__ __forceinline__ void write_positions(int64_t* prow, int S, int s0, un
   }
 }
 
-// The last CTA: fold every chunk's record into the info block.
-__device__ __noinline__ void fold_stats(const BridgeArgs& a) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  __shared__ int f_longest, f_overflow, f_most, f_total;
-  if (tid == 0) f_longest = f_overflow = f_most = f_total = 0;
-  // an L2 load beside the records': the counter this CTA acquired ordered
-  // every CTA's flag update before it
-  const unsigned failed = tid == 0 ? __ldcg(&a.hdr->gave_up) : 0u;
-  __syncthreads();
-  int lng = 0, over = 0, most = 0, total = 0;
-  const int64_t n = (int64_t)a.B * a.chunks;
-  for (int64_t i = tid; i < n; i += kThreads) {
-    // L2 loads: the records were released by the counter that thread 0 acquired
-    const int4 r = __ldcg(reinterpret_cast<const int4*>(a.stats + i));
-    lng = max(lng, r.x);
-    over |= r.y;
-    most = max(most, r.z);
-    total += r.z;
-  }
-#pragma unroll
-  for (int dd = 16; dd > 0; dd >>= 1) {
-    lng = max(lng, __shfl_xor_sync(~0u, lng, dd));
-    over |= __shfl_xor_sync(~0u, over, dd);
-    most = max(most, __shfl_xor_sync(~0u, most, dd));
-    total += __shfl_xor_sync(~0u, total, dd);
-  }
-  if (lane == 0) {
-    atomicMax(&f_longest, lng);
-    atomicOr(&f_overflow, over);
-    atomicMax(&f_most, most);
-    atomicAdd(&f_total, total);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    if (failed) a.hdr->gave_up = 0u;  // every CTA has counted itself done: no writer is left
-    const int status = failed ? PSEQ_ERR_TIMEOUT : (f_overflow ? PSEQ_ERR_CAPACITY : PSEQ_OK);
-    *a.info = pseq_info{status, f_most, f_longest, f_total};
-  }
+// The CTA that finishes last: report the call's totals and reset them (every
+// other CTA has counted itself done, so no update is left in flight).
+__device__ __forceinline__ void report(const BridgeArgs& a) {
+  // L2 loads: the counter this CTA acquired ordered every update before it
+  const unsigned failed = __ldcg(&a.hdr->gave_up), longest = __ldcg(&a.hdr->longest),
+                 overflow = __ldcg(&a.hdr->overflow), most = __ldcg(&a.hdr->most), total = __ldcg(&a.hdr->total);
+  const int status = failed ? PSEQ_ERR_TIMEOUT : (overflow ? PSEQ_ERR_CAPACITY : PSEQ_OK);
+  *a.info = pseq_info{status, (int32_t)most, (int32_t)longest, (int32_t)total};
+  a.hdr->gave_up = 0u;
+  a.hdr->longest = 0u;
+  a.hdr->overflow = 0u;
+  a.hdr->most = 0u;
+  a.hdr->total = 0u;
 }
 
 template <typename Id>
@@ -284,12 +257,12 @@ __global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restric
     s_overflow = 0;
   }
   const unsigned ctas = gridDim.x * gridDim.y;
-  // The CTA that finishes last folds every chunk's record into the info
-  // block and leaves the workspace zero.
+  // The CTA that finishes last reports the call's totals and leaves the
+  // workspace zero.
   auto finish = [&]() {
     __syncthreads();
     if (!s_last) return;
-    fold_stats(a);
+    if (tid == 0) report(a);
     if (a.chunks > 1) {
       unsigned long long* words = reinterpret_cast<unsigned long long*>(a.slots);
       const int64_t n = 4 * (int64_t)a.B * a.chunks;
@@ -443,10 +416,15 @@ __global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restric
     block_fill<8>(pad_out + used, P - used, a.pad_value);
   }
   __syncthreads();
-  const int64_t linear = (int64_t)row * a.chunks + ch;
   if (tid == 0) {
-    a.stats[linear] = Stat{s_longest, s_overflow, row_end ? row_so_far.seqs : 0, row_end ? 1 : 0};
-    // this CTA reads no more summary words and has written its record
+    // this chunk's share of the totals (atomics that return nothing)
+    if (s_longest) atomicMax(&a.hdr->longest, (unsigned)s_longest);
+    if (s_overflow) atomicOr(&a.hdr->overflow, 1u);
+    if (row_end) {
+      atomicMax(&a.hdr->most, (unsigned)row_so_far.seqs);
+      atomicAdd(&a.hdr->total, (unsigned)row_so_far.seqs);
+    }
+    // this CTA reads no more summary words and has added its share
     // (release); the last one to arrive acquires them all
     s_last = inc_acq_rel(&a.hdr->finished, ctas - 1u) == ctas - 1u;
   }
@@ -520,7 +498,6 @@ extern "C" pseq_status pseq_doc_ids_to_lengths(const void* doc_ids, int32_t id_b
                   workspace_bytes_);
     a.hdr = static_cast<Header*>(workspace);
     a.slots = reinterpret_cast<Slot*>(static_cast<unsigned char*>(workspace) + sizeof(Header));
-    a.stats = reinterpret_cast<Stat*>(a.slots + (int64_t)B * a.chunks);
     a.wait_ns = wait_limit_ns();
     a.withhold = withhold_tile();
     // each row's chunks, then (with more than one chunk) the row's fill CTA
