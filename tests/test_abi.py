@@ -49,8 +49,9 @@ def test_workspace_sizes(lib):
     big = lib.pseq_from_doc_ids_workspace_size(64, 32768)
     assert 0 < small < big
     assert lib.thd_workspace_size(8, 64) >= 8 * 64 * 16
-    assert lib.pack_squeeze_workspace_size(256, 8) >= 8 * 16
-    assert lib.pack_squeeze_workspace_size(16384, 8) == lib.pack_squeeze_workspace_size(256, 8)
+    # the squeeze's scratch is a fixed header (a counter and running totals)
+    assert lib.pack_squeeze_workspace_size(256, 8) > 0
+    assert lib.pack_squeeze_workspace_size(16384, 65535) == lib.pack_squeeze_workspace_size(256, 8)
 
 
 def test_host_argument_errors_without_gpu(lib):

@@ -18,9 +18,10 @@
 // load before any store, and writes the token or pad_value with its mask
 // byte.  Every output slot is written exactly once.
 //
-// The first window of every bin also writes the bin's cu arrays and its
-// status record; the last of those CTAs to finish (a wrapping acq_rel
-// counter) folds all records into the info block.
+// The first window of every bin also writes the bin's cu arrays and adds
+// its status and sizes to running totals in the workspace header (atomics
+// that return nothing); the last of those CTAs to finish (a wrapping acq_rel
+// counter) writes the info block from them and resets them.
 #include "common.cuh"
 
 namespace pseq {
@@ -39,15 +40,17 @@ __host__ __device__ constexpr int slots_wide() {
 }
 
 struct Header {
-  unsigned finished;
-  unsigned pad[31];
+  unsigned finished;  // bins whose first window is done; wraps back to 0 after each call
+  // the call's running totals, reset by the first window that finishes
+  // last: a bin with malformed members or offsets (bit 0) or over capacity
+  // (bit 1), the longest member, the widest bin
+  unsigned flags, longest, widest;
+  unsigned pad[28];
 };
 
-struct BinRec {
-  int status, total, longest, members;
-};
+static_assert(sizeof(Header) == 128, "header is 128 bytes");
 
-size_t workspace_bytes(int64_t num_bins) { return sizeof(Header) + sizeof(BinRec) * (size_t)num_bins; }
+size_t workspace_bytes(int64_t) { return sizeof(Header); }
 
 template <int SLOTS>
 __host__ __device__ constexpr int window() {
@@ -74,7 +77,6 @@ struct Args {
   int32_t* cup;
   pseq_info* info;
   Header* hdr;
-  BinRec* rec;
 };
 
 __device__ __forceinline__ bool offsets_bad(const Args& a, int b, int lo, int hi) {
@@ -118,30 +120,16 @@ struct Elem<8> {
   using T = unsigned long long;
 };
 
-// The last bin record to arrive: fold every bin's record into info.
-__device__ __noinline__ void fold_records(const Args& a) {
-  __shared__ int f_value, f_capacity, f_longest, f_widest;
-  const int tid = threadIdx.x;
-  if (tid == 0) f_value = f_capacity = f_longest = f_widest = 0;
-  __syncthreads();
-  int value = 0, capacity = 0, longest = 0, widest = 0;
-  for (int i = tid; i < a.num_bins; i += kThreads) {
-    // L2 loads: the records were released by the counter that thread 0 acquired
-    const int4 r = __ldcg(reinterpret_cast<const int4*>(a.rec + i));
-    value |= r.x == PSEQ_ERR_VALUE;
-    capacity |= r.x == PSEQ_ERR_CAPACITY;
-    widest = max(widest, r.y);
-    longest = max(longest, r.z);
-  }
-  if (value) f_value = 1;
-  if (capacity) f_capacity = 1;
-  atomicMax(&f_longest, longest);
-  atomicMax(&f_widest, widest);
-  __syncthreads();
-  if (tid == 0) {
-    const int status = f_value ? PSEQ_ERR_VALUE : (f_capacity ? PSEQ_ERR_CAPACITY : PSEQ_OK);
-    *a.info = status == PSEQ_OK ? pseq_info{PSEQ_OK, a.M, f_longest, f_widest} : pseq_info{status, 0, 0, 0};
-  }
+// The first window that finishes last: report the call's totals and reset
+// them (every other first window has counted itself in).
+__device__ __forceinline__ void report(const Args& a) {
+  // L2 loads: the counter this CTA acquired ordered every update before it
+  const unsigned flags = __ldcg(&a.hdr->flags), longest = __ldcg(&a.hdr->longest), widest = __ldcg(&a.hdr->widest);
+  const int status = (flags & 1u) ? PSEQ_ERR_VALUE : ((flags & 2u) ? PSEQ_ERR_CAPACITY : PSEQ_OK);
+  *a.info = status == PSEQ_OK ? pseq_info{PSEQ_OK, a.M, (int)longest, (int)widest} : pseq_info{status, 0, 0, 0};
+  a.hdr->flags = 0u;
+  a.hdr->longest = 0u;
+  a.hdr->widest = 0u;
 }
 
 // `cap` = table_entries(window, multiple): the table's length in entries.
@@ -221,23 +209,27 @@ __global__ void __launch_bounds__(kThreads, SLOTS >= 16 ? 5 : (SLOTS >= 12 ? 6 :
   int status = PSEQ_OK;
   if (bad_offsets || s_bad) status = PSEQ_ERR_VALUE;
   else if (total_pad > a.capacity || (a.out && total_pad > a.width)) status = PSEQ_ERR_CAPACITY;
-  // First windows publish their bin's record and count it in; the counter's
+  // First windows add their bin's share and count it in; the counter's
   // old value is looked at only after the window has streamed, so that its
-  // round trip overlaps the copy.  The last record to arrive folds them all.
+  // round trip overlaps the copy.  The last to arrive reports the totals.
   unsigned ticket = 0;
   if (first && tid == 0) {
     if (!bad_offsets) {
       a.cu[hi + b] = (int32_t)carry.real;
       a.cup[hi + b] = a.stretch ? (int32_t)a.capacity : (int32_t)total_pad;
     }
-    a.rec[b] = BinRec{status, (int)min(total_pad, (long long)INT32_MAX), s_longest, bad_offsets ? 0 : hi - lo};
+    // this bin's share of the totals (atomics that return nothing), then the count
+    if (status == PSEQ_ERR_VALUE) atomicOr(&a.hdr->flags, 1u);
+    else if (status == PSEQ_ERR_CAPACITY) atomicOr(&a.hdr->flags, 2u);
+    if (s_longest) atomicMax(&a.hdr->longest, (unsigned)s_longest);
+    atomicMax(&a.hdr->widest, (unsigned)min(total_pad, (long long)INT32_MAX));
     ticket = inc_acq_rel(&a.hdr->finished, (unsigned)a.num_bins - 1u);
   }
   auto finish = [&]() {
     if (!first) return;
     if (tid == 0) s_last = ticket == (unsigned)a.num_bins - 1u;
     __syncthreads();
-    if (s_last) fold_records(a);
+    if (s_last && tid == 0) report(a);
   };
   if (status != PSEQ_OK || !a.out) {
     finish();
@@ -473,7 +465,6 @@ extern "C" pseq_status pack_squeeze(const void* src, int64_t N, int64_t W, int32
   a.cup = cu_seqlens_padded;
   a.info = info;
   a.hdr = static_cast<Header*>(workspace);
-  a.rec = reinterpret_cast<BinRec*>(static_cast<unsigned char*>(workspace) + sizeof(Header));
   // 16-byte vectors when every member start, row start and window start
   // falls on a 16-byte boundary of both src and out
   const int64_t eb = elem_bytes;
