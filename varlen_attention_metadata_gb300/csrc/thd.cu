@@ -231,13 +231,17 @@ __device__ __forceinline__ Summary summarize(const MetaArgs& a, const ScanResult
   return s;
 }
 
-__device__ __forceinline__ void write_meta(const MetaArgs& a, const Summary& s) {
-  if (a.cu) a.cu[s.n] = (int32_t)s.cu_last;
-  if (a.cu_padded) a.cu_padded[s.n] = (int32_t)s.T;
-  for (int64_t k = s.n + 1; k < a.cu_pad_to; ++k) {
+// The cu arrays' filler rows [n+1, cu_pad_to), with every thread of the block.
+__device__ __forceinline__ void pad_cu(const MetaArgs& a, const Summary& s) {
+  for (int64_t k = s.n + 1 + threadIdx.x; k < a.cu_pad_to; k += blockDim.x) {
     if (a.cu) a.cu[k] = (int32_t)a.pad_value;
     if (a.cu_padded) a.cu_padded[k] = (int32_t)a.pad_value;
   }
+}
+
+__device__ __forceinline__ void write_meta(const MetaArgs& a, const Summary& s) {
+  if (a.cu) a.cu[s.n] = (int32_t)s.cu_last;
+  if (a.cu_padded) a.cu_padded[s.n] = (int32_t)s.T;
   if (a.pad_between) *a.pad_between = (uint8_t)s.pad_between;
   *a.info = s.status == PSEQ_OK ? pseq_info{PSEQ_OK, s.n, (int32_t)s.longest, (int32_t)s.shown_total}
                                 : pseq_info{s.status, 0, 0, 0};
@@ -431,6 +435,7 @@ __device__ __forceinline__ Summary fused_scan(const MetaArgs& ac, const Tables& 
   __syncthreads();  // the tables and the flags are complete
   const Summary s = summarize(ac, r, *fl, r.n ? t.real[r.n - 1] : 0);
   if (lead && threadIdx.x == 0) write_meta(ac, s);
+  if (lead) pad_cu(ac, s);
   n = r.n;
   return s;
 }
@@ -604,8 +609,9 @@ __global__ void __launch_bounds__(kMetaThreads) thd_meta_kernel(const __grid_con
   };
   const ScanResult r = scan_lengths<kMetaThreads>(a, ws.row_pfx, scratch, &fl, put);
   __syncthreads();  // the flags and the tables are complete
-  if (threadIdx.x != 0) return;
   const Summary s = summarize(a, r, fl, r.n ? ws.seq_real[r.n - 1] : 0);
+  pad_cu(a, s);
+  if (threadIdx.x != 0) return;
   ws.seq_cup[r.n] = (int32_t)s.T;
   write_meta(a, s);
   Header h = {};
