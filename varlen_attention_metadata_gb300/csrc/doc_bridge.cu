@@ -15,7 +15,7 @@
 // One pass.  Every row is cut into chunks of 4096 tokens, one CTA each.  A
 // chunk summarises its tokens -- how many sequences start in it, its last run
 // start, its last sequence start (a commutative join: sum, max, max) -- with
-// a block scan, publishes that summary, and looks back over the chunks
+// warp reductions, publishes that summary, and looks back over the chunks
 // before it in its row for the row prefix (self-validating words, 32
 // predecessors per poll round, stopping at the nearest inclusive prefix,
 // bounded waits).  It then walks its tokens: every run end writes its
@@ -71,12 +71,10 @@ __device__ __forceinline__ Marks join(const Marks& a, const Marks& b) {
   return {a.seqs + b.seqs, max(a.last_run, b.last_run), max(a.last_seq, b.last_seq)};
 }
 
-__device__ __forceinline__ Marks shfl_up(const Marks& v, int d) {
-  return {__shfl_up_sync(~0u, v.seqs, d), __shfl_up_sync(~0u, v.last_run, d), __shfl_up_sync(~0u, v.last_seq, d)};
-}
-
-__device__ __forceinline__ Marks shfl_xor(const Marks& v, int d) {
-  return {__shfl_xor_sync(~0u, v.seqs, d), __shfl_xor_sync(~0u, v.last_run, d), __shfl_xor_sync(~0u, v.last_seq, d)};
+// The join of every lane's marks, in every lane (three warp reductions).
+__device__ __forceinline__ Marks warp_join(const Marks& v) {
+  return {(int)__reduce_add_sync(~0u, (unsigned)v.seqs), __reduce_max_sync(~0u, v.last_run),
+          __reduce_max_sync(~0u, v.last_seq)};
 }
 
 // {valid, seqs, last_run} and {valid, last_seq}; positions -1 ("none") round-
@@ -192,8 +190,7 @@ __device__ __forceinline__ Marks row_prefix(const BridgeArgs& a, const Slot* row
     const unsigned inc_lanes = __ballot_sync(~0u, incl && t >= 0);
     const int stop = inc_lanes ? __ffs(inc_lanes) - 1 : 32;
     if (lane > stop || t < 0) m = {0, -1, -1};
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) m = join(m, shfl_xor(m, d));
+    m = warp_join(m);
     run = join(run, m);
     if (inc_lanes || gave_up) break;
     j -= 32;
@@ -308,30 +305,38 @@ __global__ void __launch_bounds__(kThreads, 4) bridge_kernel(const Id* __restric
   unsigned runs, seqs, nz, pnz;
   const int s0 = ch * kTile + tid * kItems;
   const Marks mine = chunk_flags(d, S, s0, runs, seqs, nz, pnz);
-  // exclusive block scan of the marks, in token order
-  Marks inc = mine;
-#pragma unroll
-  for (int dd = 1; dd < 32; dd <<= 1) {
-    const Marks o = shfl_up(inc, dd);
-    if (lane >= dd) inc = join(o, inc);
+  // The join is commutative (sum, max, max): each warp's marks are three
+  // warp reductions, the chunk's are those of the warps' (one barrier).
+  {
+    const Marks w = warp_join(mine);
+    if (lane == 0) s_warp[warp] = w;
   }
-  if (lane == 31) s_warp[warp] = inc;
   __syncthreads();
-  if (warp == 0) {
-    Marks w = lane < kThreads / 32 ? s_warp[lane] : Marks{0, -1, -1};
+  Marks chunk_sum = {0, -1, -1}, wpre = {0, -1, -1};
 #pragma unroll
-    for (int dd = 1; dd < kThreads / 32; dd <<= 1) {
-      const Marks o = shfl_up(w, dd);
-      if (lane >= dd) w = join(o, w);
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const Marks m = s_warp[w];
+    chunk_sum = join(chunk_sum, m);
+    if (w < warp) wpre = join(wpre, m);
+  }
+  // marks of the chunk's tokens before this thread's (the row prefix joins
+  // later): the sequence starts of the lanes before it, and the last run and
+  // sequence starts of the nearest lanes before it that have one
+  Marks before;
+  {
+    int c = mine.seqs;
+#pragma unroll
+    for (int dd = 1; dd < 32; dd <<= 1) {
+      const int o = __shfl_up_sync(~0u, c, dd);
+      if (lane >= dd) c += o;
     }
-    if (lane < kThreads / 32) s_warp[lane] = w;
+    const unsigned below = (1u << lane) - 1u;
+    const unsigned rb = __ballot_sync(~0u, mine.last_run >= 0) & below;
+    const unsigned sb = __ballot_sync(~0u, mine.last_seq >= 0) & below;
+    const int lr = __shfl_sync(~0u, mine.last_run, rb ? 31 - __clz(rb) : 0);
+    const int ls = __shfl_sync(~0u, mine.last_seq, sb ? 31 - __clz(sb) : 0);
+    before = join(wpre, Marks{c - mine.seqs, rb ? lr : -1, sb ? ls : -1});
   }
-  __syncthreads();
-  const Marks chunk_sum = s_warp[kThreads / 32 - 1];
-  // marks of the chunk's tokens before this thread's (the row prefix joins later)
-  Marks before = shfl_up(inc, 1);
-  if (lane == 0) before = {0, -1, -1};
-  if (warp > 0) before = join(s_warp[warp - 1], before);
   // Positions after the chunk's first run start do not depend on the row
   // prefix: write them now, while warp 0 looks back.  Only the pairs before
   // this thread's first known run start wait for the prefix.
