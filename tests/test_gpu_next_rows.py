@@ -223,6 +223,20 @@ def test_bridge_random(kind):
     check_bridge(d, 4)  # rows hold more sequences than slots
 
 
+def test_bridge_overflow_with_many_chunks():
+    """Rows of several 4096-token chunks holding more sequences than slots:
+    the walk writes only the slots that exist, the row's fill CTA has
+    nothing to fill, and the call reports PSEQ_ERR_CAPACITY; with exactly as
+    many slots as the fullest row needs it is exact."""
+    rng = np.random.default_rng(37)
+    for kind in ("runs", "iid", "alternating"):
+        d = synth.random_doc_ids(rng, 3, 5 * 4096 + 77, kind, np.int32)
+        check_bridge(d, 16)
+        ref = oracle.doc_ids_to_lengths(d, d.shape[1])
+        need = int((ref["seq_lens"] != -1000).sum(axis=1).max())
+        check_bridge(d, need)
+
+
 def test_bridge_extreme_values():
     # non-zero ids whose low 32 bits are zero are documents, not padding;
     # negative ids and the type's limits are documents too
