@@ -309,7 +309,9 @@ def check_split(batch_np: dict, num_chunks: int, hidden=None, absorb=True):
         np.testing.assert_array_equal(row[: n + 1], meta["cu_seqlens"])
         assert np.all(row[n + 1:] == -1000)
         if padded is not None:
-            np.testing.assert_array_equal(r["cu_seqlens_padded"][c, : n + 1].cpu().numpy(), meta["cu_seqlens_padded"])
+            rowp = r["cu_seqlens_padded"][c].cpu().numpy()
+            np.testing.assert_array_equal(rowp[: n + 1], meta["cu_seqlens_padded"])
+            assert np.all(rowp[n + 1:] == -1000)
         assert bool(r["pad_between"][c].item()) == meta["pad_between_seqs"]
         for (a, planes), (dst, _, rowshape) in zip(fields_np, r["dst"]):
             sub = a[:, sl] if planes > 1 else a[sl]
