@@ -55,6 +55,11 @@ MUTANTS = [
     ("o8_pad_not_absorbed", "        seq_lens_padded[b * num_packs + slot] += 1;\n      }\n    }",
      "      }\n    }"),
     ("o8_positions_not_reset", "          position_ids[t] = 0;\n        } else {", "          position_ids[t] = s;\n        } else {"),
+    ("o8_positions_start_at_one", "          position_ids[t] = 0;\n        } else {", "          position_ids[t] = 1;\n        } else {"),
+    ("o8_real_counts_pad", "        seq_lens_padded[b * num_packs + slot] += 1;\n      }\n    }",
+     "        seq_lens_padded[b * num_packs + slot] += 1;\n        seq_lens[b * num_packs + slot] += 1;\n      }\n    }"),
+    ("o5_real_slots_masked", "        mask[b * width + t] = 0;", "        mask[b * width + t] = 1;"),
+    ("o2_offset_ignored", "      seq_off[n] = offset_in_row;", "      seq_off[n] = 0;"),
     ("o8_leading_pad_dropped", "          slot = 0;\n          if (slot >= num_packs) return ORC_CAPACITY;\n          seq_lens[b * num_packs] = 0;\n          seq_lens_padded[b * num_packs] = 0;\n        }\n        seq_lens_padded[b * num_packs + slot] += 1;",
      "          continue;\n        }\n        seq_lens_padded[b * num_packs + slot] += 1;"),
 ]
