@@ -138,6 +138,17 @@ def test_doc_ids_long_lookback():
     check_doc_ids(synth.random_doc_ids(rng, 4, 2_200_001, "runs", np.int32))
 
 
+@pytest.mark.parametrize("tiles", [1, 2, 128, 129, 130])
+def test_doc_ids_tile_and_round_boundaries(tiles):
+    """Maps that end exactly on a tile, one token short of one and one token
+    into the next; 128 to 130 tiles put the last tiles at the edge of one
+    look-back round (128 predecessors per round)."""
+    rng = np.random.default_rng(tiles)
+    for n in (tiles * 16384 - 1, tiles * 16384, tiles * 16384 + 1):
+        B = 2 if n % 2 == 0 else 1
+        check_doc_ids(synth.random_doc_ids(rng, B, n // B, "runs", np.int32))
+
+
 def test_doc_ids_empty():
     v = V()
     for shape in ((0, 5), (4, 0)):
@@ -438,6 +449,20 @@ def test_thd_large_tables_two_kernel_path():
     hidden = torch.randn(B, S, 24, device=DEV).to(torch.bfloat16)
     check_thd(batch, hidden=hidden)
     check_thd(batch, absorb=False, with_padded=False)
+
+
+@pytest.mark.parametrize("B,P", [(32, 64), (41, 50), (2049, 1)])
+def test_thd_at_the_one_launch_table_limit(B, P):
+    """Tables of exactly 2048 entries (the one-launch kernel's limit) and of
+    2049 and 2050 (the metadata kernel and the gather)."""
+    rng = np.random.default_rng(B * 1000 + P)
+    S = 96
+    real, padded = synth.random_thd(rng, B, S, P, multiple=4, interleave_filler=True)
+    batch = {"input_ids": rng.integers(0, 32000, size=(B, S)).astype(np.int64),
+             "labels": rng.integers(0, 32000, size=(B, S)).astype(np.int64),
+             "seq_lens": real, "seq_lens_padded": padded}
+    check_thd(batch)
+    check_thd(batch, absorb=False)
 
 
 def test_thd_many_planes_use_block_copies():
