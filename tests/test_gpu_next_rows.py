@@ -223,6 +223,17 @@ def test_bridge_random(kind):
     check_bridge(d, 4)  # rows hold more sequences than slots
 
 
+@pytest.mark.parametrize("chunks", [1, 2, 9])
+def test_bridge_chunk_boundaries(chunks):
+    """Rows ending one token before, on and one token after a chunk boundary
+    (4096 tokens a chunk), so the last chunk is full, nearly empty or one
+    token long, and the row's fill CTA follows 1, 2 or 9 chunks."""
+    rng = np.random.default_rng(41 + chunks)
+    for S in (chunks * 4096 - 1, chunks * 4096, chunks * 4096 + 1):
+        for kind in ("runs", "alternating"):
+            check_bridge(synth.random_doc_ids(rng, 3, S, kind, np.int32), S)
+
+
 def test_bridge_overflow_with_many_chunks():
     """Rows of several 4096-token chunks holding more sequences than slots:
     the walk writes only the slots that exist, the row's fill CTA has
